@@ -1,0 +1,431 @@
+"""Benchmark: MoE dispatch + combine on one GB300 (or N replicas).
+
+One step = the whole hot path on one batch: dispatch layout + FP8 dispatch
+(one ep_dispatch call: layout kernel, then the fused cast/scatter kernel) and
+the BF16 weighted combine (ep_combine), on the low-latency workload
+R=32 virtual ranks x 128 tokens, H=7168, E=256 experts, top-8, padded
+per-expert buffers.  Inputs are resident in HBM; L2 is flushed (a write of
+twice its size) between steps, outside the timed events.
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead.
+Multi-GPU (torchrun): every rank runs its own replica of the workload; the
+time is the max over ranks and the value is all ranks' tokens over it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine µs/call, tokens/s and % HBM roofline (h7168 top-8 FP8, 1×GB300)"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
+COMBINE_SRC = os.path.join(ROOT, "combine_get_dispatch_02_gb300", "csrc", "combine.cu")
+DISPATCH_SRC = os.path.join(ROOT, "combine_get_dispatch_02_gb300", "csrc", "dispatch.cu")
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="ll")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def _traffic(kernel: str, src: str, workload: str):
+    """ncu DRAM bytes per launch recorded for this kernel source and workload,
+    or None when none was recorded for the current source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    h = _sha(src)
+    for line in open(TRAFFIC_FILE):
+        parts = line.split("#", 1)[0].split()
+        if len(parts) == 4 and parts[0] == kernel and parts[1] == workload and parts[2] == h:
+            return int(parts[3])
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampler running during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.out.name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def _oracle_sample_step(w, d, ye, tokens):
+    """One oracle step on a token sample: the full layout, then FP8 dispatch
+    and combine of the sampled tokens."""
+    import oracle
+    o = oracle.layout(d["topk_idx"], w.num_experts, w.max_tokens_per_rank, oracle.LAYOUT_PADDED)
+    x2 = d["x_bits"].reshape(w.num_tokens, w.hidden)
+    sl = o["slot"][tokens]
+    # dispatch rows of the sample into a compact buffer (row j*K + k)
+    compact = np.arange(len(tokens) * w.topk, dtype=np.int32).reshape(len(tokens), w.topk)
+    compact = np.where(sl >= 0, compact, -1).astype(np.int32)
+    oracle.dispatch(x2[tokens], compact, len(tokens) * w.topk, True)
+    oracle.combine(ye.reshape(-1, w.hidden), compact, d["topk_weights"].reshape(w.num_tokens, -1)[tokens])
+
+
+def cpu_baseline(w, seconds: float, sample_tokens: int):
+    import oracle
+    oracle.build()
+    from combine_get_dispatch_02_gb300 import workloads as wl
+    d = wl.generate(w)
+    tokens = np.arange(min(sample_tokens, w.num_tokens))
+    ye = wl.expert_outputs(w, tokens)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_sample_step(w, d, ye, tokens)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": n * len(tokens) / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} oracle steps of {len(tokens)} of the {w.num_tokens} tokens "
+                      f"(full layout each step, FP8 dispatch + combine of the sample), "
+                      f"{el:.1f} s single-threaded"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from combine_get_dispatch_02_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    d = wl.generate(w)
+    # bounded sample per step so that warmup + steps finish in about two minutes
+    import oracle
+    oracle.build()
+    probe_tokens = np.arange(16)
+    ye16 = wl.expert_outputs(w, probe_tokens)
+    t0 = time.perf_counter()
+    _oracle_sample_step(w, d, ye16, probe_tokens)
+    per_token = max((time.perf_counter() - t0) / 16, 1e-6)
+    budget = 120.0 / max(args.steps + args.warmup, 1)
+    ntok = int(max(1, min(w.num_tokens, budget / per_token)))
+    tokens = np.arange(ntok)
+    ye = wl.expert_outputs(w, tokens)
+    for _ in range(args.warmup):
+        _oracle_sample_step(w, d, ye, tokens)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_sample_step(w, d, ye, tokens)
+    el = time.perf_counter() - t0
+    value = args.steps * ntok / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": _workload_desc(w), "sample_tokens_per_step": ntok},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: full layout + FP8 dispatch and combine of {ntok} "
+                                   f"of {w.num_tokens} tokens, single-threaded C oracle"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _workload_desc(w):
+    return (f"{w.name}: R={w.num_ranks} virtual ranks x {w.tokens_per_rank} tokens, H={w.hidden}, "
+            f"E={w.num_experts}, top-{w.topk}, {'FP8 e4m3 (per-128 fp32 scales)' if w.use_fp8 else 'BF16'} "
+            f"dispatch into {w.layout} receive buffers, BF16 combine")
+
+
+# ------------------------------------------------------------------ GPU
+
+def _algorithmic_bytes(w, M):
+    N, K, H = w.num_tokens, w.topk, w.hidden
+    pay = 1 if w.use_fp8 else 2
+    disp = N * H * 2 + N * K * 8 + M * H * pay + (M * (H // 128) * 4 if w.use_fp8 else 0) \
+        + N * K * 4 + M * 4 + w.num_experts * w.num_ranks * 4
+    disp_kernel = N * H * 2 + M * H * pay + (M * (H // 128) * 4 if w.use_fp8 else 0) + N * K * 4
+    comb = M * H * 2 + N * K * 4 + N * K * 4 + N * H * 2
+    return disp, disp_kernel, comb
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    from combine_get_dispatch_02_gb300 import Buffer, ep
+    from combine_get_dispatch_02_gb300 import build as epbuild
+    from combine_get_dispatch_02_gb300 import workloads as wl
+    epbuild.build()
+    w = wl.WORKLOADS[args.workload]
+    d = wl.generate(w)
+    N, K, H = w.num_tokens, w.topk, w.hidden
+
+    buf = Buffer(w.num_ranks, w.max_tokens_per_rank, H, w.num_experts, K,
+                 low_latency_mode=(w.layout == wl.PADDED))
+    to_dev = lambda a: torch.from_numpy(a).cuda()
+    x = to_dev(np.ascontiguousarray(d["x_bits"]).view(np.int16)).view(torch.bfloat16)
+    idx = to_dev(d["topk_idx"])
+    wts = to_dev(d["topk_weights"].reshape(N, K))
+    recv, scales = buf.alloc_recv(w.use_fp8)
+    cnt = torch.empty(w.num_experts, dtype=torch.int32, device="cuda")
+    out = torch.empty(N, H, dtype=torch.bfloat16, device="cuda")
+    h = buf.new_handle()
+    ctx = buf.ctx
+    stream = torch.cuda.current_stream()
+
+    # expert outputs (combine input) at the rows the layout assigns
+    ep.ep_get_dispatch_layout(ctx, idx, w.tokens_per_rank, None, None, None, h.raw)
+    slot = h.tensors()["slot"].view(-1).long()
+    valid = slot >= 0
+    M = int(valid.sum().item())
+    y = torch.zeros(buf.rows, H, dtype=torch.bfloat16, device="cuda")
+    ye = wl.expert_outputs(w)
+    y[slot[valid]] = to_dev(ye.reshape(-1, H).view(np.int16)).view(torch.bfloat16)[valid]
+    del ye
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
+
+    def step():
+        ep.ep_dispatch(ctx, x, idx, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales, cnt, stream)
+        ev_mid = torch.cuda.Event(enable_timing=True)
+        ev_mid.record(stream)
+        ep.ep_combine(ctx, y, wts, h.raw, out, stream)
+        return ev_mid
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if buf.device_status() != ep.EP_OK:
+        raise RuntimeError("device status error during warmup")
+
+    clocks = Clocks(dev)
+    clocks.start()
+    time.sleep(0.3)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e1 = step()
+        e2.record(stream)
+        evs.append((e0, e1, e2))
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    time.sleep(0.2)
+    clk = clocks.stop()
+    disp_ms = [a.elapsed_time(b) for a, b, _ in evs]
+    comb_ms = [b.elapsed_time(c) for _, b, c in evs]
+    step_ms = [a.elapsed_time(c) for a, _, c in evs]
+    total_ms = sum(step_ms)
+    if ws > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = ws * N / (ms_per_step / 1e3)
+
+    # breakdown: each kernel alone (layout alone, dispatch with the cached
+    # layout, combine), same L2 flush between launches
+    def timed(fn, reps=200):
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        v = [a.elapsed_time(b) * 1e3 for a, b in ts]
+        return statistics.median(v), statistics.mean(v)
+
+    lay_us = timed(lambda: ep.ep_get_dispatch_layout(ctx, idx, w.tokens_per_rank, None, None, None, h.raw, stream))
+    disp_us = timed(lambda: ep.ep_dispatch(ctx, x, None, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales,
+                                           None, stream))
+    comb_us = timed(lambda: ep.ep_combine(ctx, y, wts, h.raw, out, stream))
+
+    # end to end through the public API with host buffers
+    xh = torch.from_numpy(np.ascontiguousarray(d["x_bits"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    idxh = torch.from_numpy(d["topk_idx"]).pin_memory()
+    wh = torch.from_numpy(d["topk_weights"].reshape(N, K)).pin_memory()
+    outh = torch.empty(N, H, dtype=torch.bfloat16).pin_memory()
+    for i in range(args.e2e_steps + 3):
+        if i == 3:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            ea = torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+        x.copy_(xh, non_blocking=True)
+        idx.copy_(idxh, non_blocking=True)
+        wts.copy_(wh, non_blocking=True)
+        ep.ep_dispatch(ctx, x, idx, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales, cnt, stream)
+        ep.ep_combine(ctx, y, wts, h.raw, out, stream)
+        outh.copy_(out, non_blocking=True)
+    eb = torch.cuda.Event(enable_timing=True)
+    eb.record(stream)
+    torch.cuda.synchronize()
+    wall = (time.perf_counter() - t0) / args.e2e_steps
+    e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
+    if buf.device_status() != ep.EP_OK:
+        raise RuntimeError("device status error")
+    h2d = xh.numel() * 2 + idxh.numel() * 8 + wh.numel() * 4
+    d2h = outh.numel() * 2
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    peak, peak_kind = _peaks()
+    disp_bytes, disp_kernel_bytes, comb_bytes = _algorithmic_bytes(w, M)
+    comb_avg_s = statistics.mean(comb_ms) / 1e3
+    comb_gbs = comb_bytes / comb_avg_s / 1e9
+    traffic = _traffic("combine", COMBINE_SRC, w.name)
+    disp_avg_s = disp_us[1] / 1e6
+    disp_gbs = disp_kernel_bytes / disp_avg_s / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "payload": {"dispatch": "e4m3 + f32 scales" if w.use_fp8 else "bf16", "combine": "bf16"},
+        "data": "synthetic",
+        "config": {"workload": _workload_desc(w), "tokens_per_step": N, "rows_received": M,
+                   "l2": "flushed between steps (write of 2x L2, outside the timed events)",
+                   "parallelism": f"{ws} replica(s), one per GPU" if ws > 1 else "1 GPU, 32 virtual EP ranks"},
+        "us_per_call": {
+            "step": statistics.mean(step_ms) * 1e3,
+            "dispatch_with_layout": statistics.mean(disp_ms) * 1e3,
+            "combine": statistics.mean(comb_ms) * 1e3,
+            "layout_alone_median": lay_us[0],
+            "dispatch_cached_layout_median": disp_us[0],
+            "combine_alone_median": comb_us[0],
+        },
+        "roofline": {"bound": "hbm", "kernel": "combine", "achieved": comb_gbs, "peak": peak,
+                     "unit": "GB/s", "frac": comb_gbs / peak, "traffic": traffic,
+                     "algorithmic_bytes": comb_bytes, "peak_source": f"{peak_kind} HBM copy bandwidth"},
+        "roofline_dispatch": {"bound": "hbm", "kernel": "dispatch (cached layout)", "achieved": disp_gbs,
+                              "peak": peak, "unit": "GB/s", "frac": disp_gbs / peak,
+                              "traffic": _traffic("dispatch", DISPATCH_SRC, w.name),
+                              "algorithmic_bytes": disp_kernel_bytes},
+        "e2e": {"value": N / (e2e_ms / 1e3) * ws, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step_device": e2e_ms, "ms_per_step_wall": wall * 1e3},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "host_cores": os.cpu_count(),
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, 128)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

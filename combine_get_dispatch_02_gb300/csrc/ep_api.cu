@@ -1,0 +1,358 @@
+// Host side of libep.so: the C ABI declared in include/ep.h — argument checks,
+// context / handle management and kernel launches.  No call here synchronises
+// the host except ep_get_device_status, and none allocates except
+// ep_create / ep_handle_create, so a dispatch + combine sequence can be
+// captured in a CUDA graph.
+#include <stdlib.h>
+#include <string.h>
+
+#include <cuda_runtime.h>
+
+#include "ep.h"
+#include "ep_internal.cuh"
+
+struct ep_ctx {
+    ep_config cfg;
+    int device;
+    int num_sms;
+    int64_t rows;
+    uint32_t *d_status;
+    int layout_cluster;
+    int layout_threads;
+    int dispatch_bps_bf16;
+    int dispatch_bps_fp8;
+    int combine_bps;
+};
+
+struct ep_handle {
+    ep_ctx *ctx;
+    int32_t *slot;
+    int32_t *src_info;
+    int32_t *cnt_er;
+    int32_t *off_er;
+    int64_t *base;
+    int32_t *tokens_per_expert;
+    int32_t tokens_per_rank;  // -1: no layout yet
+};
+
+namespace {
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+ep_status check_config(const ep_config *c) {
+    if (c == nullptr) return EP_ERR_INVALID_ARG;
+    if (c->num_ranks < 1 || c->max_tokens_per_rank < 1 || c->hidden < 1 || c->num_experts < 1 ||
+        c->topk < 1 || c->max_sms < 0)
+        return EP_ERR_INVALID_ARG;
+    if (c->layout != EP_LAYOUT_PADDED && c->layout != EP_LAYOUT_PACKED) return EP_ERR_INVALID_ARG;
+    if (c->num_experts % c->num_ranks != 0) return EP_ERR_INVALID_ARG;
+    if (c->hidden % 8 != 0) return EP_ERR_INVALID_ARG;
+    if (c->num_ranks > 1024 || c->topk > 32 || c->num_experts > 1024 || c->hidden > 65536)
+        return EP_ERR_UNSUPPORTED;
+    if ((int64_t)c->num_experts * c->num_ranks > 16384) return EP_ERR_UNSUPPORTED;
+    const int64_t n = (int64_t)c->num_ranks * c->max_tokens_per_rank;
+    if (n * c->topk >= ((int64_t)1 << 31)) return EP_ERR_UNSUPPORTED;
+    if (c->layout == EP_LAYOUT_PADDED && n * c->num_experts >= ((int64_t)1 << 31))
+        return EP_ERR_UNSUPPORTED;
+    return EP_OK;
+}
+
+int64_t rows_of(const ep_config *c) {
+    const int64_t n = (int64_t)c->num_ranks * c->max_tokens_per_rank;
+    return c->layout == EP_LAYOUT_PADDED ? n * c->num_experts : n * c->topk;
+}
+
+bool on_ctx_device(const ep_ctx *ctx) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return dev == ctx->device;
+}
+
+int grid_cap(const ep_ctx *ctx, int blocks_per_sm) {
+    int sms = ctx->num_sms;
+    if (ctx->cfg.max_sms > 0 && ctx->cfg.max_sms < sms) sms = ctx->cfg.max_sms;
+    return sms * blocks_per_sm;
+}
+
+ep_status enqueue_layout(ep_ctx *ctx, const int64_t *topk_idx, int32_t T, int32_t *tokens_per_rank,
+                         int32_t *user_tokens_per_expert, uint8_t *is_token_in_rank, ep_handle *h,
+                         cudaStream_t stream) {
+    const ep_config &c = ctx->cfg;
+    ep::LayoutParams p;
+    p.topk_idx = topk_idx;
+    p.R = c.num_ranks;
+    p.T = T;
+    p.K = c.topk;
+    p.E = c.num_experts;
+    p.L = c.num_experts / c.num_ranks;
+    p.layout = c.layout;
+    p.N = (int64_t)c.num_ranks * T;
+    p.cap = c.layout == EP_LAYOUT_PADDED ? (int64_t)c.num_ranks * c.max_tokens_per_rank
+                                         : (int64_t)c.num_ranks * c.max_tokens_per_rank * c.topk;
+    p.slot = h->slot;
+    p.src_info = h->src_info;
+    p.cnt_er = h->cnt_er;
+    p.off_er = h->off_er;
+    p.base = h->base;
+    p.tokens_per_expert = h->tokens_per_expert;
+    p.user_tokens_per_expert = user_tokens_per_expert;
+    p.tokens_per_rank = tokens_per_rank;
+    p.is_token_in_rank = is_token_in_rank;
+    p.status = ctx->d_status;
+    if (ep::launch_layout(p, ctx->layout_cluster, ctx->layout_threads, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    h->tokens_per_rank = T;
+    return EP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ep_status_str(int32_t s) {
+    switch (s) {
+        case EP_OK: return "ok";
+        case EP_ERR_INVALID_ARG: return "invalid argument";
+        case EP_ERR_UNSUPPORTED: return "unsupported size";
+        case EP_ERR_OOM: return "device allocation failed";
+        case EP_ERR_CUDA: return "CUDA error";
+        case EP_ERR_BAD_EXPERT: return "expert id outside [-1, num_experts)";
+        case EP_ERR_CAPACITY: return "padded expert buffer overflow";
+        case EP_ERR_NO_LAYOUT: return "handle holds no layout for these sizes";
+        default: return "unknown status";
+    }
+}
+
+ep_status ep_config_check(const ep_config *cfg) { return check_config(cfg); }
+
+ep_status ep_recv_rows(const ep_config *cfg, int64_t *rows) {
+    const ep_status s = check_config(cfg);
+    if (s != EP_OK) return s;
+    if (rows == nullptr) return EP_ERR_INVALID_ARG;
+    *rows = rows_of(cfg);
+    return EP_OK;
+}
+
+ep_status ep_recv_bytes(const ep_config *cfg, int32_t use_fp8, uint64_t *payload_bytes,
+                        uint64_t *scale_bytes) {
+    const ep_status s = check_config(cfg);
+    if (s != EP_OK) return s;
+    if (payload_bytes == nullptr) return EP_ERR_INVALID_ARG;
+    if (use_fp8 && cfg->hidden % 128 != 0) return EP_ERR_UNSUPPORTED;
+    const uint64_t rows = (uint64_t)rows_of(cfg);
+    *payload_bytes = rows * (uint64_t)cfg->hidden * (use_fp8 ? 1u : 2u);
+    if (scale_bytes) *scale_bytes = use_fp8 ? rows * (uint64_t)(cfg->hidden / 128) * 4u : 0u;
+    return EP_OK;
+}
+
+ep_status ep_create(const ep_config *cfg, ep_ctx **out) {
+    if (out == nullptr) return EP_ERR_INVALID_ARG;
+    *out = nullptr;
+    const ep_status s = check_config(cfg);
+    if (s != EP_OK) return s;
+    ep_ctx *ctx = (ep_ctx *)calloc(1, sizeof(ep_ctx));
+    if (ctx == nullptr) return EP_ERR_OOM;
+    ctx->cfg = *cfg;
+    ctx->rows = rows_of(cfg);
+    if (cudaGetDevice(&ctx->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess) {
+        cudaGetLastError();
+        free(ctx);
+        return EP_ERR_CUDA;
+    }
+    if (!ep::layout_pick_shape(cfg->num_experts, cfg->num_ranks, &ctx->layout_cluster, &ctx->layout_threads)) {
+        free(ctx);
+        return EP_ERR_UNSUPPORTED;
+    }
+    ctx->dispatch_bps_bf16 = ep::dispatch_blocks_per_sm(false);
+    ctx->dispatch_bps_fp8 = ep::dispatch_blocks_per_sm(true);
+    ctx->combine_bps = ep::combine_blocks_per_sm();
+    if (cudaMalloc(&ctx->d_status, sizeof(uint32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        free(ctx);
+        return EP_ERR_OOM;
+    }
+    if (cudaMemset(ctx->d_status, 0, sizeof(uint32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(ctx->d_status);
+        free(ctx);
+        return EP_ERR_CUDA;
+    }
+    *out = ctx;
+    return EP_OK;
+}
+
+ep_status ep_destroy(ep_ctx *ctx) {
+    if (ctx == nullptr) return EP_ERR_INVALID_ARG;
+    cudaFree(ctx->d_status);
+    free(ctx);
+    return EP_OK;
+}
+
+ep_status ep_handle_create(ep_ctx *ctx, ep_handle **out) {
+    if (ctx == nullptr || out == nullptr) return EP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    const ep_config &c = ctx->cfg;
+    ep_handle *h = (ep_handle *)calloc(1, sizeof(ep_handle));
+    if (h == nullptr) return EP_ERR_OOM;
+    h->ctx = ctx;
+    h->tokens_per_rank = -1;
+    const size_t nk = (size_t)c.num_ranks * c.max_tokens_per_rank * c.topk;
+    const size_t er = (size_t)c.num_experts * c.num_ranks;
+    bool ok = cudaMalloc(&h->slot, nk * sizeof(int32_t)) == cudaSuccess &&
+              cudaMalloc(&h->src_info, (size_t)ctx->rows * sizeof(int32_t)) == cudaSuccess &&
+              cudaMalloc(&h->cnt_er, er * sizeof(int32_t)) == cudaSuccess &&
+              cudaMalloc(&h->off_er, er * sizeof(int32_t)) == cudaSuccess &&
+              cudaMalloc(&h->base, (size_t)c.num_experts * sizeof(int64_t)) == cudaSuccess &&
+              cudaMalloc(&h->tokens_per_expert, (size_t)c.num_experts * sizeof(int32_t)) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        ep_handle_destroy(h);
+        return EP_ERR_OOM;
+    }
+    *out = h;
+    return EP_OK;
+}
+
+ep_status ep_handle_destroy(ep_handle *h) {
+    if (h == nullptr) return EP_ERR_INVALID_ARG;
+    cudaFree(h->slot);
+    cudaFree(h->src_info);
+    cudaFree(h->cnt_er);
+    cudaFree(h->off_er);
+    cudaFree(h->base);
+    cudaFree(h->tokens_per_expert);
+    free(h);
+    return EP_OK;
+}
+
+ep_status ep_handle_get_info(const ep_handle *h, ep_handle_info *out) {
+    if (h == nullptr || out == nullptr) return EP_ERR_INVALID_ARG;
+    out->tokens_per_rank = h->tokens_per_rank;
+    out->num_tokens = h->tokens_per_rank < 0 ? 0 : h->tokens_per_rank * h->ctx->cfg.num_ranks;
+    out->rows = h->ctx->rows;
+    out->slot = h->slot;
+    out->src_info = h->src_info;
+    out->cnt_er = h->cnt_er;
+    out->off_er = h->off_er;
+    out->base = h->base;
+    out->tokens_per_expert = h->tokens_per_expert;
+    return EP_OK;
+}
+
+ep_status ep_get_dispatch_layout(ep_ctx *ctx, const int64_t *d_topk_idx, int32_t tokens_per_rank,
+                                 int32_t *d_num_tokens_per_rank, int32_t *d_num_tokens_per_expert,
+                                 uint8_t *d_is_token_in_rank, ep_handle *handle, void *stream) {
+    if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
+    if (tokens_per_rank < 0 || tokens_per_rank > ctx->cfg.max_tokens_per_rank) return EP_ERR_INVALID_ARG;
+    if (d_topk_idx == nullptr && tokens_per_rank > 0) return EP_ERR_INVALID_ARG;
+    if (!aligned(d_topk_idx, 8) || !aligned(d_num_tokens_per_rank, 4) || !aligned(d_num_tokens_per_expert, 4))
+        return EP_ERR_INVALID_ARG;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    return enqueue_layout(ctx, d_topk_idx, tokens_per_rank, d_num_tokens_per_rank, d_num_tokens_per_expert,
+                          d_is_token_in_rank, handle, (cudaStream_t)stream);
+}
+
+ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, int32_t tokens_per_rank,
+                      int32_t use_fp8, ep_handle *handle, void *d_recv_x, float *d_recv_scales,
+                      int32_t *d_recv_count, void *stream) {
+    if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
+    const ep_config &c = ctx->cfg;
+    if (tokens_per_rank < 0 || tokens_per_rank > c.max_tokens_per_rank) return EP_ERR_INVALID_ARG;
+    if (use_fp8 != 0 && use_fp8 != 1) return EP_ERR_INVALID_ARG;
+    if (use_fp8 && c.hidden % 128 != 0) return EP_ERR_UNSUPPORTED;
+    const int64_t N = (int64_t)c.num_ranks * tokens_per_rank;
+    if (N > 0 && (d_x == nullptr || d_recv_x == nullptr || (use_fp8 && d_recv_scales == nullptr)))
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(d_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_recv_scales, 4) ||
+        !aligned(d_recv_count, 4) || !aligned(d_topk_idx, 8))
+        return EP_ERR_INVALID_ARG;
+    if (d_topk_idx == nullptr && tokens_per_rank > 0 && handle->tokens_per_rank != tokens_per_rank)
+        return EP_ERR_NO_LAYOUT;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+
+    // With no tokens there is nothing to read: an (empty) layout is computed
+    // even when d_topk_idx is NULL.
+    const bool fresh = d_topk_idx != nullptr || tokens_per_rank == 0;
+    if (fresh) {
+        const ep_status s = enqueue_layout(ctx, d_topk_idx, tokens_per_rank, nullptr, d_recv_count, nullptr,
+                                           handle, st);
+        if (s != EP_OK) return s;
+    }
+    if (N == 0) {
+        if (!fresh && d_recv_count != nullptr &&
+            cudaMemcpyAsync(d_recv_count, handle->tokens_per_expert, (size_t)c.num_experts * sizeof(int32_t),
+                            cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
+            cudaGetLastError();
+            return EP_ERR_CUDA;
+        }
+        return EP_OK;
+    }
+    ep::DispatchParams p;
+    p.x = d_x;
+    p.slot = handle->slot;
+    p.recv = d_recv_x;
+    p.recv_scales = d_recv_scales;
+    p.N = N;
+    p.K = c.topk;
+    p.H = c.hidden;
+    p.count_src = handle->tokens_per_expert;
+    p.count_dst = fresh ? nullptr : d_recv_count;
+    p.E = c.num_experts;
+    const int cap = grid_cap(ctx, use_fp8 ? ctx->dispatch_bps_fp8 : ctx->dispatch_bps_bf16);
+    if (ep::launch_dispatch(p, use_fp8 != 0, cap, /*pdl=*/true, st) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    return EP_OK;
+}
+
+ep_status ep_combine(ep_ctx *ctx, const void *d_y, const float *d_topk_weights, const ep_handle *handle,
+                     void *d_out, void *stream) {
+    if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
+    if (handle->tokens_per_rank < 0) return EP_ERR_NO_LAYOUT;
+    const ep_config &c = ctx->cfg;
+    const int64_t N = (int64_t)c.num_ranks * handle->tokens_per_rank;
+    if (N == 0) return EP_OK;
+    if (d_y == nullptr || d_out == nullptr) return EP_ERR_INVALID_ARG;
+    if (!aligned(d_y, 16) || !aligned(d_out, 16) || !aligned(d_topk_weights, 4)) return EP_ERR_INVALID_ARG;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    ep::CombineParams p;
+    p.y = d_y;
+    p.weights = d_topk_weights;
+    p.slot = handle->slot;
+    p.out = d_out;
+    p.N = N;
+    p.K = c.topk;
+    p.H = c.hidden;
+    if (ep::launch_combine(p, grid_cap(ctx, ctx->combine_bps), /*pdl=*/true, (cudaStream_t)stream) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    return EP_OK;
+}
+
+ep_status ep_get_device_status(ep_ctx *ctx, void *stream) {
+    if (ctx == nullptr) return EP_ERR_INVALID_ARG;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    uint32_t bits = 0;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess ||
+        cudaMemcpy(&bits, ctx->d_status, sizeof bits, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(ctx->d_status, 0, sizeof bits) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    if (bits & ep::kStatusBadExpert) return EP_ERR_BAD_EXPERT;
+    if (bits & ep::kStatusCapacity) return EP_ERR_CAPACITY;
+    return EP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// Internal declarations shared by the libep translation units: kernel
+// parameter blocks, launchers and small device helpers.  Not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ep {
+
+// Bits of the per-context device status word.
+constexpr uint32_t kStatusBadExpert = 1u;  // topk_idx entry outside [-1, E)
+constexpr uint32_t kStatusCapacity = 2u;   // padded expert buffer offered > R*Tmax entries
+
+constexpr int kLayoutPadded = 0;
+constexpr int kLayoutPacked = 1;
+
+// ------------------------------------------------------------------ layout
+struct LayoutParams {
+    const int64_t *topk_idx;   // [N*K]
+    int32_t R, T, K, E, L;     // L = E / R
+    int32_t layout;
+    int64_t N;                 // R*T
+    int64_t cap;               // rows per expert buffer (padded) or N*K (packed)
+    int32_t *slot;             // [N*K]
+    int32_t *src_info;         // [rows]
+    int32_t *cnt_er;           // [E*R]
+    int32_t *off_er;           // [E*R]
+    int64_t *base;             // [E]
+    int32_t *tokens_per_expert;       // [E] (handle)
+    int32_t *user_tokens_per_expert;  // [E] or nullptr
+    int32_t *tokens_per_rank;         // [R] or nullptr
+    uint8_t *is_token_in_rank;        // [N*R] or nullptr
+    uint32_t *status;
+};
+
+// Launch the single-cluster layout kernel.  cluster_size / threads come from
+// layout_pick_shape.  Returns the launch error.
+cudaError_t launch_layout(const LayoutParams &p, int cluster_size, int threads,
+                          cudaStream_t stream);
+// Dynamic shared memory the layout kernel needs for these sizes.
+size_t layout_smem_bytes(int E, int R, int threads, int cluster_size);
+// Largest cluster size (16, 8, 4, 2 or 1) and thread count the device can run
+// for these sizes; false if none fits.
+bool layout_pick_shape(int E, int R, int *cluster_size, int *threads);
+
+// ------------------------------------------------------------------ dispatch
+struct DispatchParams {
+    const void *x;             // bf16 [N, H]
+    const int32_t *slot;       // [N*K]
+    void *recv;                // bf16 or e4m3 [rows, H]
+    float *recv_scales;        // [rows, H/128] (FP8)
+    int64_t N;
+    int32_t K, H;
+    const int32_t *count_src;  // [E] copied to count_dst by block 0, or nullptr
+    int32_t *count_dst;
+    int32_t E;
+};
+
+cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks,
+                            bool pdl, cudaStream_t stream);
+// Resident blocks per SM of the dispatch kernel (for grid sizing).
+int dispatch_blocks_per_sm(bool fp8);
+
+// ------------------------------------------------------------------ combine
+struct CombineParams {
+    const void *y;             // bf16 [rows, H]
+    const float *weights;      // [N*K] or nullptr (all ones)
+    const int32_t *slot;       // [N*K]
+    void *out;                 // bf16 [N, H]
+    int64_t N;
+    int32_t K, H;
+};
+
+cudaError_t launch_combine(const CombineParams &p, int max_blocks, bool pdl,
+                           cudaStream_t stream);
+int combine_blocks_per_sm();
+
+// ------------------------------------------------------------------ device helpers
+#ifdef __CUDACC__
+// Programmatic dependent launch: let the next kernel in the stream start, and
+// wait for the previous one's results.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// 16-byte read-only load that does not allocate in L1 (the buffer is not
+// written while the kernel runs).
+__device__ __forceinline__ uint4 ld_nc_na_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// 16-byte streaming store (evict-first): the written rows are not read again
+// by this kernel.
+__device__ __forceinline__ void st_cs_v4(void *p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// bf16 pair (low half = first element) -> two floats, exactly.
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+#endif
+
+}  // namespace ep

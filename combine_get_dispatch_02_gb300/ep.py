@@ -1,0 +1,204 @@
+"""Thin Python binding of libep.so: the C ABI of include/ep.h, one Python
+function per C entry point with the same name, marshalling torch tensors to
+device pointers.  Every step of the computation runs in libep.so's kernels;
+this module only checks shapes / dtypes and passes pointers.
+
+The library must have been built (``python -m combine_get_dispatch_02_gb300.build``
+or ``__graft_entry__.build()``); loading fails loudly otherwise.  There is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libep.so")
+
+EP_OK = 0
+EP_ERR_INVALID_ARG = 1
+EP_ERR_UNSUPPORTED = 2
+EP_ERR_OOM = 3
+EP_ERR_CUDA = 4
+EP_ERR_BAD_EXPERT = 5
+EP_ERR_CAPACITY = 6
+EP_ERR_NO_LAYOUT = 7
+
+EP_LAYOUT_PADDED = 0
+EP_LAYOUT_PACKED = 1
+
+# Every entry point include/ep.h declares (checked against the header and the
+# library by the tests).
+ENTRY_POINTS = (
+    "ep_status_str", "ep_config_check", "ep_recv_rows", "ep_recv_bytes",
+    "ep_create", "ep_destroy", "ep_handle_create", "ep_handle_destroy",
+    "ep_handle_get_info", "ep_get_dispatch_layout", "ep_dispatch", "ep_combine",
+    "ep_get_device_status",
+)
+
+
+class EPError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_str(status)} (status {status})")
+
+
+class ep_config(ctypes.Structure):
+    _fields_ = [("num_ranks", ctypes.c_int32), ("max_tokens_per_rank", ctypes.c_int32),
+                ("hidden", ctypes.c_int32), ("num_experts", ctypes.c_int32),
+                ("topk", ctypes.c_int32), ("layout", ctypes.c_int32),
+                ("max_sms", ctypes.c_int32)]
+
+
+class ep_handle_info(ctypes.Structure):
+    _fields_ = [("tokens_per_rank", ctypes.c_int32), ("num_tokens", ctypes.c_int32),
+                ("rows", ctypes.c_int64), ("slot", ctypes.c_void_p),
+                ("src_info", ctypes.c_void_p), ("cnt_er", ctypes.c_void_p),
+                ("off_er", ctypes.c_void_p), ("base", ctypes.c_void_p),
+                ("tokens_per_expert", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libep.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                               "`python -m combine_get_dispatch_02_gb300.build`")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        CFG = ctypes.POINTER(ep_config)
+        sig = {
+            "ep_status_str": (ctypes.c_char_p, [I32]),
+            "ep_config_check": (I32, [CFG]),
+            "ep_recv_rows": (I32, [CFG, ctypes.POINTER(I64)]),
+            "ep_recv_bytes": (I32, [CFG, I32, ctypes.POINTER(ctypes.c_uint64),
+                                    ctypes.POINTER(ctypes.c_uint64)]),
+            "ep_create": (I32, [CFG, ctypes.POINTER(P)]),
+            "ep_destroy": (I32, [P]),
+            "ep_handle_create": (I32, [P, ctypes.POINTER(P)]),
+            "ep_handle_destroy": (I32, [P]),
+            "ep_handle_get_info": (I32, [P, ctypes.POINTER(ep_handle_info)]),
+            "ep_get_dispatch_layout": (I32, [P, P, I32, P, P, P, P, P]),
+            "ep_dispatch": (I32, [P, P, P, I32, I32, P, P, P, P, P]),
+            "ep_combine": (I32, [P, P, P, P, P, P]),
+            "ep_get_device_status": (I32, [P, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().ep_status_str(status).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != EP_OK:
+        raise EPError(status, where)
+
+
+def _ptr(t: torch.Tensor | None, dtype: torch.dtype | None = None, name: str = "tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_config(num_ranks, max_tokens_per_rank, hidden, num_experts, topk,
+                layout=EP_LAYOUT_PADDED, max_sms=0) -> ep_config:
+    return ep_config(num_ranks, max_tokens_per_rank, hidden, num_experts, topk, layout, max_sms)
+
+
+# ------------------------------------------------------------- entry points
+
+def ep_config_check(cfg: ep_config) -> int:
+    return lib().ep_config_check(ctypes.byref(cfg))
+
+
+def ep_recv_rows(cfg: ep_config) -> int:
+    rows = ctypes.c_int64()
+    _check(lib().ep_recv_rows(ctypes.byref(cfg), ctypes.byref(rows)), "ep_recv_rows")
+    return rows.value
+
+
+def ep_recv_bytes(cfg: ep_config, use_fp8: bool) -> tuple[int, int]:
+    pb, sb = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(lib().ep_recv_bytes(ctypes.byref(cfg), int(use_fp8), ctypes.byref(pb), ctypes.byref(sb)),
+           "ep_recv_bytes")
+    return pb.value, sb.value
+
+
+def ep_create(cfg: ep_config) -> ctypes.c_void_p:
+    ctx = ctypes.c_void_p()
+    _check(lib().ep_create(ctypes.byref(cfg), ctypes.byref(ctx)), "ep_create")
+    return ctx
+
+
+def ep_destroy(ctx) -> None:
+    _check(lib().ep_destroy(ctx), "ep_destroy")
+
+
+def ep_handle_create(ctx) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    _check(lib().ep_handle_create(ctx, ctypes.byref(h)), "ep_handle_create")
+    return h
+
+
+def ep_handle_destroy(h) -> None:
+    _check(lib().ep_handle_destroy(h), "ep_handle_destroy")
+
+
+def ep_handle_get_info(h) -> ep_handle_info:
+    info = ep_handle_info()
+    _check(lib().ep_handle_get_info(h, ctypes.byref(info)), "ep_handle_get_info")
+    return info
+
+
+def ep_get_dispatch_layout(ctx, topk_idx: torch.Tensor | None, tokens_per_rank: int,
+                           num_tokens_per_rank: torch.Tensor | None,
+                           num_tokens_per_expert: torch.Tensor | None,
+                           is_token_in_rank: torch.Tensor | None, handle, stream=None) -> None:
+    _check(lib().ep_get_dispatch_layout(
+        ctx, _ptr(topk_idx, torch.int64, "topk_idx"), int(tokens_per_rank),
+        _ptr(num_tokens_per_rank, torch.int32, "num_tokens_per_rank"),
+        _ptr(num_tokens_per_expert, torch.int32, "num_tokens_per_expert"),
+        _ptr(is_token_in_rank, None, "is_token_in_rank"), handle, _stream(stream)),
+        "ep_get_dispatch_layout")
+
+
+def ep_dispatch(ctx, x: torch.Tensor, topk_idx: torch.Tensor | None, tokens_per_rank: int,
+                use_fp8: bool, handle, recv_x: torch.Tensor, recv_scales: torch.Tensor | None,
+                recv_count: torch.Tensor | None, stream=None) -> None:
+    _check(lib().ep_dispatch(
+        ctx, _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int64, "topk_idx"),
+        int(tokens_per_rank), int(bool(use_fp8)), handle, _ptr(recv_x, None, "recv_x"),
+        _ptr(recv_scales, torch.float32, "recv_scales"),
+        _ptr(recv_count, torch.int32, "recv_count"), _stream(stream)), "ep_dispatch")
+
+
+def ep_combine(ctx, y: torch.Tensor, topk_weights: torch.Tensor | None, handle,
+               out: torch.Tensor, stream=None) -> None:
+    _check(lib().ep_combine(
+        ctx, _ptr(y, torch.bfloat16, "y"), _ptr(topk_weights, torch.float32, "topk_weights"),
+        handle, _ptr(out, torch.bfloat16, "out"), _stream(stream)), "ep_combine")
+
+
+def ep_get_device_status(ctx, stream=None) -> int:
+    return lib().ep_get_device_status(ctx, _stream(stream))

@@ -145,12 +145,15 @@ def _route(w: Workload, rng: np.random.Generator):
     return idx.astype(np.int64), weights.astype(np.float32)
 
 
-def generate(w: Workload) -> dict:
-    """x_bits uint16 [R, T, H]; topk_idx int64 [R, T, K];
-    topk_weights float32 [R, T, K]."""
+def generate(w: Workload, with_x: bool = True) -> dict:
+    """x_bits uint16 [R, T, H] (unless with_x is False); topk_idx int64
+    [R, T, K]; topk_weights float32 [R, T, K].  The routing is drawn before
+    x, so it does not depend on with_x."""
     rng = np.random.default_rng(w.seed)
     R, T, H, K = w.num_ranks, w.tokens_per_rank, w.hidden, w.topk
     idx, weights = _route(w, rng)
+    if not with_x:
+        return dict(topk_idx=idx.reshape(R, T, K), topk_weights=weights.reshape(R, T, K))
     x = rng.standard_normal((R * T, H), dtype=np.float32)
     if w.x_scale == "loguniform":
         s = 10.0 ** rng.uniform(-2.0, 2.0, size=(R * T, 1))

@@ -1,0 +1,211 @@
+/*
+ * ep.h — C ABI of libep.so: MoE dispatch / combine for one GB300 (sm_103a).
+ *
+ * The operations are the expert-parallel (EP) exchange of DeepEP as described
+ * by "如何突破MoE通信瓶颈：DeepEP跨节点优化技术终极指南" (cyqw.cn):
+ *   - section 核心API示例: low_latency_dispatch(hidden_states, topk_idx,
+ *     num_max_dispatch_tokens_per_rank, num_experts) and
+ *     low_latency_combine(hidden_states, topk_idx, topk_weights, handle,
+ *     num_experts);
+ *   - section 技术解析: the dispatch layout is computed once and reused
+ *     through a handle;
+ *   - section 核心优势: FP8 dispatch and BF16 combine (128 tokens, hidden 7168,
+ *     top-8 in the low-latency setting);
+ *   - section 低延迟模式关键特性 / 性能调优: preallocated fixed-size receive
+ *     buffers and a size hint (Buffer.get_low_latency_rdma_size_hint()).
+ * The DeepTech announcement of DeepEP (010bt.com) adds the two kernel
+ * families (low-latency and high-throughput "normal"), native FP8 dispatch
+ * and SM-count control.
+ *
+ * Model.  R expert-parallel ranks are R *virtual* ranks whose send and receive
+ * partitions all live in this GPU's memory.  Rank r holds T tokens
+ * (T <= Tmax = num_max_dispatch_tokens_per_rank); token t of rank r is global
+ * token g = r*T + t.  There are E experts (E % R == 0); expert e lives on rank
+ * e / (E/R).  Each token picks K experts: topk_idx[g*K + k], -1 = none.
+ *
+ * Receive layout.  Every entry (g, k) with topk_idx != -1 gets one receive
+ * row.  The rows of expert e start at base[e] and hold its entries in
+ * ascending (g, k) order — deterministic, identical on every call.
+ *   EP_LAYOUT_PADDED  (low-latency mode): E fixed buffers of R*Tmax rows,
+ *                     base[e] = e*R*Tmax, rows = E*R*Tmax.  Rows past an
+ *                     expert's count are never written.
+ *   EP_LAYOUT_PACKED  (normal mode): base[e] = sum of the counts of experts
+ *                     e' < e, rows = R*Tmax*K (worst case); rows past the
+ *                     total count are never written.
+ * Payload: BF16 rows [rows, H], or FP8 rows [rows, H] of OCP E4M3FN codes
+ * plus fp32 scales [rows, H/128] (row-major).  FP8 cast per 128 channels of
+ * a token: amax = max |x|, a = max(amax, 1e-4), scale = a/448 and
+ * q = e4m3(x * (448/a)) rounded to nearest-even with saturation at +-448,
+ * each step one IEEE fp32 operation.
+ * Combine: out[g, c] = bf16( fma chain over k = 0..K-1 ascending of
+ * w[g,k] * y[row(g,k), c], starting from +0, masked entries skipped ),
+ * accumulated in fp32 and rounded once to bf16 (nearest-even).
+ *
+ * Conventions.
+ *   - Pointers named d_* / documented "device" are device memory of the
+ *     context's GPU; the caller allocates and owns them.  Everything else is
+ *     host memory.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work: none of them synchronises the host, except
+ *     ep_get_device_status.
+ *   - Errors a host can see (bad sizes, NULL pointers, misalignment) return at
+ *     once and enqueue nothing.  Errors only the GPU can see (an expert id
+ *     outside [-1, E), a padded expert buffer offered more than R*Tmax
+ *     entries) set bits in a per-context device status word, read and
+ *     cleared by ep_get_device_status; the offending entries get no row.
+ *   - A context and its handles belong to the device current at ep_create;
+ *     calls must be made with that device current.  A context is not
+ *     thread-safe; calls on one context must not overlap on the GPU unless
+ *     they use different handles and output buffers.
+ */
+#ifndef EP_H
+#define EP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define EP_ABI_VERSION 1
+
+typedef enum ep_status {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1,  /* a host-checkable argument is wrong; nothing enqueued */
+    EP_ERR_UNSUPPORTED = 2,  /* valid but beyond this build's limits (see ep_config) */
+    EP_ERR_OOM = 3,          /* a device allocation in ep_create / ep_handle_create failed */
+    EP_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    EP_ERR_BAD_EXPERT = 5,   /* device: a topk_idx entry was outside [-1, E) */
+    EP_ERR_CAPACITY = 6,     /* device: padded layout, an expert was offered more than R*Tmax entries */
+    EP_ERR_NO_LAYOUT = 7     /* the handle holds no layout yet, or one for other sizes */
+} ep_status;
+
+typedef enum ep_layout {
+    EP_LAYOUT_PADDED = 0,    /* low-latency mode: fixed-size per-expert buffers */
+    EP_LAYOUT_PACKED = 1     /* normal mode: experts back to back (prefix sums) */
+} ep_layout;
+
+/* Sizes of one expert-parallel group.  Limits of this build:
+ *   1 <= num_ranks <= 1024, 1 <= max_tokens_per_rank, 1 <= topk <= 32,
+ *   num_experts % num_ranks == 0, 1 <= num_experts <= 1024,
+ *   num_experts * num_ranks <= 16384,
+ *   8 <= hidden <= 65536, hidden % 8 == 0 (FP8 dispatch: hidden % 128 == 0),
+ *   receive rows and R*Tmax*K below 2^31.
+ * max_sms caps the SMs the dispatch and combine kernels spread over (0 = all),
+ * the SM-count control of the normal kernels. */
+typedef struct ep_config {
+    int32_t num_ranks;            /* R */
+    int32_t max_tokens_per_rank;  /* Tmax (num_max_dispatch_tokens_per_rank) */
+    int32_t hidden;               /* H, channels per token */
+    int32_t num_experts;          /* E */
+    int32_t topk;                 /* K */
+    int32_t layout;               /* ep_layout */
+    int32_t max_sms;              /* 0 = every SM */
+} ep_config;
+
+typedef struct ep_ctx ep_ctx;       /* a configured group + its device status word */
+typedef struct ep_handle ep_handle; /* a cached dispatch layout (device buffers) */
+
+/* Device buffers of a handle, for callers that consume the layout directly
+ * (e.g. an expert kernel that needs src_info).  All pointers are device
+ * pointers owned by the handle; contents are valid in stream order after the
+ * ep_get_dispatch_layout / ep_dispatch call that filled them. */
+typedef struct ep_handle_info {
+    int32_t tokens_per_rank;   /* T of the layout held, -1 if none */
+    int32_t num_tokens;        /* N = R*T */
+    int64_t rows;              /* receive rows (ep_recv_rows) */
+    int32_t *slot;             /* [N, K]  receive row of entry (g,k), -1 if none */
+    int32_t *src_info;         /* [rows]  g*K + k of the entry in each written row */
+    int32_t *cnt_er;           /* [E, R]  entries of source rank r for expert e */
+    int32_t *off_er;           /* [E, R]  first row of (e, r) relative to base[e] */
+    int64_t *base;             /* [E]     first receive row of expert e */
+    int32_t *tokens_per_expert;/* [E]     rows expert e receives */
+} ep_handle_info;
+
+/* Human-readable name of a status code (static string). */
+const char *ep_status_str(int32_t status);
+
+/* EP_OK if cfg is within the limits above, else INVALID_ARG / UNSUPPORTED.
+ * Touches no GPU. */
+ep_status ep_config_check(const ep_config *cfg);
+
+/* Receive rows of the configured layout (E*R*Tmax padded, R*Tmax*K packed).
+ * Touches no GPU. */
+ep_status ep_recv_rows(const ep_config *cfg, int64_t *rows);
+
+/* Bytes the caller must allocate for the receive buffers, the analogue of
+ * Buffer.get_low_latency_rdma_size_hint(): payload = rows*H*2 (BF16) or
+ * rows*H (FP8); scales = rows*(H/128)*4 for FP8, else 0.  Touches no GPU. */
+ep_status ep_recv_bytes(const ep_config *cfg, int32_t use_fp8,
+                        uint64_t *payload_bytes, uint64_t *scale_bytes);
+
+/* Create a context on the current device: validates cfg, allocates the
+ * 4-byte device status word and reads the device's SM count.  *out is NULL on
+ * error. */
+ep_status ep_create(const ep_config *cfg, ep_ctx **out);
+ep_status ep_destroy(ep_ctx *ctx);
+
+/* Allocate a handle's device buffers (slot [R*Tmax*K], src_info [rows],
+ * cnt_er/off_er [E*R], base/tokens_per_expert [E]) once, so that the calls
+ * below allocate nothing and can be captured in a CUDA graph. */
+ep_status ep_handle_create(ep_ctx *ctx, ep_handle **out);
+ep_status ep_handle_destroy(ep_handle *handle);
+ep_status ep_handle_get_info(const ep_handle *handle, ep_handle_info *out);
+
+/* Dispatch layout (the "layout information" DeepEP computes once and reuses).
+ *   d_topk_idx            device int64 [R, T, K], read only
+ *   tokens_per_rank       T, 0 <= T <= Tmax
+ *   d_num_tokens_per_rank device int32 [R] or NULL: tokens with >= 1 entry on rank d
+ *   d_num_tokens_per_expert device int32 [E] or NULL: rows expert e receives
+ *   d_is_token_in_rank    device uint8 [R*T, R] or NULL: 1 if token g has an
+ *                         entry on rank d, else 0
+ *   handle                receives slot / src_info / counts / bases
+ * One kernel (a thread-block cluster; no host synchronisation). */
+ep_status ep_get_dispatch_layout(ep_ctx *ctx, const int64_t *d_topk_idx,
+                                 int32_t tokens_per_rank,
+                                 int32_t *d_num_tokens_per_rank,
+                                 int32_t *d_num_tokens_per_expert,
+                                 uint8_t *d_is_token_in_rank,
+                                 ep_handle *handle, void *stream);
+
+/* low_latency_dispatch: scatter every token row to the receive rows of its
+ * top-k experts, BF16 (bit copy) or FP8 (cast once per token, stored K times).
+ *   d_x            device bf16 [R*T, H] (16-byte aligned), read only
+ *   d_topk_idx     device int64 [R, T, K]: the layout is computed into handle
+ *                  first (layout kernel + dispatch kernel); NULL: reuse the
+ *                  layout already in handle (dispatch kernel only), except
+ *                  that with tokens_per_rank == 0 an empty layout is computed
+ *   tokens_per_rank T (must match the handle when reusing)
+ *   use_fp8        0 = BF16 payload, 1 = FP8 payload + scales
+ *   d_recv_x       device [rows, H] bf16 or uint8 (16-byte aligned)
+ *   d_recv_scales  device fp32 [rows, H/128] when use_fp8, else ignored
+ *   d_recv_count   device int32 [E] or NULL: rows each expert received
+ * Rows that receive nothing are not written. */
+ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
+                      int32_t tokens_per_rank, int32_t use_fp8, ep_handle *handle,
+                      void *d_recv_x, float *d_recv_scales, int32_t *d_recv_count,
+                      void *stream);
+
+/* low_latency_combine: for each token, the fp32 weighted sum over its top-k
+ * entries (ascending k, fused multiply-add) of the expert outputs found in
+ * the entries' receive rows, rounded once to bf16.
+ *   d_y            device bf16 [rows, H] in the handle's receive layout
+ *                  (16-byte aligned), read only; only rows that received an
+ *                  entry are read
+ *   d_topk_weights device fp32 [R*T, K], or NULL for all weights 1 (the
+ *                  backward of dispatch)
+ *   handle         a layout from ep_get_dispatch_layout / ep_dispatch
+ *   d_out          device bf16 [R*T, H] (16-byte aligned) */
+ep_status ep_combine(ep_ctx *ctx, const void *d_y, const float *d_topk_weights,
+                     const ep_handle *handle, void *d_out, void *stream);
+
+/* Synchronise `stream`, read and clear the context's device status word.
+ * Returns EP_OK, EP_ERR_BAD_EXPERT, EP_ERR_CAPACITY or EP_ERR_CUDA. */
+ep_status ep_get_device_status(ep_ctx *ctx, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_H */

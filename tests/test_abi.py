@@ -1,0 +1,91 @@
+"""C ABI checks that need no GPU: the library loads, exports every entry point
+include/ep.h declares, and rejects bad arguments on the host before touching
+the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from combine_get_dispatch_02_gb300 import build as epbuild
+from combine_get_dispatch_02_gb300 import ep
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ep.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    epbuild.build()
+    return ep.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|ep_status)\s*(ep_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_entry_points():
+    assert _declared() == sorted(ep.ENTRY_POINTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert ep.status_str(s) and ep.status_str(s) != "unknown status"
+    assert ep.status_str(99) == "unknown status"
+
+
+def test_config_limits(lib):
+    ok = ep.make_config(32, 128, 7168, 256, 8)
+    assert ep.ep_config_check(ok) == ep.EP_OK
+    bad = [
+        (ep.make_config(0, 128, 7168, 256, 8), ep.EP_ERR_INVALID_ARG),
+        (ep.make_config(32, 0, 7168, 256, 8), ep.EP_ERR_INVALID_ARG),
+        (ep.make_config(32, 128, 7170, 256, 8), ep.EP_ERR_INVALID_ARG),   # H % 8
+        (ep.make_config(32, 128, 7168, 250, 8), ep.EP_ERR_INVALID_ARG),   # E % R
+        (ep.make_config(32, 128, 7168, 256, 0), ep.EP_ERR_INVALID_ARG),
+        (ep.make_config(32, 128, 7168, 256, 8, layout=5), ep.EP_ERR_INVALID_ARG),
+        (ep.make_config(32, 128, 7168, 256, 8, max_sms=-1), ep.EP_ERR_INVALID_ARG),
+        (ep.make_config(32, 128, 7168, 256, 33), ep.EP_ERR_UNSUPPORTED),
+        (ep.make_config(32, 128, 7168, 2048, 8), ep.EP_ERR_UNSUPPORTED),
+        (ep.make_config(64, 128, 7168, 512, 8), ep.EP_ERR_UNSUPPORTED),   # E*R > 16384
+        (ep.make_config(32, 1 << 20, 7168, 256, 8), ep.EP_ERR_UNSUPPORTED),  # rows >= 2^31
+    ]
+    for cfg, want in bad:
+        assert ep.ep_config_check(cfg) == want, (cfg.num_ranks, cfg.hidden, cfg.num_experts)
+    assert lib.ep_config_check(None) == ep.EP_ERR_INVALID_ARG
+
+
+def test_size_queries(lib):
+    cfg = ep.make_config(32, 128, 7168, 256, 8)
+    assert ep.ep_recv_rows(cfg) == 256 * 32 * 128
+    assert ep.ep_recv_bytes(cfg, True) == (256 * 4096 * 7168, 256 * 4096 * 56 * 4)
+    assert ep.ep_recv_bytes(cfg, False) == (256 * 4096 * 7168 * 2, 0)
+    packed = ep.make_config(8, 4096, 7168, 256, 8, layout=ep.EP_LAYOUT_PACKED)
+    assert ep.ep_recv_rows(packed) == 8 * 4096 * 8
+    odd = ep.make_config(4, 32, 200, 32, 4)
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_recv_bytes(odd, True)  # FP8 needs H % 128 == 0
+    assert e.value.status == ep.EP_ERR_UNSUPPORTED
+
+
+def test_host_rejections_touch_no_device(lib):
+    P = ctypes.c_void_p
+    # invalid config: rejected before any CUDA call
+    out = P(123)
+    assert lib.ep_create(ctypes.byref(ep.make_config(0, 1, 8, 1, 1)), ctypes.byref(out)) == ep.EP_ERR_INVALID_ARG
+    assert out.value is None
+    assert lib.ep_create(None, ctypes.byref(out)) == ep.EP_ERR_INVALID_ARG
+    # NULL context / handle
+    assert lib.ep_dispatch(None, None, None, 1, 0, None, None, None, None, None) == ep.EP_ERR_INVALID_ARG
+    assert lib.ep_combine(None, None, None, None, None, None) == ep.EP_ERR_INVALID_ARG
+    assert lib.ep_get_dispatch_layout(None, None, 0, None, None, None, None, None) == ep.EP_ERR_INVALID_ARG
+    assert lib.ep_get_device_status(None, None) == ep.EP_ERR_INVALID_ARG
+    assert lib.ep_destroy(None) == ep.EP_ERR_INVALID_ARG
+    assert lib.ep_handle_destroy(None) == ep.EP_ERR_INVALID_ARG
+    assert lib.ep_handle_create(None, ctypes.byref(out)) == ep.EP_ERR_INVALID_ARG
+    assert lib.ep_handle_get_info(None, None) == ep.EP_ERR_INVALID_ARG
