@@ -45,6 +45,10 @@ def _args():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--breakdown-reps", type=int, default=200)
+    ap.add_argument("--layout", choices=["padded", "packed"], default=None,
+                    help="override the workload's receive layout (packed keeps a profiled run small)")
     return ap.parse_args()
 
 
@@ -222,6 +226,21 @@ def _workload_desc(w):
 
 # ------------------------------------------------------------------ GPU
 
+def replica_throughput(total_ms: float, steps: int, tokens_per_replica: int, world_size: int,
+                       device="cpu"):
+    """Whole-job throughput of ``world_size`` independent replicas: the
+    slowest rank's time decides (max over ranks), every rank's tokens count.
+    Returns (ms per step, tokens/s)."""
+    if world_size > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / steps
+    return ms_per_step, world_size * tokens_per_replica / (ms_per_step / 1e3)
+
+
 def _algorithmic_bytes(w, M):
     N, K, H = w.num_tokens, w.topk, w.hidden
     pay = 1 if w.use_fp8 else 2
@@ -247,6 +266,8 @@ def run_ours(args):
     from combine_get_dispatch_02_gb300 import workloads as wl
     epbuild.build()
     w = wl.WORKLOADS[args.workload]
+    if args.layout is not None:
+        w = w.with_(layout=args.layout)
     d = wl.generate(w)
     N, K, H = w.num_tokens, w.topk, w.hidden
 
@@ -313,17 +334,13 @@ def run_ours(args):
     disp_ms = [a.elapsed_time(b) for a, b, _ in evs]
     comb_ms = [b.elapsed_time(c) for _, b, c in evs]
     step_ms = [a.elapsed_time(c) for a, _, c in evs]
-    total_ms = sum(step_ms)
-    if ws > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    value = ws * N / (ms_per_step / 1e3)
+    ms_per_step, value = replica_throughput(sum(step_ms), args.steps, N, ws, device="cuda")
 
     # breakdown: each kernel alone (layout alone, dispatch with the cached
     # layout, combine), same L2 flush between launches
-    def timed(fn, reps=200):
+    def timed(fn, reps=args.breakdown_reps):
+        if reps <= 0:
+            return float("nan"), float("nan")
         ts = []
         for _ in range(reps):
             flush.fill_(1)
@@ -343,6 +360,25 @@ def run_ours(args):
     comb_us = timed(lambda: ep.ep_combine(ctx, y, wts, h.raw, out, stream))
 
     # end to end through the public API with host buffers
+    e2e = None if args.no_e2e else _e2e(args, w, d, x, idx, wts, out, ctx, h, recv, scales, cnt, y, stream)
+    if buf.device_status() != ep.EP_OK:
+        raise RuntimeError("device status error")
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+    _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
+            e2e, clk)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def _e2e(args, w, d, x, idx, wts, out, ctx, h, recv, scales, cnt, y, stream):
+    import torch
+    from combine_get_dispatch_02_gb300 import ep
+    N, K, H = w.num_tokens, w.topk, w.hidden
+    ws = _dist()[0]
     xh = torch.from_numpy(np.ascontiguousarray(d["x_bits"]).view(np.int16)).view(torch.bfloat16).pin_memory()
     idxh = torch.from_numpy(d["topk_idx"]).pin_memory()
     wh = torch.from_numpy(d["topk_weights"].reshape(N, K)).pin_memory()
@@ -364,23 +400,22 @@ def run_ours(args):
     torch.cuda.synchronize()
     wall = (time.perf_counter() - t0) / args.e2e_steps
     e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
-    if buf.device_status() != ep.EP_OK:
-        raise RuntimeError("device status error")
     h2d = xh.numel() * 2 + idxh.numel() * 8 + wh.numel() * 4
     d2h = outh.numel() * 2
+    return {"value": N / (e2e_ms / 1e3) * ws, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step_device": e2e_ms, "ms_per_step_wall": wall * 1e3}
 
-    if rank != 0:
-        if ws > 1:
-            torch.distributed.destroy_process_group()
-        return
 
+def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
+            e2e, clk):
     peak, peak_kind = _peaks()
     disp_bytes, disp_kernel_bytes, comb_bytes = _algorithmic_bytes(w, M)
     comb_avg_s = statistics.mean(comb_ms) / 1e3
     comb_gbs = comb_bytes / comb_avg_s / 1e9
     traffic = _traffic("combine", COMBINE_SRC, w.name)
-    disp_avg_s = disp_us[1] / 1e6
-    disp_gbs = disp_kernel_bytes / disp_avg_s / 1e9
+    disp_gbs = disp_kernel_bytes / (disp_us[1] / 1e6) / 1e9 if disp_us[1] == disp_us[1] else None
+    nan_none = lambda v: None if v != v else v
+    lay_us, disp_us, comb_us = [tuple(nan_none(v) for v in t) for t in (lay_us, disp_us, comb_us)]
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
@@ -403,11 +438,10 @@ def run_ours(args):
                      "unit": "GB/s", "frac": comb_gbs / peak, "traffic": traffic,
                      "algorithmic_bytes": comb_bytes, "peak_source": f"{peak_kind} HBM copy bandwidth"},
         "roofline_dispatch": {"bound": "hbm", "kernel": "dispatch (cached layout)", "achieved": disp_gbs,
-                              "peak": peak, "unit": "GB/s", "frac": disp_gbs / peak,
+                              "peak": peak, "unit": "GB/s", "frac": disp_gbs / peak if disp_gbs else None,
                               "traffic": _traffic("dispatch", DISPATCH_SRC, w.name),
                               "algorithmic_bytes": disp_kernel_bytes},
-        "e2e": {"value": N / (e2e_ms / 1e3) * ws, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step_device": e2e_ms, "ms_per_step_wall": wall * 1e3},
+        "e2e": e2e,
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
         "host_cores": os.cpu_count(),
@@ -415,8 +449,6 @@ def run_ours(args):
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, 128)
     print(json.dumps(line), flush=True)
-    if ws > 1:
-        torch.distributed.destroy_process_group()
 
 
 def main():

@@ -32,14 +32,20 @@ LAYOUT_PADDED = 0
 LAYOUT_PACKED = 1
 
 
+def compile_source(src: str, out: str) -> str:
+    """gcc -O2 -ffp-contract=off (no fast-math) of one C file into a shared library."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.check_call(
+        ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
+         "-Wall", "-shared", "-fPIC", "-o", tmp, src, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compile ep_oracle.c into libep_oracle.so next to it (gcc, no fast-math)."""
+    """Compile ep_oracle.c into libep_oracle.so next to it."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(
-            ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
-             "-Wall", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
-        os.replace(tmp, _LIB)
+        compile_source(_SRC, _LIB)
     return _LIB
 
 
@@ -47,26 +53,37 @@ _lib = None
 
 
 def _load():
-    global _lib
     if _lib is None:
-        lib = ctypes.CDLL(build())
-        P = ctypes.c_void_p
-        I32, I64 = ctypes.c_int, ctypes.c_int64
-        lib.orc_layout.restype = None
-        lib.orc_layout.argtypes = [I32, I32, I32, I32, I32, I32, P,
-                                   P, P, P, P, P, P, P, P, I64, P]
-        lib.orc_quant_block.argtypes = [P, P, P]
-        lib.orc_quant_token.argtypes = [P, I32, P, P]
-        lib.orc_dispatch.argtypes = [I64, I32, I32, I32, P, P, P, P]
-        lib.orc_combine.argtypes = [I64, I32, I32, P, P, P, P]
-        for name in ("orc_f32_to_bf16_n", "orc_bf16_to_f32_n",
-                     "orc_f32_to_e4m3_n", "orc_e4m3_to_f32_n"):
-            getattr(lib, name).argtypes = [P, P, I64]
-        lib.orc_f32_to_bf16.restype = ctypes.c_uint16
-        lib.orc_f32_to_bf16.argtypes = [ctypes.c_float]
-        lib.orc_f32_to_e4m3.restype = ctypes.c_uint8
-        lib.orc_f32_to_e4m3.argtypes = [ctypes.c_float]
-        _lib = lib
+        use_library(build())
+    return _lib
+
+
+def use_library(path: str | None):
+    """Bind this module to the oracle library at ``path`` (None: unbind, so the
+    next call loads the built ep_oracle.c again).  The tests use it to run the
+    pins against deliberately broken copies of the oracle."""
+    global _lib
+    if path is None:
+        _lib = None
+        return None
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    I32, I64 = ctypes.c_int, ctypes.c_int64
+    lib.orc_layout.restype = None
+    lib.orc_layout.argtypes = [I32, I32, I32, I32, I32, I32, P,
+                               P, P, P, P, P, P, P, P, I64, P]
+    lib.orc_quant_block.argtypes = [P, P, P]
+    lib.orc_quant_token.argtypes = [P, I32, P, P]
+    lib.orc_dispatch.argtypes = [I64, I32, I32, I32, P, P, P, P]
+    lib.orc_combine.argtypes = [I64, I32, I32, P, P, P, P]
+    for name in ("orc_f32_to_bf16_n", "orc_bf16_to_f32_n",
+                 "orc_f32_to_e4m3_n", "orc_e4m3_to_f32_n"):
+        getattr(lib, name).argtypes = [P, P, I64]
+    lib.orc_f32_to_bf16.restype = ctypes.c_uint16
+    lib.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+    lib.orc_f32_to_e4m3.restype = ctypes.c_uint8
+    lib.orc_f32_to_e4m3.argtypes = [ctypes.c_float]
+    _lib = lib
     return _lib
 
 
