@@ -31,6 +31,7 @@ struct LayoutParams {
     int32_t *tokens_per_rank;         // [R] or nullptr
     uint8_t *is_token_in_rank;        // [N*R] or nullptr
     uint32_t *status;
+    int32_t staged;            // set by launch_layout: expert ids staged in shared memory
 };
 
 // Launch the single-cluster layout kernel.  cluster_size / threads come from

@@ -33,6 +33,7 @@ namespace ep {
 namespace {
 
 constexpr size_t kMaxSmem = 227 * 1024;
+constexpr int kMaxCluster = 16;
 
 // Exclusive scan of one int per thread across the block; *total gets the sum.
 // scan must hold NT/32 + 1 ints.  Ends with a barrier.
@@ -66,6 +67,23 @@ __device__ int block_exclusive_scan(int v, int *scan, int *total) {
     return excl;
 }
 
+// Sum over the cluster's CTAs of a shared-memory int at `off` (all peers'
+// loads are issued before the first add), and the part from CTAs ranked
+// below `crank`.
+__device__ __forceinline__ int2 cluster_sum_below(cg::cluster_group &cluster, int32_t *base, int off,
+                                                  int CL, int crank) {
+    int v[kMaxCluster];
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) v[c] = c < CL ? cluster.map_shared_rank(base, c)[off] : 0;
+    int pre = 0, tot = 0;
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) {
+        pre += c < crank ? v[c] : 0;
+        tot += v[c];
+    }
+    return make_int2(pre, tot);
+}
+
 template <int NT>
 __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     // The dispatch kernel queued behind this one may start loading and
@@ -78,7 +96,8 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     const int crank = (int)cluster.block_rank();
     constexpr int NW = NT / 32;
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    const int E = p.E, R = p.R, K = p.K;
+    const int E = p.E, R = p.R, K = p.K, T = p.T;
+    const int N = (int)p.N;  // N*K < 2^31 (checked on the host)
     const int per = (E + CL - 1) / CL;
 
     extern __shared__ int32_t sm[];
@@ -90,55 +109,69 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     int32_t *ebase = epre + E;            // [E]     totals, then first rows
     int32_t *scan = ebase + E;            // [NW+1]
     int32_t *pair = scan + NW + 1;        // [per][R]
+    int16_t *stage = reinterpret_cast<int16_t *>(pair + per * R);  // [NW][tpw*K] expert ids
 
     const int zero_words = NW * E + E + E * R + R;
     for (int i = tid; i < zero_words; i += NT) sm[i] = 0;
 
     // contiguous token range per warp, warps of a CTA adjacent
-    const int64_t nwarps = (int64_t)CL * NW;
-    const int64_t tpw = (p.N + nwarps - 1) / nwarps;
-    const int64_t cta_t0 = min(p.N, (int64_t)crank * NW * tpw);
-    const int64_t cta_t1 = min(p.N, cta_t0 + (int64_t)NW * tpw);
-    const int64_t t0 = min(cta_t1, cta_t0 + (int64_t)w * tpw);
-    const int64_t t1 = min(cta_t1, t0 + tpw);
-    const int64_t i0 = t0 * K, i1 = t1 * K;
+    const int nwarps = CL * NW;
+    const int tpw = (N + nwarps - 1) / nwarps;
+    const int cta_t0 = min(N, crank * NW * tpw);
+    const int cta_t1 = min(N, cta_t0 + NW * tpw);
+    const int t0 = min(cta_t1, cta_t0 + w * tpw);
+    const int t1 = min(cta_t1, t0 + tpw);
+    const int i0 = t0 * K, i1 = t1 * K;
+    // this warp's entry ids in shared memory for pass 2 (when they fit)
+    int16_t *my_stage = p.staged ? stage + (size_t)w * tpw * K : nullptr;
 
     // membership rows of this CTA's tokens start at zero
     if (p.is_token_in_rank) {
-        for (int64_t b = cta_t0 * R + tid; b < cta_t1 * R; b += NT) p.is_token_in_rank[b] = 0;
+        for (int b = cta_t0 * R + tid; b < cta_t1 * R; b += NT) p.is_token_in_rank[b] = 0;
     }
     __syncthreads();
 
-    // ---------------- pass 1: counts
-    for (int64_t ib = i0; ib < i1; ib += 32) {
-        const int64_t i = ib + lane;
-        const bool in = i < i1;
-        const int64_t e = in ? p.topk_idx[i] : -1;
-        const bool valid = in && e >= 0 && e < E;
-        if (in && (e < -1 || e >= E)) atomicOr(p.status, kStatusBadExpert);
-        const int key = valid ? (int)e * R + (int)((i / K) / p.T) : -1;
-        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key);
-        if (valid && lane == __ffs(peers) - 1) {
-            const int n = __popc(peers);
-            atomicAdd(&hist_w[w * E + (int)e], n);
-            atomicAdd(&hist_er[key], n);
+    // ---------------- pass 1: counts (four loads in flight per lane)
+    constexpr int kU = 4;
+    for (int ib = i0; ib < i1; ib += 32 * kU) {
+        int64_t ev[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = ib + u * 32 + lane;
+            ev[u] = i < i1 ? p.topk_idx[i] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = ib + u * 32 + lane;
+            const bool in = i < i1;
+            const int64_t e = ev[u];
+            const bool valid = in && e >= 0 && e < E;
+            if (in && (e < -1 || e >= E)) atomicOr(p.status, kStatusBadExpert);
+            if (in && my_stage) my_stage[i - i0] = valid ? (int16_t)e : (int16_t)-1;
+            const int key = valid ? (int)e * R + (i / K) / T : -1;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key);
+            if (valid && lane == __ffs(peers) - 1) {
+                const int n = __popc(peers);
+                atomicAdd(&hist_w[w * E + (int)e], n);
+                atomicAdd(&hist_er[key], n);
+            }
         }
     }
     if (p.tokens_per_rank || p.is_token_in_rank) {
-        for (int64_t g = t0 + lane; g < t1; g += 32) {
-            const int64_t *row = p.topk_idx + g * K;
+        for (int g = t0 + lane; g < t1; g += 32) {
+            const int64_t *row = p.topk_idx + (int64_t)g * K;
             for (int k = 0; k < K; ++k) {
                 const int64_t e = row[k];
                 if (e < 0 || e >= E) continue;
-                const int d = (int)(e / p.L);
+                const int d = (int)e / p.L;
                 bool seen = false;
                 for (int k2 = 0; k2 < k && !seen; ++k2) {
                     const int64_t e2 = row[k2];
-                    seen = e2 >= 0 && e2 < E && (int)(e2 / p.L) == d;
+                    seen = e2 >= 0 && e2 < E && (int)e2 / p.L == d;
                 }
                 if (seen) continue;
                 atomicAdd(&tok_rank[d], 1);
-                if (p.is_token_in_rank) p.is_token_in_rank[g * R + d] = 1;
+                if (p.is_token_in_rank) p.is_token_in_rank[(int64_t)g * R + d] = 1;
             }
         }
     }
@@ -158,14 +191,21 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
 
     // per expert: entries in lower-ranked CTAs, and the total over the cluster
     for (int e = tid; e < E; e += NT) {
-        int pre = 0, tot = 0;
-        for (int c = 0; c < CL; ++c) {
-            const int v = cluster.map_shared_rank(cta_hist, c)[e];
-            pre += c < crank ? v : 0;
-            tot += v;
-        }
-        epre[e] = pre;
-        ebase[e] = tot;
+        const int2 pt = cluster_sum_below(cluster, cta_hist, e, CL, crank);
+        epre[e] = pt.x;
+        ebase[e] = pt.y;
+    }
+    // counts per (expert, source rank) for this CTA's slice of experts
+    const int pe0 = min(E, crank * per), pe1 = min(E, pe0 + per);
+    const int npairs = (pe1 - pe0) * R;
+    for (int q = tid; q < npairs; q += NT) {
+        const int j = pe0 * R + q;
+        const int v = cluster_sum_below(cluster, hist_er, j, CL, 0).y;
+        pair[q] = v;
+        p.cnt_er[j] = v;
+    }
+    if (crank == 0 && p.tokens_per_rank) {
+        for (int d = tid; d < R; d += NT) p.tokens_per_rank[d] = cluster_sum_below(cluster, tok_rank, d, CL, 0).y;
     }
     __syncthreads();
 
@@ -191,25 +231,6 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
             ebase[e] = b;
         }
     }
-
-    // counts per (expert, source rank) for this CTA's slice of experts
-    const int pe0 = min(E, crank * per), pe1 = min(E, pe0 + per);
-    const int npairs = (pe1 - pe0) * R;
-    for (int q = tid; q < npairs; q += NT) {
-        const int j = pe0 * R + q;
-        int v = 0;
-        for (int c = 0; c < CL; ++c) v += cluster.map_shared_rank(hist_er, c)[j];
-        pair[q] = v;
-        p.cnt_er[j] = v;
-    }
-    if (crank == 0 && p.tokens_per_rank) {
-        for (int d = tid; d < R; d += NT) {
-            int v = 0;
-            for (int c = 0; c < CL; ++c) v += cluster.map_shared_rank(tok_rank, c)[d];
-            p.tokens_per_rank[d] = v;
-        }
-    }
-    __syncthreads();
     for (int e = pe0 + tid; e < pe1; e += NT) {
         int run = 0;
         for (int r = 0; r < R; ++r) {
@@ -223,35 +244,58 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
 
     // ---------------- pass 2: rows, in (g, k) order
     const uint32_t lt = lanemask_lt();
-    for (int64_t ib = i0; ib < i1; ib += 32) {
-        const int64_t i = ib + lane;
-        const bool in = i < i1;
-        const int64_t e = in ? p.topk_idx[i] : -1;
-        const bool valid = in && e >= 0 && e < E;
-        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? (int)e : -1);
-        int pos = 0;
-        if (valid) pos = hist_w[w * E + (int)e] + __popc(peers & lt);
-        __syncwarp();
-        if (valid && lane == __ffs(peers) - 1) hist_w[w * E + (int)e] += __popc(peers);
-        __syncwarp();
-        if (in) {
-            int32_t s = -1;
-            if (valid) {
-                if (pos < p.cap) {
-                    s = ebase[(int)e] + pos;
-                    p.src_info[s] = (int32_t)i;
-                } else {
-                    atomicOr(p.status, kStatusCapacity);
-                }
+    const int cap = (int)min(p.cap, (int64_t)0x7FFFFFFF);
+    for (int ib = i0; ib < i1; ib += 32 * kU) {
+        int ev[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = ib + u * 32 + lane;
+            if (i >= i1) {
+                ev[u] = -1;
+            } else if (my_stage) {
+                ev[u] = my_stage[i - i0];
+            } else {
+                const int64_t e = p.topk_idx[i];
+                ev[u] = (e >= 0 && e < E) ? (int)e : -1;
             }
-            p.slot[i] = s;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = ib + u * 32 + lane;
+            const int e = ev[u];
+            const bool valid = e >= 0;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+            int pos = 0;
+            if (valid) pos = hist_w[w * E + e] + __popc(peers & lt);
+            __syncwarp();
+            if (valid && lane == __ffs(peers) - 1) hist_w[w * E + e] += __popc(peers);
+            __syncwarp();
+            if (i < i1) {
+                int32_t s = -1;
+                if (valid) {
+                    if (pos < cap) {
+                        s = ebase[e] + pos;
+                        p.src_info[s] = i;
+                    } else {
+                        atomicOr(p.status, kStatusCapacity);
+                    }
+                }
+                p.slot[i] = s;
+            }
         }
     }
 }
 
 template <int NT>
-cudaError_t launch_nt(const LayoutParams &p, int cl, cudaStream_t stream) {
-    const size_t smem = layout_smem_bytes(p.E, p.R, NT, cl);
+cudaError_t launch_nt(LayoutParams p, int cl, cudaStream_t stream) {
+    size_t smem = layout_smem_bytes(p.E, p.R, NT, cl);
+    // stage the entries' expert ids in shared memory for the second pass
+    // when they fit next to the histograms
+    const int64_t nwarps = (int64_t)cl * (NT / 32);
+    const int64_t tpw = (p.N + nwarps - 1) / nwarps;
+    const size_t stage = (size_t)(NT / 32) * tpw * p.K * sizeof(int16_t);
+    p.staged = (smem + stage <= kMaxSmem) ? 1 : 0;
+    if (p.staged) smem += (stage + 15) / 16 * 16;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cl, 1, 1);
     cfg.blockDim = dim3(NT, 1, 1);
