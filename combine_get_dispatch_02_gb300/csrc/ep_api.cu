@@ -33,6 +33,7 @@ struct ep_handle {
     int64_t *base;
     int32_t *tokens_per_expert;
     int32_t tokens_per_rank;  // -1: no layout yet
+    int32_t has_rank_ranges;  // cnt_er / off_er hold the current layout's ranges
 };
 
 namespace {
@@ -78,8 +79,8 @@ int grid_cap(const ep_ctx *ctx, int blocks_per_sm) {
 }
 
 ep_status enqueue_layout(ep_ctx *ctx, const int64_t *topk_idx, int32_t T, int32_t *tokens_per_rank,
-                         int32_t *user_tokens_per_expert, uint8_t *is_token_in_rank, ep_handle *h,
-                         cudaStream_t stream) {
+                         int32_t *user_tokens_per_expert, uint8_t *is_token_in_rank, bool want_ranges,
+                         ep_handle *h, cudaStream_t stream) {
     const ep_config &c = ctx->cfg;
     ep::LayoutParams p;
     p.topk_idx = topk_idx;
@@ -94,8 +95,8 @@ ep_status enqueue_layout(ep_ctx *ctx, const int64_t *topk_idx, int32_t T, int32_
                                          : (int64_t)c.num_ranks * c.max_tokens_per_rank * c.topk;
     p.slot = h->slot;
     p.src_info = h->src_info;
-    p.cnt_er = h->cnt_er;
-    p.off_er = h->off_er;
+    p.cnt_er = want_ranges ? h->cnt_er : nullptr;
+    p.off_er = want_ranges ? h->off_er : nullptr;
     p.base = h->base;
     p.tokens_per_expert = h->tokens_per_expert;
     p.user_tokens_per_expert = user_tokens_per_expert;
@@ -107,6 +108,7 @@ ep_status enqueue_layout(ep_ctx *ctx, const int64_t *topk_idx, int32_t T, int32_
         return EP_ERR_CUDA;
     }
     h->tokens_per_rank = T;
+    h->has_rank_ranges = want_ranges ? 1 : 0;
     return EP_OK;
 }
 
@@ -243,6 +245,7 @@ ep_status ep_handle_get_info(const ep_handle *h, ep_handle_info *out) {
     out->off_er = h->off_er;
     out->base = h->base;
     out->tokens_per_expert = h->tokens_per_expert;
+    out->has_rank_ranges = h->has_rank_ranges;
     return EP_OK;
 }
 
@@ -256,7 +259,7 @@ ep_status ep_get_dispatch_layout(ep_ctx *ctx, const int64_t *d_topk_idx, int32_t
         return EP_ERR_INVALID_ARG;
     if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
     return enqueue_layout(ctx, d_topk_idx, tokens_per_rank, d_num_tokens_per_rank, d_num_tokens_per_expert,
-                          d_is_token_in_rank, handle, (cudaStream_t)stream);
+                          d_is_token_in_rank, /*want_ranges=*/true, handle, (cudaStream_t)stream);
 }
 
 ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, int32_t tokens_per_rank,
@@ -283,7 +286,7 @@ ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, i
     const bool fresh = d_topk_idx != nullptr || tokens_per_rank == 0;
     if (fresh) {
         const ep_status s = enqueue_layout(ctx, d_topk_idx, tokens_per_rank, nullptr, d_recv_count, nullptr,
-                                           handle, st);
+                                           /*want_ranges=*/false, handle, st);
         if (s != EP_OK) return s;
     }
     if (N == 0) {

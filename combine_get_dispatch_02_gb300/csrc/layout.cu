@@ -12,16 +12,20 @@
 //   * One cluster of CL CTAs (16 when the device allows it) covers all tokens;
 //     CTA c owns a contiguous token range, split again into one contiguous
 //     range per warp, so (CTA, warp, lane) order is (g, k) order.
-//   * Pass 1: each warp counts its entries per expert and per (expert,
-//     source rank) in shared memory, aggregating equal keys with
-//     __match_any_sync so one atomic per distinct key per 32 entries.
-//   * The CTAs exchange their per-expert totals through distributed shared
-//     memory after a hardware cluster barrier: every CTA gets the count of
-//     each expert in lower-ranked CTAs and the grand totals (hence the bases),
-//     with no global-memory atomics, no spin-waits and no second launch.
-//   * Pass 2: each warp walks its entries again in order; an entry's row is
-//     base + (entries of the expert before this warp) + (entries earlier in
-//     this warp), the last term from __match_any_sync and a lane mask.
+//   * Equal keys inside a warp are found with one ballot per key bit (a
+//     deterministic multi-split: lanes whose bits all agree hold the same
+//     key), which is much cheaper than match.any on this GPU.
+//   * Pass 1: each warp counts its entries per expert in shared memory.  Each
+//     CTA then stores its per-expert totals into every peer's shared memory
+//     (distributed shared memory) and, after one hardware cluster barrier,
+//     every CTA holds all totals locally: its prefix, the grand totals and the
+//     bases follow without global atomics, spin-waits or a second launch.
+//   * Pass 2: each warp walks its entries again (from a shared-memory copy
+//     when it fits); an entry's row is base + (entries of the expert before
+//     this CTA) + (before this warp) + (earlier in this warp).
+//   * Per-(expert, source rank) ranges (cnt_er / off_er) are optional: pass 2
+//     adds the per-round counts to the zeroed global cnt_er, and after a
+//     second cluster barrier the owner CTAs turn them into offsets.
 #include <cooperative_groups.h>
 
 #include "ep_internal.cuh"
@@ -33,7 +37,23 @@ namespace ep {
 namespace {
 
 constexpr size_t kMaxSmem = 227 * 1024;
-constexpr int kMaxCluster = 16;
+constexpr int kU = 4;  // 32-entry rounds per warp in flight
+
+// Lanes of the warp whose key equals this lane's (all lanes take part; keys
+// are non-negative and below 2^nbits).
+__device__ __forceinline__ uint32_t warp_match(int key, int nbits) {
+    uint32_t m = 0xFFFFFFFFu;
+    for (int b = 0; b < nbits; ++b) {
+        const bool bit = (key >> b) & 1;
+        const uint32_t v = __ballot_sync(0xFFFFFFFFu, bit);
+        m &= bit ? v : ~v;
+    }
+    return m;
+}
+
+__device__ __forceinline__ int bits_for(int n) {  // smallest b with n <= 2^b
+    return 32 - __clz(max(n - 1, 1));
+}
 
 // Exclusive scan of one int per thread across the block; *total gets the sum.
 // scan must hold NT/32 + 1 ints.  Ends with a barrier.
@@ -67,21 +87,13 @@ __device__ int block_exclusive_scan(int v, int *scan, int *total) {
     return excl;
 }
 
-// Sum over the cluster's CTAs of a shared-memory int at `off` (all peers'
-// loads are issued before the first add), and the part from CTAs ranked
-// below `crank`.
-__device__ __forceinline__ int2 cluster_sum_below(cg::cluster_group &cluster, int32_t *base, int off,
-                                                  int CL, int crank) {
-    int v[kMaxCluster];
-#pragma unroll
-    for (int c = 0; c < kMaxCluster; ++c) v[c] = c < CL ? cluster.map_shared_rank(base, c)[off] : 0;
-    int pre = 0, tot = 0;
-#pragma unroll
-    for (int c = 0; c < kMaxCluster; ++c) {
-        pre += c < crank ? v[c] : 0;
-        tot += v[c];
-    }
-    return make_int2(pre, tot);
+// Expert id of entry i (or -1 for none / out of range / past the end).
+__device__ __forceinline__ int load_expert(const int64_t *idx, int i, int i1, int E, uint32_t *status) {
+    if (i >= i1) return -1;
+    const int64_t e = idx[i];
+    if (e >= 0 && e < E) return (int)e;
+    if (e != -1) atomicOr(status, kStatusBadExpert);
+    return -1;
 }
 
 template <int NT>
@@ -90,6 +102,9 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     // quantising token rows now; it waits for these results before it reads
     // any slot.
     pdl_launch_dependents();
+    // peers may write into this CTA's shared memory only once every CTA of
+    // the cluster is running: arrive now, wait just before the first push
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     cg::cluster_group cluster = cg::this_cluster();
     const int CL = (int)cluster.num_blocks();
@@ -98,21 +113,17 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int E = p.E, R = p.R, K = p.K, T = p.T;
     const int N = (int)p.N;  // N*K < 2^31 (checked on the host)
-    const int per = (E + CL - 1) / CL;
+    const int ebits = bits_for(E + 1);  // keys 0..E-1 and E for "none"
 
     extern __shared__ int32_t sm[];
-    int32_t *hist_w = sm;                 // [NW][E] warp counts -> warp start positions
-    int32_t *cta_hist = hist_w + NW * E;  // [E]     read by peer CTAs
-    int32_t *hist_er = cta_hist + E;      // [E][R]  read by peer CTAs
-    int32_t *tok_rank = hist_er + E * R;  // [R]     read by peer CTAs
-    int32_t *epre = tok_rank + R;         // [E]     entries of e in lower CTAs
-    int32_t *ebase = epre + E;            // [E]     totals, then first rows
-    int32_t *scan = ebase + E;            // [NW+1]
-    int32_t *pair = scan + NW + 1;        // [per][R]
-    int16_t *stage = reinterpret_cast<int16_t *>(pair + per * R);  // [NW][tpw*K] expert ids
-
-    const int zero_words = NW * E + E + E * R + R;
-    for (int i = tid; i < zero_words; i += NT) sm[i] = 0;
+    int32_t *hist_w = sm;                   // [NW][E] warp counts -> warp start positions
+    int32_t *tok_rank = hist_w + NW * E;    // [R]     this CTA's tokens per rank
+    int32_t *recv_hist = tok_rank + R;      // [CL][E] per-expert totals of every CTA (pushed)
+    int32_t *recv_tok = recv_hist + CL * E; // [CL][R] tokens per rank of every CTA (pushed to CTA 0)
+    int32_t *epre = recv_tok + CL * R;      // [E]     entries of e in lower CTAs
+    int32_t *ebase = epre + E;              // [E]     first row of e
+    int32_t *scan = ebase + E;              // [NW+1]
+    int16_t *stage = reinterpret_cast<int16_t *>(scan + NW + 1);  // [NW][tpw*K] expert ids
 
     // contiguous token range per warp, warps of a CTA adjacent
     const int nwarps = CL * NW;
@@ -122,39 +133,38 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     const int t0 = min(cta_t1, cta_t0 + w * tpw);
     const int t1 = min(cta_t1, t0 + tpw);
     const int i0 = t0 * K, i1 = t1 * K;
-    // this warp's entry ids in shared memory for pass 2 (when they fit)
     int16_t *my_stage = p.staged ? stage + (size_t)w * tpw * K : nullptr;
 
-    // membership rows of this CTA's tokens start at zero
+    // first batch of entries in flight while shared memory is cleared
+    int ev[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) ev[u] = load_expert(p.topk_idx, i0 + u * 32 + lane, i1, E, p.status);
+
+    for (int i = tid; i < NW * E + R; i += NT) sm[i] = 0;
     if (p.is_token_in_rank) {
         for (int b = cta_t0 * R + tid; b < cta_t1 * R; b += NT) p.is_token_in_rank[b] = 0;
     }
+    if (p.cnt_er != nullptr) {  // owners clear their slice of the global (e, r) counts
+        const int per = (E + CL - 1) / CL;
+        const int j0 = min(E, crank * per) * R, j1 = min(E, crank * per + per) * R;
+        for (int j = j0 + tid; j < j1; j += NT) p.cnt_er[j] = 0;
+    }
     __syncthreads();
 
-    // ---------------- pass 1: counts (four loads in flight per lane)
-    constexpr int kU = 4;
+    // ---------------- pass 1: per-warp counts per expert
     for (int ib = i0; ib < i1; ib += 32 * kU) {
-        int64_t ev[kU];
+        if (ib != i0) {
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int i = ib + u * 32 + lane;
-            ev[u] = i < i1 ? p.topk_idx[i] : -1;
+            for (int u = 0; u < kU; ++u) ev[u] = load_expert(p.topk_idx, ib + u * 32 + lane, i1, E, p.status);
         }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int i = ib + u * 32 + lane;
-            const bool in = i < i1;
-            const int64_t e = ev[u];
-            const bool valid = in && e >= 0 && e < E;
-            if (in && (e < -1 || e >= E)) atomicOr(p.status, kStatusBadExpert);
-            if (in && my_stage) my_stage[i - i0] = valid ? (int16_t)e : (int16_t)-1;
-            const int key = valid ? (int)e * R + (i / K) / T : -1;
-            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key);
-            if (valid && lane == __ffs(peers) - 1) {
-                const int n = __popc(peers);
-                atomicAdd(&hist_w[w * E + (int)e], n);
-                atomicAdd(&hist_er[key], n);
-            }
+            const int e = ev[u];
+            if (i < i1 && my_stage) my_stage[i - i0] = (int16_t)e;
+            const uint32_t peers = warp_match(e < 0 ? E : e, ebits);
+            if (e >= 0 && lane == __ffs(peers) - 1) hist_w[w * E + e] += __popc(peers);
+            __syncwarp();
         }
     }
     if (p.tokens_per_rank || p.is_token_in_rank) {
@@ -177,7 +187,9 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     }
     __syncthreads();
 
-    // per expert: exclusive prefix over this CTA's warps, and the CTA total
+    // per expert: exclusive prefix over this CTA's warps; the CTA total goes
+    // to every CTA of the cluster (slot crank of their recv_hist)
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     for (int e = tid; e < E; e += NT) {
         int s = 0;
         for (int ww = 0; ww < NW; ++ww) {
@@ -185,27 +197,31 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
             hist_w[ww * E + e] = s;
             s += v;
         }
-        cta_hist[e] = s;
+        for (int c = 0; c < CL; ++c) cluster.map_shared_rank(recv_hist, c)[crank * E + e] = s;
     }
-    cluster.sync();  // every CTA's cta_hist / hist_er / tok_rank is final
+    if (p.tokens_per_rank) {
+        int32_t *dst = cluster.map_shared_rank(recv_tok, 0);
+        for (int d = tid; d < R; d += NT) dst[crank * R + d] = tok_rank[d];
+    }
+    cluster.sync();  // every CTA's totals are in every CTA's shared memory
 
     // per expert: entries in lower-ranked CTAs, and the total over the cluster
     for (int e = tid; e < E; e += NT) {
-        const int2 pt = cluster_sum_below(cluster, cta_hist, e, CL, crank);
-        epre[e] = pt.x;
-        ebase[e] = pt.y;
-    }
-    // counts per (expert, source rank) for this CTA's slice of experts
-    const int pe0 = min(E, crank * per), pe1 = min(E, pe0 + per);
-    const int npairs = (pe1 - pe0) * R;
-    for (int q = tid; q < npairs; q += NT) {
-        const int j = pe0 * R + q;
-        const int v = cluster_sum_below(cluster, hist_er, j, CL, 0).y;
-        pair[q] = v;
-        p.cnt_er[j] = v;
+        int pre = 0, tot = 0;
+        for (int c = 0; c < CL; ++c) {
+            const int v = recv_hist[c * E + e];
+            pre += c < crank ? v : 0;
+            tot += v;
+        }
+        epre[e] = pre;
+        ebase[e] = tot;
     }
     if (crank == 0 && p.tokens_per_rank) {
-        for (int d = tid; d < R; d += NT) p.tokens_per_rank[d] = cluster_sum_below(cluster, tok_rank, d, CL, 0).y;
+        for (int d = tid; d < R; d += NT) {
+            int v = 0;
+            for (int c = 0; c < CL; ++c) v += recv_tok[c * R + d];
+            p.tokens_per_rank[d] = v;
+        }
     }
     __syncthreads();
 
@@ -231,42 +247,28 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
             ebase[e] = b;
         }
     }
-    for (int e = pe0 + tid; e < pe1; e += NT) {
-        int run = 0;
-        for (int r = 0; r < R; ++r) {
-            p.off_er[e * R + r] = run;
-            run += pair[(e - pe0) * R + r];
-        }
-    }
-    // start position of each warp within each expert
-    for (int i = tid; i < NW * E; i += NT) hist_w[i] += epre[i % E];
-    cluster.sync();  // peers are done reading this CTA's shared memory
+    __syncthreads();
 
     // ---------------- pass 2: rows, in (g, k) order
     const uint32_t lt = lanemask_lt();
     const int cap = (int)min(p.cap, (int64_t)0x7FFFFFFF);
+    const bool want_er = p.cnt_er != nullptr;
+    const int erbits = bits_for(E * R + 1);
     for (int ib = i0; ib < i1; ib += 32 * kU) {
-        int ev[kU];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int i = ib + u * 32 + lane;
-            if (i >= i1) {
-                ev[u] = -1;
-            } else if (my_stage) {
-                ev[u] = my_stage[i - i0];
-            } else {
-                const int64_t e = p.topk_idx[i];
-                ev[u] = (e >= 0 && e < E) ? (int)e : -1;
-            }
+            if (my_stage) ev[u] = i < i1 ? my_stage[i - i0] : -1;
+            else ev[u] = load_expert(p.topk_idx, i, i1, E, p.status);
         }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int i = ib + u * 32 + lane;
             const int e = ev[u];
             const bool valid = e >= 0;
-            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+            const uint32_t peers = warp_match(valid ? e : E, ebits);
             int pos = 0;
-            if (valid) pos = hist_w[w * E + e] + __popc(peers & lt);
+            if (valid) pos = epre[e] + hist_w[w * E + e] + __popc(peers & lt);
             __syncwarp();
             if (valid && lane == __ffs(peers) - 1) hist_w[w * E + e] += __popc(peers);
             __syncwarp();
@@ -282,18 +284,53 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
                 }
                 p.slot[i] = s;
             }
+            if (want_er) {  // entries per (expert, source rank), one atomic per key per round
+                const int key = valid ? e * R + (i / K) / T : E * R;
+                const uint32_t pk = warp_match(key, erbits);
+                if (valid && lane == __ffs(pk) - 1) atomicAdd(&p.cnt_er[key], __popc(pk));
+            }
+        }
+    }
+
+    if (want_er) {
+        cluster.sync();  // every CTA's (e, r) counts have landed in global memory
+        // owners: off_er[e][r] = exclusive prefix over r, one warp per expert
+        const int per = (E + CL - 1) / CL;
+        const int pe0 = min(E, crank * per), pe1 = min(E, pe0 + per);
+        for (int e = pe0 + w; e < pe1; e += NW) {
+            int run = 0;
+            for (int r0 = 0; r0 < R; r0 += 32) {
+                const int r = r0 + lane;
+                const int v = r < R ? __ldcg(&p.cnt_er[e * R + r]) : 0;
+                int x = v;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int y = __shfl_up_sync(0xFFFFFFFFu, x, d);
+                    if (lane >= d) x += y;
+                }
+                if (r < R) p.off_er[e * R + r] = run + x - v;
+                run += __shfl_sync(0xFFFFFFFFu, x, 31);
+            }
         }
     }
 }
 
+size_t smem_words(int E, int R, int NT, int CL) {
+    const size_t NW = NT / 32;
+    return NW * E + R + (size_t)CL * E + (size_t)CL * R + 2 * (size_t)E + NW + 1;
+}
+
+// stage bytes for the per-warp copies of the entries' expert ids
+size_t stage_bytes(int64_t N, int K, int NT, int CL) {
+    const int64_t nwarps = (int64_t)CL * (NT / 32);
+    const int64_t tpw = (N + nwarps - 1) / nwarps;
+    return (size_t)(NT / 32) * tpw * K * sizeof(int16_t);
+}
+
 template <int NT>
 cudaError_t launch_nt(LayoutParams p, int cl, cudaStream_t stream) {
-    size_t smem = layout_smem_bytes(p.E, p.R, NT, cl);
-    // stage the entries' expert ids in shared memory for the second pass
-    // when they fit next to the histograms
-    const int64_t nwarps = (int64_t)cl * (NT / 32);
-    const int64_t tpw = (p.N + nwarps - 1) / nwarps;
-    const size_t stage = (size_t)(NT / 32) * tpw * p.K * sizeof(int16_t);
+    size_t smem = smem_words(p.E, p.R, NT, cl) * sizeof(int32_t);
+    const size_t stage = stage_bytes(p.N, p.K, NT, cl);
     p.staged = (smem + stage <= kMaxSmem) ? 1 : 0;
     if (p.staged) smem += (stage + 15) / 16 * 16;
     cudaLaunchConfig_t cfg = {};
@@ -313,7 +350,7 @@ cudaError_t launch_nt(LayoutParams p, int cl, cudaStream_t stream) {
 
 template <int NT>
 bool fits(int E, int R, int cl) {
-    const size_t smem = layout_smem_bytes(E, R, NT, cl);
+    const size_t smem = smem_words(E, R, NT, cl) * sizeof(int32_t);
     if (smem > kMaxSmem) return false;
     auto k = layout_kernel<NT>;
     // the limit is set to the most any shape needs, so contexts of different
@@ -345,10 +382,7 @@ bool fits(int E, int R, int cl) {
 }  // namespace
 
 size_t layout_smem_bytes(int E, int R, int threads, int cluster_size) {
-    const size_t NW = threads / 32;
-    const size_t per = (E + cluster_size - 1) / cluster_size;
-    const size_t words = NW * E + E + (size_t)E * R + R + E + E + (NW + 1) + per * R;
-    return words * sizeof(int32_t);
+    return smem_words(E, R, threads, cluster_size) * sizeof(int32_t);
 }
 
 bool layout_pick_shape(int E, int R, int *cluster_size, int *threads) {

@@ -56,7 +56,7 @@ class ep_handle_info(ctypes.Structure):
                 ("rows", ctypes.c_int64), ("slot", ctypes.c_void_p),
                 ("src_info", ctypes.c_void_p), ("cnt_er", ctypes.c_void_p),
                 ("off_er", ctypes.c_void_p), ("base", ctypes.c_void_p),
-                ("tokens_per_expert", ctypes.c_void_p)]
+                ("tokens_per_expert", ctypes.c_void_p), ("has_rank_ranges", ctypes.c_int32)]
 
 
 _lib = None

@@ -121,6 +121,9 @@ typedef struct ep_handle_info {
     int32_t *off_er;           /* [E, R]  first row of (e, r) relative to base[e] */
     int64_t *base;             /* [E]     first receive row of expert e */
     int32_t *tokens_per_expert;/* [E]     rows expert e receives */
+    int32_t has_rank_ranges;   /* 1: cnt_er / off_er belong to the layout held
+                                  (ep_get_dispatch_layout computes them; the
+                                  layout computed inside ep_dispatch does not) */
 } ep_handle_info;
 
 /* Human-readable name of a status code (static string). */

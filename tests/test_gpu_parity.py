@@ -42,6 +42,7 @@ def _check_layout(w, idx, buf=None, expect_status=ep.EP_OK):
     ntr, nte, itr, h = buf.get_dispatch_layout(torch.from_numpy(idx).cuda())
     assert buf.device_status() == expect_status
     t = h.tensors()
+    assert h.info().has_rank_ranges == 1
     assert np.array_equal(t["slot"].cpu().numpy(), o["slot"])
     rows = valid_rows(o["slot"])
     assert np.array_equal(t["src_info"].cpu().numpy()[rows], o["src_info"][rows])
@@ -171,6 +172,8 @@ def test_dispatch_parity(name, reuse):
                                              use_fp8=w.use_fp8, out=(recv, scales))
     assert buf.device_status() == ep.EP_OK
     assert np.array_equal(cnt.cpu().numpy(), o["tokens_per_expert"])
+    # per-(expert, rank) ranges come with the explicit layout call only
+    assert h.info().has_rank_ranges == (1 if reuse else 0)
     slot = o["slot"]
     rows = valid_rows(slot)
     g_of = np.nonzero(slot.reshape(-1) >= 0)[0] // w.topk
