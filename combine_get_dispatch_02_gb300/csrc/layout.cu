@@ -87,10 +87,14 @@ __device__ int block_exclusive_scan(int v, int *scan, int *total) {
     return excl;
 }
 
-// Expert id of entry i (or -1 for none / out of range / past the end).
-__device__ __forceinline__ int load_expert(const int64_t *idx, int i, int i1, int E, uint32_t *status) {
-    if (i >= i1) return -1;
-    const int64_t e = idx[i];
+// Raw topk_idx entry i, or -1 past the end (no branch on the loaded value, so
+// several of these stay in flight).
+__device__ __forceinline__ int64_t load_raw(const int64_t *idx, int i, int i1) {
+    return i < i1 ? __ldg(idx + i) : -1;
+}
+
+// Expert id of a raw entry, -1 for "none"; ids outside [-1, E) are flagged.
+__device__ __forceinline__ int to_expert(int64_t e, int E, uint32_t *status) {
     if (e >= 0 && e < E) return (int)e;
     if (e != -1) atomicOr(status, kStatusBadExpert);
     return -1;
@@ -136,9 +140,9 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     int16_t *my_stage = p.staged ? stage + (size_t)w * tpw * K : nullptr;
 
     // first batch of entries in flight while shared memory is cleared
-    int ev[kU];
+    int64_t raw[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) ev[u] = load_expert(p.topk_idx, i0 + u * 32 + lane, i1, E, p.status);
+    for (int u = 0; u < kU; ++u) raw[u] = load_raw(p.topk_idx, i0 + u * 32 + lane, i1);
 
     for (int i = tid; i < NW * E + R; i += NT) sm[i] = 0;
     if (p.is_token_in_rank) {
@@ -155,12 +159,13 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     for (int ib = i0; ib < i1; ib += 32 * kU) {
         if (ib != i0) {
 #pragma unroll
-            for (int u = 0; u < kU; ++u) ev[u] = load_expert(p.topk_idx, ib + u * 32 + lane, i1, E, p.status);
+            for (int u = 0; u < kU; ++u) raw[u] = load_raw(p.topk_idx, ib + u * 32 + lane, i1);
         }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
+            if (ib + u * 32 >= i1) break;  // warp-uniform
             const int i = ib + u * 32 + lane;
-            const int e = ev[u];
+            const int e = to_expert(raw[u], E, p.status);
             if (i < i1 && my_stage) my_stage[i - i0] = (int16_t)e;
             const uint32_t peers = warp_match(e < 0 ? E : e, ebits);
             if (e >= 0 && lane == __ffs(peers) - 1) hist_w[w * E + e] += __popc(peers);
@@ -255,14 +260,22 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     const bool want_er = p.cnt_er != nullptr;
     const int erbits = bits_for(E * R + 1);
     for (int ib = i0; ib < i1; ib += 32 * kU) {
+        int ev[kU];
+        if (my_stage) {
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int i = ib + u * 32 + lane;
-            if (my_stage) ev[u] = i < i1 ? my_stage[i - i0] : -1;
-            else ev[u] = load_expert(p.topk_idx, i, i1, E, p.status);
+            for (int u = 0; u < kU; ++u) {
+                const int i = ib + u * 32 + lane;
+                ev[u] = i < i1 ? my_stage[i - i0] : -1;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kU; ++u) raw[u] = load_raw(p.topk_idx, ib + u * 32 + lane, i1);
+#pragma unroll
+            for (int u = 0; u < kU; ++u) ev[u] = to_expert(raw[u], E, p.status);
         }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
+            if (ib + u * 32 >= i1) break;  // warp-uniform
             const int i = ib + u * 32 + lane;
             const int e = ev[u];
             const bool valid = e >= 0;
