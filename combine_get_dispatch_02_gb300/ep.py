@@ -34,7 +34,7 @@ ENTRY_POINTS = (
     "ep_status_str", "ep_config_check", "ep_recv_rows", "ep_recv_bytes",
     "ep_create", "ep_destroy", "ep_handle_create", "ep_handle_destroy",
     "ep_handle_get_info", "ep_get_dispatch_layout", "ep_dispatch", "ep_combine",
-    "ep_get_device_status",
+    "ep_get_device_status", "ep_dispatch_noalloc",
 )
 
 
@@ -87,6 +87,7 @@ def lib() -> ctypes.CDLL:
             "ep_dispatch": (I32, [P, P, P, I32, I32, P, P, P, P, P]),
             "ep_combine": (I32, [P, P, P, P, P, P]),
             "ep_get_device_status": (I32, [P, P]),
+            "ep_dispatch_noalloc": (I32, [CFG, P, P, I32, I32, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -202,3 +203,15 @@ def ep_combine(ctx, y: torch.Tensor, topk_weights: torch.Tensor | None, handle,
 
 def ep_get_device_status(ctx, stream=None) -> int:
     return lib().ep_get_device_status(ctx, _stream(stream))
+
+
+def ep_dispatch_noalloc(cfg: ep_config, x: torch.Tensor, topk_idx: torch.Tensor, tokens_per_rank: int,
+                        use_fp8: bool, recv_x: torch.Tensor, recv_scales: torch.Tensor | None,
+                        recv_count: torch.Tensor | None, stream=None) -> None:
+    """Dispatch without any device allocation (intermediate state in the
+    library's static device array); see include/ep.h for limits."""
+    _check(lib().ep_dispatch_noalloc(
+        ctypes.byref(cfg), _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int64, "topk_idx"),
+        int(tokens_per_rank), int(bool(use_fp8)), _ptr(recv_x, None, "recv_x"),
+        _ptr(recv_scales, torch.float32, "recv_scales"), _ptr(recv_count, torch.int32, "recv_count"),
+        _stream(stream)), "ep_dispatch_noalloc")

@@ -203,6 +203,30 @@ ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
 ep_status ep_combine(ep_ctx *ctx, const void *d_y, const float *d_topk_weights,
                      const ep_handle *handle, void *d_out, void *stream);
 
+/* Dispatch for callers that cannot allocate device memory (no counterpart on
+ * the pages: it is this library's own addition).  Same operation and output as
+ * ep_dispatch with d_topk_idx given (layout, then BF16 copy or FP8 cast into
+ * d_recv_x / d_recv_scales, rows per expert into d_recv_count), but it needs
+ * no context or handle: every intermediate buffer lives in one static device
+ * array that libep.so holds on each GPU that loads it (about 4.3 MB, kept
+ * until the process exits).  It calls no cudaMalloc, cudaFree or allocating
+ * library routine, so code inside a stream capture that must not allocate,
+ * runtimes that give all device memory to their own allocator, and plugins
+ * that may only use the memory they are handed can still dispatch.
+ *   cfg            sizes and layout, as for ep_create (host pointer)
+ *   other args     as for ep_dispatch
+ * Limits: R*tokens_per_rank*K <= 65536 entries, receive rows <= 1048576,
+ * num_experts <= 1024; beyond them it returns EP_ERR_UNSUPPORTED and enqueues
+ * nothing.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and sets kernel attributes; make it before any stream
+ * capture.  All calls share the array and each clears the status word it uses
+ * first: calls whose work overlaps on the GPU race.  Device-detected errors
+ * (ids outside [-1, E), padded overflow) drop the offending entries as in
+ * ep_dispatch but are not reported (there is no context to report them to). */
+ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, const int64_t *d_topk_idx,
+                              int32_t tokens_per_rank, int32_t use_fp8, void *d_recv_x,
+                              float *d_recv_scales, int32_t *d_recv_count, void *stream);
+
 /* Synchronise `stream`, read and clear the context's device status word.
  * Returns EP_OK, EP_ERR_BAD_EXPERT, EP_ERR_CAPACITY or EP_ERR_CUDA. */
 ep_status ep_get_device_status(ep_ctx *ctx, void *stream);
