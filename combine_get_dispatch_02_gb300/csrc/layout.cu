@@ -20,9 +20,12 @@
 //     (distributed shared memory) and, after one hardware cluster barrier,
 //     every CTA holds all totals locally: its prefix, the grand totals and the
 //     bases follow without global atomics, spin-waits or a second launch.
-//   * Pass 2: each warp walks its entries again (from a shared-memory copy
-//     when it fits); an entry's row is base + (entries of the expert before
-//     this CTA) + (before this warp) + (earlier in this warp).
+//   * Pass 1 also records each entry's position among its warp's entries of
+//     the same expert (in a shared-memory copy of the warp's entries when it
+//     fits), so pass 2 needs no cross-lane work: an entry's row is base +
+//     (entries of the expert in lower CTAs) + (in lower warps) + (its
+//     position in the warp).  Without the copy pass 2 re-derives the
+//     positions from topk_idx.
 //   * Per-(expert, source rank) ranges (cnt_er / off_er) are optional: pass 2
 //     adds the per-round counts to the zeroed global cnt_er, and after a
 //     second cluster barrier the owner CTAs turn them into offsets.
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     int32_t *epre = recv_tok + CL * R;      // [E]     entries of e in lower CTAs
     int32_t *ebase = epre + E;              // [E]     first row of e
     int32_t *scan = ebase + E;              // [NW+1]
-    int16_t *stage = reinterpret_cast<int16_t *>(scan + NW + 1);  // [NW][tpw*K] expert ids
+    int32_t *stage = scan + NW + 1;         // [NW][tpw*K] (position in warp << 11) | (expert + 1)
 
     // contiguous token range per warp, warps of a CTA adjacent
     const int nwarps = CL * NW;
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     const int t0 = min(cta_t1, cta_t0 + w * tpw);
     const int t1 = min(cta_t1, t0 + tpw);
     const int i0 = t0 * K, i1 = t1 * K;
-    int16_t *my_stage = p.staged ? stage + (size_t)w * tpw * K : nullptr;
+    int32_t *my_stage = p.staged ? stage + (size_t)w * tpw * K : nullptr;
 
     // first batch of entries in flight while shared memory is cleared
     int64_t raw[kU];
@@ -166,10 +169,14 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
             if (ib + u * 32 >= i1) break;  // warp-uniform
             const int i = ib + u * 32 + lane;
             const int e = to_expert(raw[u], E, p.status);
-            if (i < i1 && my_stage) my_stage[i - i0] = (int16_t)e;
             const uint32_t peers = warp_match(e < 0 ? E : e, ebits);
+            // position of this entry among the warp's entries of expert e
+            int local = 0;
+            if (e >= 0) local = hist_w[w * E + e] + __popc(peers & lanemask_lt());
+            __syncwarp();
             if (e >= 0 && lane == __ffs(peers) - 1) hist_w[w * E + e] += __popc(peers);
             __syncwarp();
+            if (i < i1 && my_stage) my_stage[i - i0] = (local << 11) | (e + 1);
         }
     }
     if (p.tokens_per_rank || p.is_token_in_rank) {
@@ -259,13 +266,31 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     const int cap = (int)min(p.cap, (int64_t)0x7FFFFFFF);
     const bool want_er = p.cnt_er != nullptr;
     const int erbits = bits_for(E * R + 1);
-    for (int ib = i0; ib < i1; ib += 32 * kU) {
+    if (my_stage && !want_er) {
+        // every entry's position inside its warp is known: rows follow directly
+        for (int i = i0 + lane; i < i1; i += 32) {
+            const int v = my_stage[i - i0];
+            const int e = (v & 2047) - 1;
+            int32_t s = -1;
+            if (e >= 0) {
+                const int pos = epre[e] + hist_w[w * E + e] + (v >> 11);
+                if (pos < cap) {
+                    s = ebase[e] + pos;
+                    p.src_info[s] = i;
+                } else {
+                    atomicOr(p.status, kStatusCapacity);
+                }
+            }
+            p.slot[i] = s;
+        }
+    }
+    for (int ib = (my_stage && !want_er) ? i1 : i0; ib < i1; ib += 32 * kU) {
         int ev[kU];
         if (my_stage) {
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 const int i = ib + u * 32 + lane;
-                ev[u] = i < i1 ? my_stage[i - i0] : -1;
+                ev[u] = i < i1 ? (my_stage[i - i0] & 2047) - 1 : -1;
             }
         } else {
 #pragma unroll
@@ -337,7 +362,7 @@ size_t smem_words(int E, int R, int NT, int CL) {
 size_t stage_bytes(int64_t N, int K, int NT, int CL) {
     const int64_t nwarps = (int64_t)CL * (NT / 32);
     const int64_t tpw = (N + nwarps - 1) / nwarps;
-    return (size_t)(NT / 32) * tpw * K * sizeof(int16_t);
+    return (size_t)(NT / 32) * tpw * K * sizeof(int32_t);
 }
 
 template <int NT>
@@ -400,9 +425,9 @@ size_t layout_smem_bytes(int E, int R, int threads, int cluster_size) {
 
 bool layout_pick_shape(int E, int R, int *cluster_size, int *threads) {
     static const int cls[] = {16, 8, 4, 2, 1};
-    for (int cl : cls) {
-        if (fits<1024>(E, R, cl)) { *cluster_size = cl; *threads = 1024; return true; }
+    for (int cl : cls) {  // 512 threads measured fastest at the low-latency sizes
         if (fits<512>(E, R, cl)) { *cluster_size = cl; *threads = 512; return true; }
+        if (fits<1024>(E, R, cl)) { *cluster_size = cl; *threads = 1024; return true; }
         if (fits<256>(E, R, cl)) { *cluster_size = cl; *threads = 256; return true; }
     }
     return false;
