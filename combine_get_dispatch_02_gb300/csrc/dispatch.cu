@@ -7,7 +7,11 @@
 // cast is per 128 channels: amax = max |x|, a = max(amax, 1e-4),
 // scale = a / 448, q = e4m3(x * (448 / a)), nearest-even with saturation.
 //
-// Design: the work item is (token, 512-channel chunk) for one warp, 16
+// Two kernels.  For hidden sizes that are a multiple of 512 (all the
+// workloads) the row kernel below stages a whole token row in shared memory
+// and writes it with bulk asynchronous copies.  Otherwise the warp-item
+// kernel does:
+// the work item is (token, 512-channel chunk) for one warp, 16
 // channels (two 16-byte loads) per lane.  The token row is read once from
 // HBM (read-only, no L1 allocation), cast once, and written K times with
 // 16-byte streaming stores, so the kernel moves the algorithmic bytes and
@@ -108,6 +112,123 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const DispatchParams
     }
 }
 
+// ---------------------------------------------------------------- row kernel
+// One CTA per token at a time (H/16 threads, 16 channels each): the row is
+// loaded once, cast once (FP8) and laid out in shared memory, then one
+// thread issues K bulk asynchronous copies (cp.async.bulk) of the whole row
+// (and of its scale row) to the K receive rows.  Each destination row is
+// written as one contiguous transfer by the copy engine instead of 512-byte
+// pieces from many warps.  Two row buffers alternate, so the casts of the
+// next token overlap the copies of the previous one; the next token's row
+// and slots are loaded while the current one is cast.  Needs H % 512 == 0
+// and H <= 16384.
+constexpr int kRowBlocksPerSM = 2;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most one committed group still reads shared memory
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchParams p) {
+    extern __shared__ __align__(128) uint8_t row_smem[];
+    const int H = p.H, K = p.K;
+    const int t = threadIdx.x, lane = t & 31;
+    const int payload = FP8 ? H : 2 * H;             // bytes of one receive row
+    const int rowb = FP8 ? H + H / 32 : 2 * H;       // bytes of one buffer
+    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(p.x);
+
+    int64_t g = blockIdx.x;
+    uint4 a = make_uint4(0, 0, 0, 0), b = a;
+    if (g < p.N) {
+        a = ld_nc_na_v4(x + g * H + t * 16);
+        b = ld_nc_na_v4(x + g * H + t * 16 + 8);
+    }
+    pdl_wait();  // slots come from the layout kernel
+    if (p.count_dst != nullptr && blockIdx.x == 0)
+        for (int e = t; e < p.E; e += blockDim.x) p.count_dst[e] = p.count_src[e];
+    int32_t slot_next = (g < p.N && t < K) ? p.slot[g * K + t] : -1;
+
+    for (int it = 0; g < p.N; g += gridDim.x, ++it) {
+        uint8_t *row = row_smem + (it & 1) * rowb;
+        const uint4 ca = a, cb = b;
+        const int32_t my_slot = slot_next;
+        const int64_t gn = g + gridDim.x;
+        if (gn < p.N) {
+            a = ld_nc_na_v4(x + gn * H + t * 16);
+            b = ld_nc_na_v4(x + gn * H + t * 16 + 8);
+            slot_next = t < K ? p.slot[gn * K + t] : -1;
+        }
+        uint4 q = make_uint4(0, 0, 0, 0);
+        float scale = 0.0f;
+        if constexpr (FP8) {
+            const uint32_t u[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+            float f[16];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                f[2 * j] = bf16_lo(u[j]);
+                f[2 * j + 1] = bf16_hi(u[j]);
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+            const float ac = fmaxf(amax, 1e-4f);
+            scale = __fdiv_rn(ac, 448.0f);
+            const float inv = __fdiv_rn(448.0f, ac);
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t lo = cast_pair(__fmul_rn(f[4 * j], inv), __fmul_rn(f[4 * j + 1], inv));
+                const uint32_t hi = cast_pair(__fmul_rn(f[4 * j + 2], inv), __fmul_rn(f[4 * j + 3], inv));
+                w[j] = lo | (hi << 16);
+            }
+            q = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        // this buffer was last filled two tokens ago: its copies must have read it
+        if (it >= 2 && t == 0) bulk_wait_read_1();
+        __syncthreads();
+        if constexpr (FP8) {
+            *reinterpret_cast<uint4 *>(row + t * 16) = q;
+            if ((lane & 7) == 0) reinterpret_cast<float *>(row + H)[t >> 3] = scale;
+        } else {
+            *reinterpret_cast<uint4 *>(row + t * 32) = ca;
+            *reinterpret_cast<uint4 *>(row + t * 32 + 16) = cb;
+        }
+        fence_proxy_async_smem();  // make the row visible to the copy engine
+        __syncthreads();
+        if (t < 32) {
+#pragma unroll 1
+            for (int k = 0; k < K; ++k) {
+                const int32_t s = __shfl_sync(0xFFFFFFFFu, my_slot, k);
+                if (lane == 0 && s >= 0) {
+                    bulk_store(static_cast<uint8_t *>(p.recv) + (int64_t)s * payload, smem_addr(row), payload);
+                    if constexpr (FP8)
+                        bulk_store(p.recv_scales + (int64_t)s * (H / 128), smem_addr(row + H), H / 32);
+                }
+            }
+            if (lane == 0) bulk_commit();
+        }
+    }
+    if (t == 0) bulk_wait_all();  // copies read shared memory until they finish
+}
+
+bool row_kernel_fits(int H) { return H % 512 == 0 && H / 16 <= 1024; }
+
+size_t row_smem_bytes(bool fp8, int H) { return 2 * (size_t)(fp8 ? H + H / 32 : 2 * H); }
+
 template <bool FP8>
 int blocks_per_sm() {
     int n = 0;
@@ -122,8 +243,34 @@ int blocks_per_sm() {
 
 int dispatch_blocks_per_sm(bool fp8) { return fp8 ? blocks_per_sm<true>() : blocks_per_sm<false>(); }
 
+void dispatch_init() {
+    // the row kernel's shared memory can exceed the 48 KB default (BF16, H > 6144)
+    cudaFuncSetAttribute(dispatch_row_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)row_smem_bytes(false, 16384));
+    cudaFuncSetAttribute(dispatch_row_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)row_smem_bytes(true, 16384));
+    cudaGetLastError();
+}
+
 cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks, bool pdl,
                             cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (row_kernel_fits(p.H) && p.row_sms > 0) {
+        int64_t blocks = (int64_t)p.row_sms * kRowBlocksPerSM;
+        if (blocks > p.N) blocks = p.N;
+        if (blocks < 1) blocks = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+        cfg.blockDim = dim3(p.H / 16, 1, 1);
+        cfg.dynamicSmemBytes = row_smem_bytes(fp8, p.H);
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        return fp8 ? cudaLaunchKernelEx(&cfg, dispatch_row_kernel<true>, p)
+                   : cudaLaunchKernelEx(&cfg, dispatch_row_kernel<false>, p);
+    }
     const int nch = (p.H + kChunk - 1) / kChunk;
     const int64_t warps = p.N * nch;
     int64_t blocks = (warps + (kThreads / 32) - 1) / (kThreads / 32);
@@ -134,9 +281,6 @@ cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks, b
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return fp8 ? cudaLaunchKernelEx(&cfg, dispatch_kernel<true>, p)

@@ -174,6 +174,7 @@ ep_status ep_create(const ep_config *cfg, ep_ctx **out) {
     ctx->dispatch_bps_bf16 = ep::dispatch_blocks_per_sm(false);
     ctx->dispatch_bps_fp8 = ep::dispatch_blocks_per_sm(true);
     ctx->combine_bps = ep::combine_blocks_per_sm();
+    ep::dispatch_init();
     if (cudaMalloc(&ctx->d_status, sizeof(uint32_t)) != cudaSuccess) {
         cudaGetLastError();
         free(ctx);
@@ -309,6 +310,7 @@ ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, i
     p.count_src = handle->tokens_per_expert;
     p.count_dst = fresh ? nullptr : d_recv_count;
     p.E = c.num_experts;
+    p.row_sms = (c.max_sms > 0 && c.max_sms < ctx->num_sms) ? c.max_sms : ctx->num_sms;
     const int cap = grid_cap(ctx, use_fp8 ? ctx->dispatch_bps_fp8 : ctx->dispatch_bps_bf16);
     if (ep::launch_dispatch(p, use_fp8 != 0, cap, /*pdl=*/true, st) != cudaSuccess) {
         cudaGetLastError();

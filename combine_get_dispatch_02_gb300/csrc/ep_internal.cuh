@@ -55,12 +55,15 @@ struct DispatchParams {
     const int32_t *count_src;  // [E] copied to count_dst by block 0, or nullptr
     int32_t *count_dst;
     int32_t E;
+    int32_t row_sms;           // SMs for the row kernel (H % 512 == 0), 0 = use the warp-item kernel
 };
 
 cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks,
                             bool pdl, cudaStream_t stream);
-// Resident blocks per SM of the dispatch kernel (for grid sizing).
+// Resident blocks per SM of the warp-item dispatch kernel (for grid sizing).
 int dispatch_blocks_per_sm(bool fp8);
+// One-time kernel attribute set-up (call with the device current).
+void dispatch_init();
 
 // ------------------------------------------------------------------ combine
 struct CombineParams {

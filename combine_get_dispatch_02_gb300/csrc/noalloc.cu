@@ -98,6 +98,7 @@ extern "C" ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, 
             d.scratch = static_cast<unsigned char *>(ptr);
             d.bps_bf16 = ep::dispatch_blocks_per_sm(false);
             d.bps_fp8 = ep::dispatch_blocks_per_sm(true);
+            ep::dispatch_init();
             d.shape_E = d.shape_R = -1;
             d.ready = true;
         }
@@ -155,6 +156,7 @@ extern "C" ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, 
     dp.E = c.num_experts;
     int sms = s.num_sms;
     if (c.max_sms > 0 && c.max_sms < sms) sms = c.max_sms;
+    dp.row_sms = sms;
     const int cap = sms * (use_fp8 ? s.bps_fp8 : s.bps_bf16);
     if (ep::launch_dispatch(dp, use_fp8 != 0, cap, /*pdl=*/true, st) != cudaSuccess) {
         cudaGetLastError();
