@@ -50,6 +50,10 @@ def _args():
     ap.add_argument("--breakdown-reps", type=int, default=200)
     ap.add_argument("--layout", choices=["padded", "packed"], default=None,
                     help="override the workload's receive layout (packed keeps a profiled run small)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the sweep grid (one JSON line per point) instead of the bench step")
+    ap.add_argument("--sweep-filter", default="", help="only sweep points whose name contains this")
+    ap.add_argument("--sweep-reps", type=int, default=10)
     return ap.parse_args()
 
 
@@ -369,6 +373,31 @@ def run_ours(args):
                                            None, stream))
     comb_us = timed(lambda: ep.ep_combine(ctx, y, wts, h.raw, out, stream))
 
+    # the same step captured once in a CUDA graph and replayed (no host
+    # launch overhead; programmatic dependent launch becomes a graph edge)
+    graph_us = None
+    try:
+        s_cap = torch.cuda.Stream()
+        s_cap.wait_stream(stream)
+        with torch.cuda.stream(s_cap):
+            for _ in range(2):
+                ep.ep_dispatch(ctx, x, idx, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales, cnt, s_cap)
+                ep.ep_combine(ctx, y, wts, h.raw, out, s_cap)
+        stream.wait_stream(s_cap)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s_cap):
+            ep.ep_dispatch(ctx, x, idx, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales, cnt, s_cap)
+            ep.ep_combine(ctx, y, wts, h.raw, out, s_cap)
+        graph_us = timed(graph.replay)
+    except Exception as exc:  # report, do not hide, a capture failure
+        graph_us = (f"capture failed: {exc}", None)
+
+    # HBM copy bandwidth of this GPU through torch (context for the fractions)
+    cbuf = torch.empty(2 << 30, dtype=torch.uint8, device="cuda")
+    cdst = torch.empty_like(cbuf)
+    copy_gbs = 2 * cbuf.numel() / (timed(lambda: cdst.copy_(cbuf), reps=10)[0] / 1e6) / 1e9
+    del cbuf, cdst
+
     # end to end through the public API with host buffers
     e2e = None if args.no_e2e else _e2e(args, w, d, x, idx, wts, out, ctx, h, recv, scales, cnt, y, stream)
     if buf.device_status() != ep.EP_OK:
@@ -379,7 +408,7 @@ def run_ours(args):
             torch.distributed.destroy_process_group()
         return
     _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
-            e2e, clk)
+            e2e, clk, graph_us, copy_gbs)
     if ws > 1:
         torch.distributed.destroy_process_group()
 
@@ -449,7 +478,7 @@ def _e2e(args, w, d, x, idx, wts, out, ctx, h, recv, scales, cnt, y, stream):
 
 
 def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
-            e2e, clk):
+            e2e, clk, graph_us=None, copy_gbs=None):
     peak, peak_kind = _peaks()
     disp_bytes, disp_kernel_bytes, comb_bytes = _algorithmic_bytes(w, M)
     comb_avg_s = statistics.mean(comb_ms) / 1e3
@@ -475,7 +504,9 @@ def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, la
             "layout_alone_median": lay_us[0],
             "dispatch_cached_layout_median": disp_us[0],
             "combine_alone_median": comb_us[0],
+            "step_cuda_graph_replay_median": graph_us[0] if graph_us else None,
         },
+        "hbm_copy_gbs_torch_here": copy_gbs,
         "roofline": {"bound": "hbm", "kernel": "combine", "achieved": comb_gbs, "peak": peak,
                      "unit": "GB/s", "frac": comb_gbs / peak, "traffic": traffic,
                      "algorithmic_bytes": comb_bytes, "peak_source": f"{peak_kind} HBM copy bandwidth"},
@@ -493,8 +524,82 @@ def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, la
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """Sweep grid (tokens per rank x R x H x E x K x {BF16, FP8}): per point the
+    median µs of layout + dispatch, dispatch with the cached layout and
+    combine, with the fraction of the HBM roofline.  Inputs are drawn on the
+    device from a seeded torch generator (timing only; parity is covered by
+    the tests)."""
+    import torch
+    from combine_get_dispatch_02_gb300 import Buffer, ep
+    from combine_get_dispatch_02_gb300 import build as epbuild
+    from combine_get_dispatch_02_gb300 import workloads as wl
+    epbuild.build()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = _peaks()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush_w = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
+    flush_r = torch.ones(2 * l2 // 4, dtype=torch.float32, device="cuda")
+    sink = torch.empty(1, device="cuda")
+
+    def timed(fn):
+        ts = []
+        for i in range(args.sweep_reps + 2):
+            flush_w.fill_(1)
+            torch.sum(flush_r, dim=0, keepdim=True, out=sink)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            if i >= 2:
+                ts.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median([a.elapsed_time(b) * 1e3 for a, b in ts])
+
+    for w in wl.sweep_points():
+        if args.sweep_filter not in w.name:
+            continue
+        N, K, H, E = w.num_tokens, w.topk, w.hidden, w.num_experts
+        gen = torch.Generator(device="cuda").manual_seed(w.seed)
+        x = torch.randn(N, H, device="cuda", generator=gen).to(torch.bfloat16)
+        logits = torch.randn(N, E, device="cuda", generator=gen)
+        top = torch.topk(logits, K, dim=1)
+        idx = top.indices.to(torch.int64).contiguous()
+        wts = torch.softmax(top.values, dim=1).contiguous()
+        buf = Buffer(w.num_ranks, w.max_tokens_per_rank, H, E, K, low_latency_mode=(w.layout == wl.PADDED))
+        recv, scales = buf.alloc_recv(w.use_fp8)
+        y = torch.empty(buf.rows, H, dtype=torch.bfloat16, device="cuda")
+        out = torch.empty(N, H, dtype=torch.bfloat16, device="cuda")
+        h = buf.new_handle()
+        ctx = buf.ctx
+        idx3 = idx.view(w.num_ranks, w.tokens_per_rank, K)
+        fresh = timed(lambda: ep.ep_dispatch(ctx, x, idx3, w.tokens_per_rank, w.use_fp8, h.raw, recv,
+                                             scales, None, stream))
+        cached = timed(lambda: ep.ep_dispatch(ctx, x, None, w.tokens_per_rank, w.use_fp8, h.raw, recv,
+                                              scales, None, stream))
+        comb = timed(lambda: ep.ep_combine(ctx, y, wts, h.raw, out, stream))
+        if buf.device_status() != ep.EP_OK:
+            raise RuntimeError(f"device status error at {w.name}")
+        M = N * K
+        _, disp_bytes, comb_bytes = _algorithmic_bytes(w, M)
+        line = {"point": w.name, "layout": w.layout, "tokens": N, "rows": M,
+                "us": {"layout_and_dispatch": fresh, "dispatch_cached_layout": cached, "combine": comb},
+                "hbm_frac": {"dispatch_cached_layout": disp_bytes / (cached / 1e6) / 1e9 / peak,
+                             "combine": comb_bytes / (comb / 1e6) / 1e9 / peak},
+                "tokens_per_s": {"dispatch_and_combine": N / ((fresh + comb) / 1e6)},
+                "peak_gbs": peak, "peak_source": peak_kind}
+        print(json.dumps(line), flush=True)
+        del buf, recv, scales, y, out, h, x, logits, idx, wts
+        torch.cuda.empty_cache()
+
+
 def main():
     args = _args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

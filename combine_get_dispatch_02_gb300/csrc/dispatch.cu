@@ -154,20 +154,19 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
         a = ld_nc_na_v4(x + g * H + t * 16);
         b = ld_nc_na_v4(x + g * H + t * 16 + 8);
     }
-    pdl_wait();  // slots come from the layout kernel
-    if (p.count_dst != nullptr && blockIdx.x == 0)
-        for (int e = t; e < p.E; e += blockDim.x) p.count_dst[e] = p.count_src[e];
-    int32_t slot_next = (g < p.N && t < K) ? p.slot[g * K + t] : -1;
+    // slots come from the layout kernel (launched just before with programmatic
+    // dependent launch): the first token is loaded, cast and laid out in
+    // shared memory before waiting for them
+    bool waited = false;
+    int32_t slot_next = -1;
 
     for (int it = 0; g < p.N; g += gridDim.x, ++it) {
         uint8_t *row = row_smem + (it & 1) * rowb;
         const uint4 ca = a, cb = b;
-        const int32_t my_slot = slot_next;
         const int64_t gn = g + gridDim.x;
         if (gn < p.N) {
             a = ld_nc_na_v4(x + gn * H + t * 16);
             b = ld_nc_na_v4(x + gn * H + t * 16 + 8);
-            slot_next = t < K ? p.slot[gn * K + t] : -1;
         }
         uint4 q = make_uint4(0, 0, 0, 0);
         float scale = 0.0f;
@@ -208,6 +207,15 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
             *reinterpret_cast<uint4 *>(row + t * 32 + 16) = cb;
         }
         fence_proxy_async_smem();  // make the row visible to the copy engine
+        if (!waited) {
+            pdl_wait();
+            waited = true;
+            if (p.count_dst != nullptr && blockIdx.x == 0)
+                for (int e = t; e < p.E; e += blockDim.x) p.count_dst[e] = p.count_src[e];
+            slot_next = t < K ? p.slot[g * K + t] : -1;
+        }
+        const int32_t my_slot = slot_next;
+        if (gn < p.N) slot_next = t < K ? p.slot[gn * K + t] : -1;
         __syncthreads();
         if (t < 32) {
 #pragma unroll 1
@@ -222,6 +230,9 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
             if (lane == 0) bulk_commit();
         }
     }
+    if (!waited) pdl_wait();  // a CTA without tokens still orders the count copy
+    if (!waited && p.count_dst != nullptr && blockIdx.x == 0)
+        for (int e = t; e < p.E; e += blockDim.x) p.count_dst[e] = p.count_src[e];
     if (t == 0) bulk_wait_all();  // copies read shared memory until they finish
 }
 

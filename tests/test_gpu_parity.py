@@ -72,6 +72,9 @@ LAYOUT_CASES = {
     "r16_e1024": wl.TINY.with_(num_ranks=16, num_experts=1024, topk=8, tokens_per_rank=40,
                                max_tokens_per_rank=64),
     "empty": wl.TINY.with_(tokens_per_rank=0),
+    # 1M entries: too many to keep a shared-memory copy per CTA, so the
+    # second pass re-reads topk_idx
+    "unstaged_packed": wl.LL.with_(tokens_per_rank=4096, max_tokens_per_rank=4096, layout=wl.PACKED),
 }
 
 
@@ -376,3 +379,18 @@ def test_empty_batch():
     assert buf.device_status() == ep.EP_OK
     assert out.shape == (0, w.hidden)
     assert int(cnt.sum().item()) == 0
+
+
+def test_fresh_dispatch_layout_unstaged():
+    """The layout computed inside ep_dispatch (no per-rank ranges) at a size
+    whose entries do not fit in shared memory."""
+    w = LAYOUT_CASES["unstaged_packed"]
+    d = wl.generate(w, with_x=False)
+    o = _orc_layout(w, d["topk_idx"])
+    buf = make_buffer(w)
+    x = torch.zeros(w.num_tokens, w.hidden, dtype=torch.bfloat16, device="cuda")
+    _, cnt, h = buf.low_latency_dispatch(x, torch.from_numpy(d["topk_idx"]).cuda(), w.max_tokens_per_rank,
+                                         w.num_experts, use_fp8=True)
+    assert buf.device_status() == ep.EP_OK
+    assert np.array_equal(h.tensors()["slot"].cpu().numpy(), o["slot"])
+    assert np.array_equal(cnt.cpu().numpy(), o["tokens_per_expert"])
