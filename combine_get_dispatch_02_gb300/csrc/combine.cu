@@ -8,12 +8,13 @@
 //   masked entries: acc = fma(w[g,k], y[row(g,k), c], acc)   (fp32)
 // so the result is identical to the oracle's bit for bit.
 //
-// Design: the work item is (token, 256-channel chunk) for one warp, 8
-// channels (one 16-byte row segment) per lane.  For each group of up to 8
-// entries the warp loads the slots and weights once (lanes 0..7, then
-// shuffles) and issues all of the group's 16-byte row loads before the first
-// FMA, so each lane has up to 128 bytes in flight; the rows are read-only and
-// bypass L1.  One 16-byte store per lane writes the bf16 result.
+// Design: the work item is (token, CPI 256-channel chunks) for one warp, 8
+// channels (one 16-byte row segment) per lane and chunk.  For each group of
+// 8/CPI entries the warp loads the slots and weights once (one lane each,
+// then shuffles) and issues all of the group's 16-byte row loads before the
+// first FMA, so each lane has 8 loads (128 bytes) in flight for any K; the
+// rows are read-only and bypass L1.  One 16-byte store per lane and chunk
+// writes the bf16 result.
 #include <cuda_bf16.h>
 
 #include "ep_internal.cuh"
@@ -23,63 +24,78 @@ namespace ep {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kChunk = 256;  // channels per warp item
-constexpr int kGroup = 8;    // entries whose loads are in flight together
+constexpr int kChunk = 256;  // channels per lane-row segment (8 per lane)
+constexpr int kLoads = 8;    // 16-byte row loads in flight per lane
 
+// CPI = 256-channel chunks per warp item; entries are taken kLoads / CPI at a
+// time, so every group keeps kLoads loads in flight whatever K is (CPI = 1
+// for K > 4, 2 for K 3..4, 4 for K <= 2).
+template <int CPI>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p) {
+    constexpr int G = kLoads / CPI;  // entries per group
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const int64_t nwarp = ((int64_t)gridDim.x * kThreads) >> 5;
     const int H = p.H, K = p.K;
-    const int nch = (H + kChunk - 1) / kChunk;
+    const int nch = (H + kChunk * CPI - 1) / (kChunk * CPI);
     const int64_t items = p.N * nch;
     const __nv_bfloat16 *y = static_cast<const __nv_bfloat16 *>(p.y);
 
     for (int64_t it = warp; it < items; it += nwarp) {
         const int64_t g = it / nch;
-        const int c = (int)(it - g * nch) * kChunk + lane * 8;
-        const bool act = c < H;
-        float acc[8];
+        const int c0 = (int)(it - g * nch) * kChunk * CPI + lane * 8;
+        float acc[CPI][8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+        for (int q = 0; q < CPI; ++q)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[q][j] = 0.0f;
 
-        for (int k0 = 0; k0 < K; k0 += kGroup) {
+        for (int k0 = 0; k0 < K; k0 += G) {
             int32_t s_l = -1;
             float w_l = 1.0f;
-            if (lane < kGroup && k0 + lane < K) {
+            if (lane < G && k0 + lane < K) {
                 s_l = p.slot[g * K + k0 + lane];
                 if (p.weights != nullptr) w_l = p.weights[g * K + k0 + lane];
             }
-            int32_t s[kGroup];
-            float w[kGroup];
-            uint4 v[kGroup];
+            int32_t s[G];
+            float w[G];
+            uint4 v[G][CPI];
 #pragma unroll
-            for (int j = 0; j < kGroup; ++j) {
+            for (int j = 0; j < G; ++j) {
                 s[j] = __shfl_sync(0xFFFFFFFFu, s_l, j);
                 w[j] = __shfl_sync(0xFFFFFFFFu, w_l, j);
             }
 #pragma unroll
-            for (int j = 0; j < kGroup; ++j) {
-                v[j] = make_uint4(0, 0, 0, 0);
-                if (act && s[j] >= 0) v[j] = ld_nc_na_v4(y + (int64_t)s[j] * H + c);
-            }
+            for (int j = 0; j < G; ++j)
 #pragma unroll
-            for (int j = 0; j < kGroup; ++j) {
+                for (int q = 0; q < CPI; ++q) {
+                    v[j][q] = make_uint4(0, 0, 0, 0);
+                    const int c = c0 + q * kChunk;
+                    if (c < H && s[j] >= 0) v[j][q] = ld_nc_na_v4(y + (int64_t)s[j] * H + c);
+                }
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
                 if (s[j] < 0) continue;
-                const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] = __fmaf_rn(w[j], bf16_lo(u[i]), acc[2 * i]);
-                    acc[2 * i + 1] = __fmaf_rn(w[j], bf16_hi(u[i]), acc[2 * i + 1]);
+                for (int q = 0; q < CPI; ++q) {
+                    const uint32_t u[4] = {v[j][q].x, v[j][q].y, v[j][q].z, v[j][q].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[q][2 * i] = __fmaf_rn(w[j], bf16_lo(u[i]), acc[q][2 * i]);
+                        acc[q][2 * i + 1] = __fmaf_rn(w[j], bf16_hi(u[i]), acc[q][2 * i + 1]);
+                    }
                 }
             }
         }
-        if (act) {
+#pragma unroll
+        for (int q = 0; q < CPI; ++q) {
+            const int c = c0 + q * kChunk;
+            if (c >= H) continue;
             uint32_t o[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+                const __nv_bfloat162 h = __floats2bfloat162_rn(acc[q][2 * i], acc[q][2 * i + 1]);
                 o[i] = *reinterpret_cast<const uint32_t *>(&h);
             }
             *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + g * H + c) =
@@ -90,17 +106,31 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
 
 }  // namespace
 
-int combine_blocks_per_sm() {
+namespace {
+int cpi_for(int K) { return K <= 2 ? 4 : (K <= 4 ? 2 : 1); }
+
+template <int CPI>
+int occupancy() {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, combine_kernel, kThreads, 0) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, combine_kernel<CPI>, kThreads, 0) != cudaSuccess) {
         cudaGetLastError();
         return 1;
     }
     return n > 0 ? n : 1;
 }
+}  // namespace
+
+int combine_blocks_per_sm(int K) {
+    switch (cpi_for(K)) {
+        case 4: return occupancy<4>();
+        case 2: return occupancy<2>();
+        default: return occupancy<1>();
+    }
+}
 
 cudaError_t launch_combine(const CombineParams &p, int max_blocks, bool pdl, cudaStream_t stream) {
-    const int nch = (p.H + kChunk - 1) / kChunk;
+    const int cpi = cpi_for(p.K);
+    const int nch = (p.H + kChunk * cpi - 1) / (kChunk * cpi);
     const int64_t warps = p.N * nch;
     int64_t blocks = (warps + (kThreads / 32) - 1) / (kThreads / 32);
     if (blocks > max_blocks) blocks = max_blocks;
@@ -115,7 +145,11 @@ cudaError_t launch_combine(const CombineParams &p, int max_blocks, bool pdl, cud
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, p);
+    switch (cpi) {
+        case 4: return cudaLaunchKernelEx(&cfg, combine_kernel<4>, p);
+        case 2: return cudaLaunchKernelEx(&cfg, combine_kernel<2>, p);
+        default: return cudaLaunchKernelEx(&cfg, combine_kernel<1>, p);
+    }
 }
 
 }  // namespace ep

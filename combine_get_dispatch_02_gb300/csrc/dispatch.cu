@@ -122,7 +122,11 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const DispatchParams
 // next token overlap the copies of the previous one; the next token's row
 // and slots are loaded while the current one is cast.  Needs H % 512 == 0
 // and H <= 16384.
-constexpr int kRowBlocksPerSM = 2;
+// CTAs per SM: about 1024 threads, at least 2 (measured best at H = 7168)
+int row_blocks_per_sm(int H) {
+    const int b = 16384 / H;
+    return b < 2 ? 2 : (b > 16 ? 16 : b);
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -269,7 +273,7 @@ cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks, b
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     if (row_kernel_fits(p.H) && p.row_sms > 0) {
-        int64_t blocks = (int64_t)p.row_sms * kRowBlocksPerSM;
+        int64_t blocks = (int64_t)p.row_sms * row_blocks_per_sm(p.H);
         if (blocks > p.N) blocks = p.N;
         if (blocks < 1) blocks = 1;
         cudaLaunchConfig_t cfg = {};

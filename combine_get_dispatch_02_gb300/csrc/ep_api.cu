@@ -103,9 +103,10 @@ ep_status enqueue_layout(ep_ctx *ctx, const int64_t *topk_idx, int32_t T, int32_
     p.tokens_per_rank = tokens_per_rank;
     p.is_token_in_rank = is_token_in_rank;
     p.status = ctx->d_status;
-    if (ep::launch_layout(p, ctx->layout_cluster, ctx->layout_threads, stream) != cudaSuccess) {
+    const cudaError_t err = ep::launch_layout(p, ctx->layout_cluster, ctx->layout_threads, stream);
+    if (err != cudaSuccess) {
         cudaGetLastError();
-        return EP_ERR_CUDA;
+        return err == cudaErrorInvalidConfiguration ? EP_ERR_UNSUPPORTED : EP_ERR_CUDA;
     }
     h->tokens_per_rank = T;
     h->has_rank_ranges = want_ranges ? 1 : 0;
@@ -173,7 +174,7 @@ ep_status ep_create(const ep_config *cfg, ep_ctx **out) {
     }
     ctx->dispatch_bps_bf16 = ep::dispatch_blocks_per_sm(false);
     ctx->dispatch_bps_fp8 = ep::dispatch_blocks_per_sm(true);
-    ctx->combine_bps = ep::combine_blocks_per_sm();
+    ctx->combine_bps = ep::combine_blocks_per_sm(cfg->topk);
     ep::dispatch_init();
     if (cudaMalloc(&ctx->d_status, sizeof(uint32_t)) != cudaSuccess) {
         cudaGetLastError();

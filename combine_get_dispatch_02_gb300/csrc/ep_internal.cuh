@@ -31,7 +31,8 @@ struct LayoutParams {
     int32_t *tokens_per_rank;         // [R] or nullptr
     uint8_t *is_token_in_rank;        // [N*R] or nullptr
     uint32_t *status;
-    int32_t staged;            // set by launch_layout: expert ids staged in shared memory
+    int32_t staged;            // set by launch_layout: entries staged in shared memory
+    int32_t er_span;           // set by launch_layout: ranks per CTA for the (e, r) counts
 };
 
 // Launch the single-cluster layout kernel.  cluster_size / threads come from
@@ -77,7 +78,7 @@ struct CombineParams {
 
 cudaError_t launch_combine(const CombineParams &p, int max_blocks, bool pdl,
                            cudaStream_t stream);
-int combine_blocks_per_sm();
+int combine_blocks_per_sm(int K);
 
 // ------------------------------------------------------------------ device helpers
 #ifdef __CUDACC__

@@ -26,9 +26,10 @@
 //     (entries of the expert in lower CTAs) + (in lower warps) + (its
 //     position in the warp).  Without the copy pass 2 re-derives the
 //     positions from topk_idx.
-//   * Per-(expert, source rank) ranges (cnt_er / off_er) are optional: pass 2
-//     adds the per-round counts to the zeroed global cnt_er, and after a
-//     second cluster barrier the owner CTAs turn them into offsets.
+//   * Per-(expert, source rank) ranges (cnt_er / off_er) are optional: pass 1
+//     also counts per (expert, source rank) in shared memory, each CTA adds
+//     its counts to the zeroed global cnt_er after the cluster barrier, and
+//     after a second barrier the owner CTAs turn them into offsets.
 #include <cooperative_groups.h>
 
 #include "ep_internal.cuh"
@@ -130,7 +131,9 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     int32_t *epre = recv_tok + CL * R;      // [E]     entries of e in lower CTAs
     int32_t *ebase = epre + E;              // [E]     first row of e
     int32_t *scan = ebase + E;              // [NW+1]
-    int32_t *stage = scan + NW + 1;         // [NW][tpw*K] (position in warp << 11) | (expert + 1)
+    const int span = p.er_span;             // source ranks one CTA's tokens can cover (0: no ranges)
+    int32_t *hist_er = scan + NW + 1;       // [E][span] entries per (expert, rank - first rank)
+    int32_t *stage = hist_er + E * span;    // [NW][tpw*K] (position in warp << 11) | (expert + 1)
 
     // contiguous token range per warp, warps of a CTA adjacent
     const int nwarps = CL * NW;
@@ -140,7 +143,12 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     const int t0 = min(cta_t1, cta_t0 + w * tpw);
     const int t1 = min(cta_t1, t0 + tpw);
     const int i0 = t0 * K, i1 = t1 * K;
-    int32_t *my_stage = p.staged ? stage + (size_t)w * tpw * K : nullptr;
+    // (position, expert) of each entry between the passes: in shared memory
+    // when it fits, else in the entry's own slot cell (the same thread writes
+    // and later overwrites it)
+    int32_t *my_stage = p.staged ? stage + (size_t)w * tpw * K : p.slot + i0;
+    const bool want_er = p.cnt_er != nullptr;
+    const int r0 = T > 0 ? cta_t0 / T : 0;  // first source rank of this CTA
 
     // first batch of entries in flight while shared memory is cleared
     int64_t raw[kU];
@@ -148,6 +156,7 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     for (int u = 0; u < kU; ++u) raw[u] = load_raw(p.topk_idx, i0 + u * 32 + lane, i1);
 
     for (int i = tid; i < NW * E + R; i += NT) sm[i] = 0;
+    for (int i = tid; i < E * span; i += NT) hist_er[i] = 0;
     if (p.is_token_in_rank) {
         for (int b = cta_t0 * R + tid; b < cta_t1 * R; b += NT) p.is_token_in_rank[b] = 0;
     }
@@ -159,6 +168,7 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     __syncthreads();
 
     // ---------------- pass 1: per-warp counts per expert
+    const int erbits = bits_for(E * span + 1);
     for (int ib = i0; ib < i1; ib += 32 * kU) {
         if (ib != i0) {
 #pragma unroll
@@ -176,7 +186,12 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
             __syncwarp();
             if (e >= 0 && lane == __ffs(peers) - 1) hist_w[w * E + e] += __popc(peers);
             __syncwarp();
-            if (i < i1 && my_stage) my_stage[i - i0] = (local << 11) | (e + 1);
+            if (i < i1) my_stage[i - i0] = (local << 11) | (e + 1);
+            if (want_er) {  // entries per (expert, source rank), one atomic per key per round
+                const int key = e >= 0 ? e * span + (i / K) / T - r0 : E * span;
+                const uint32_t pk = warp_match(key, erbits);
+                if (e >= 0 && lane == __ffs(pk) - 1) atomicAdd(&hist_er[key], __popc(pk));
+            }
         }
     }
     if (p.tokens_per_rank || p.is_token_in_rank) {
@@ -235,6 +250,12 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
             p.tokens_per_rank[d] = v;
         }
     }
+    if (want_er) {  // the owners cleared cnt_er before the cluster barrier
+        for (int j = tid; j < E * span; j += NT) {
+            const int v = hist_er[j];
+            if (v != 0) atomicAdd(&p.cnt_er[(j / span) * R + r0 + j % span], v);
+        }
+    }
     __syncthreads();
 
     // first row of each expert: e * cap (padded) or the exclusive prefix of
@@ -262,72 +283,22 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
     __syncthreads();
 
     // ---------------- pass 2: rows, in (g, k) order
-    const uint32_t lt = lanemask_lt();
+    // every entry's position inside its warp is known: rows follow directly
     const int cap = (int)min(p.cap, (int64_t)0x7FFFFFFF);
-    const bool want_er = p.cnt_er != nullptr;
-    const int erbits = bits_for(E * R + 1);
-    if (my_stage && !want_er) {
-        // every entry's position inside its warp is known: rows follow directly
-        for (int i = i0 + lane; i < i1; i += 32) {
-            const int v = my_stage[i - i0];
-            const int e = (v & 2047) - 1;
-            int32_t s = -1;
-            if (e >= 0) {
-                const int pos = epre[e] + hist_w[w * E + e] + (v >> 11);
-                if (pos < cap) {
-                    s = ebase[e] + pos;
-                    p.src_info[s] = i;
-                } else {
-                    atomicOr(p.status, kStatusCapacity);
-                }
-            }
-            p.slot[i] = s;
-        }
-    }
-    for (int ib = (my_stage && !want_er) ? i1 : i0; ib < i1; ib += 32 * kU) {
-        int ev[kU];
-        if (my_stage) {
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int i = ib + u * 32 + lane;
-                ev[u] = i < i1 ? (my_stage[i - i0] & 2047) - 1 : -1;
-            }
-        } else {
-#pragma unroll
-            for (int u = 0; u < kU; ++u) raw[u] = load_raw(p.topk_idx, ib + u * 32 + lane, i1);
-#pragma unroll
-            for (int u = 0; u < kU; ++u) ev[u] = to_expert(raw[u], E, p.status);
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            if (ib + u * 32 >= i1) break;  // warp-uniform
-            const int i = ib + u * 32 + lane;
-            const int e = ev[u];
-            const bool valid = e >= 0;
-            const uint32_t peers = warp_match(valid ? e : E, ebits);
-            int pos = 0;
-            if (valid) pos = epre[e] + hist_w[w * E + e] + __popc(peers & lt);
-            __syncwarp();
-            if (valid && lane == __ffs(peers) - 1) hist_w[w * E + e] += __popc(peers);
-            __syncwarp();
-            if (i < i1) {
-                int32_t s = -1;
-                if (valid) {
-                    if (pos < cap) {
-                        s = ebase[e] + pos;
-                        p.src_info[s] = i;
-                    } else {
-                        atomicOr(p.status, kStatusCapacity);
-                    }
-                }
-                p.slot[i] = s;
-            }
-            if (want_er) {  // entries per (expert, source rank), one atomic per key per round
-                const int key = valid ? e * R + (i / K) / T : E * R;
-                const uint32_t pk = warp_match(key, erbits);
-                if (valid && lane == __ffs(pk) - 1) atomicAdd(&p.cnt_er[key], __popc(pk));
+    for (int i = i0 + lane; i < i1; i += 32) {
+        const int v = my_stage[i - i0];
+        const int e = (v & 2047) - 1;
+        int32_t s = -1;
+        if (e >= 0) {
+            const int pos = epre[e] + hist_w[w * E + e] + (v >> 11);
+            if (pos < cap) {
+                s = ebase[e] + pos;
+                p.src_info[s] = i;
+            } else {
+                atomicOr(p.status, kStatusCapacity);
             }
         }
+        p.slot[i] = s;
     }
 
     if (want_er) {
@@ -358,6 +329,17 @@ size_t smem_words(int E, int R, int NT, int CL) {
     return NW * E + R + (size_t)CL * E + (size_t)CL * R + 2 * (size_t)E + NW + 1;
 }
 
+// Source ranks the token range of one CTA can touch (0 when no per-rank
+// ranges are wanted).
+int er_span_of(const LayoutParams &p, int NT, int CL) {
+    if (p.cnt_er == nullptr) return 0;
+    if (p.T <= 0) return 1;
+    const int64_t nwarps = (int64_t)CL * (NT / 32);
+    const int64_t tpw = (p.N + nwarps - 1) / nwarps;
+    const int64_t span = (tpw * (NT / 32) + p.T - 1) / p.T + 1;
+    return (int)(span < p.R ? span : p.R);
+}
+
 // stage bytes for the per-warp copies of the entries' expert ids
 size_t stage_bytes(int64_t N, int K, int NT, int CL) {
     const int64_t nwarps = (int64_t)CL * (NT / 32);
@@ -367,7 +349,13 @@ size_t stage_bytes(int64_t N, int K, int NT, int CL) {
 
 template <int NT>
 cudaError_t launch_nt(LayoutParams p, int cl, cudaStream_t stream) {
-    size_t smem = smem_words(p.E, p.R, NT, cl) * sizeof(int32_t);
+    {   // an entry's position in its warp is packed into 20 bits between the passes
+        const int64_t nwarps = (int64_t)cl * (NT / 32);
+        if ((p.N + nwarps - 1) / nwarps * p.K >= (int64_t(1) << 20)) return cudaErrorInvalidConfiguration;
+    }
+    p.er_span = er_span_of(p, NT, cl);
+    size_t smem = (smem_words(p.E, p.R, NT, cl) + (size_t)p.E * p.er_span) * sizeof(int32_t);
+    if (smem > kMaxSmem) return cudaErrorInvalidConfiguration;
     const size_t stage = stage_bytes(p.N, p.K, NT, cl);
     p.staged = (smem + stage <= kMaxSmem) ? 1 : 0;
     if (p.staged) smem += (stage + 15) / 16 * 16;

@@ -91,7 +91,9 @@ typedef enum ep_layout {
  *   num_experts % num_ranks == 0, 1 <= num_experts <= 1024,
  *   num_experts * num_ranks <= 16384,
  *   8 <= hidden <= 65536, hidden % 8 == 0 (FP8 dispatch: hidden % 128 == 0),
- *   receive rows and R*Tmax*K below 2^31.
+ *   receive rows and R*Tmax*K below 2^31, and fewer than 2^20 entries per
+ *   warp of the layout kernel (R*T*K < 2^28 when the device runs 16-CTA
+ *   clusters of 512 threads; larger calls return EP_ERR_UNSUPPORTED).
  * max_sms caps the SMs the dispatch and combine kernels spread over (0 = all),
  * the SM-count control of the normal kernels. */
 typedef struct ep_config {
