@@ -72,6 +72,8 @@ def use_library(path: str | None):
     lib.orc_layout.restype = None
     lib.orc_layout.argtypes = [I32, I32, I32, I32, I32, I32, P,
                                P, P, P, P, P, P, P, P, I64, P]
+    lib.orc_rank_layout.restype = None
+    lib.orc_rank_layout.argtypes = [I32, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, I64]
     lib.orc_quant_block.argtypes = [P, P, P]
     lib.orc_quant_token.argtypes = [P, I32, P, P]
     lib.orc_dispatch.argtypes = [I64, I32, I32, I32, P, P, P, P]
@@ -157,6 +159,36 @@ def layout(topk_idx: np.ndarray, num_experts: int, max_tokens_per_rank: int,
         _p(out["slot"]), _p(out["src_info"]), rows, _p(errors))
     out["n_bad"] = int(errors[0])
     out["n_overflow"] = int(errors[1])
+    out["rows"] = rows
+    return out
+
+
+def rank_recv_rows(R: int, Tmax: int, K: int, layout: int) -> int:
+    """Rows of a rank-deduplicated receive buffer: R buffers of R*Tmax rows
+    (padded) or the worst case R*Tmax*min(K, R) rows (packed)."""
+    return R * R * Tmax if layout == LAYOUT_PADDED else R * Tmax * min(K, R)
+
+
+def rank_layout(topk_idx: np.ndarray, topk_weights: np.ndarray | None, num_experts: int,
+                max_tokens_per_rank: int, layout: int = LAYOUT_PACKED) -> dict:
+    """Rank-deduplicated layout of topk_idx [R, T, K]: rank_slot [N, K] (row of
+    the entry that carries the token to its rank, else -1), tokens_per_rank
+    [R], rbase [R], src_info [rows] (-1 where nothing lands), recv_topk_idx
+    [rows, K] (local expert ids or -1), recv_topk_weights [rows, K], rows."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    R, T, K = idx.shape
+    E = int(num_experts)
+    N = R * T
+    rows = rank_recv_rows(R, max_tokens_per_rank, K, layout)
+    w = None if topk_weights is None else np.ascontiguousarray(topk_weights, dtype=np.float32).reshape(N, K)
+    out = dict(rank_slot=np.zeros((N, K), np.int32), tokens_per_rank=np.zeros(R, np.int32),
+               rbase=np.zeros(R, np.int64), src_info=np.full(rows, -1, np.int32),
+               recv_topk_idx=np.full((rows, K), -1, np.int32),
+               recv_topk_weights=np.zeros((rows, K), np.float32))
+    _load().orc_rank_layout(R, T, max_tokens_per_rank, K, E, layout, _p(idx),
+                            None if w is None else _p(w), _p(out["rank_slot"]),
+                            _p(out["tokens_per_rank"]), _p(out["rbase"]), _p(out["src_info"]),
+                            _p(out["recv_topk_idx"]), _p(out["recv_topk_weights"]), rows)
     out["rows"] = rows
     return out
 

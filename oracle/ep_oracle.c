@@ -275,6 +275,83 @@ void orc_layout(int R, int T, int Tmax, int K, int E, int layout,
 }
 
 /* ------------------------------------------------------------------ */
+/* Rank-deduplicated layout  [ANN] normal kernels: tokens forwarded per   */
+/* destination rank rather than per expert                               */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Each token is sent once to every rank that owns at least one of its
+ * experts.  The entry (g, k) that carries token g to rank d is the first k of
+ * the token whose expert lives on d; every other entry gets rank_slot -1.
+ * Rows of rank d start at rbase[d] (d * R * Tmax padded, i.e. room for every
+ * token; exclusive prefix of tokens_per_rank packed) and hold its tokens in
+ * ascending g.  For each written row: src_info = g * K + k of the carrying
+ * entry; recv_topk_idx[row * K + k'] = local expert id (e - d * L) of the
+ * token's k'-th expert if it lives on d, else -1; recv_topk_w the matching
+ * weight (w == NULL: 1), else 0.  Ids outside [0, E) are ignored.
+ */
+void orc_rank_layout(int R, int T, int Tmax, int K, int E, int layout,
+                     const int64_t *topk_idx, const float *w,
+                     int32_t *rank_slot, int32_t *tokens_per_rank, int64_t *rbase,
+                     int32_t *src_info, int32_t *recv_topk_idx, float *recv_topk_w,
+                     int64_t rows)
+{
+    int64_t N = (int64_t)R * T;
+    int L = E / R;
+    for (int d = 0; d < R; d++)
+        tokens_per_rank[d] = 0;
+    for (int64_t g = 0; g < N; g++)
+        for (int k = 0; k < K; k++) {
+            int64_t e = topk_idx[g * K + k];
+            if (e < 0 || e >= E)
+                continue;
+            int first = 1;
+            for (int k2 = 0; k2 < k; k2++) {
+                int64_t e2 = topk_idx[g * K + k2];
+                if (e2 >= 0 && e2 < E && e2 / L == e / L)
+                    first = 0;
+            }
+            if (first)
+                tokens_per_rank[e / L]++;
+        }
+    int64_t acc = 0;
+    for (int d = 0; d < R; d++) {
+        rbase[d] = layout == ORC_LAYOUT_PADDED ? (int64_t)d * R * Tmax : acc;
+        acc += tokens_per_rank[d];
+    }
+    int32_t *fill = (int32_t *)calloc(R > 0 ? (size_t)R : 1u, sizeof(int32_t));
+    for (int64_t g = 0; g < N; g++) {
+        for (int k = 0; k < K; k++) {
+            int64_t e = topk_idx[g * K + k];
+            rank_slot[g * K + k] = -1;
+            if (e < 0 || e >= E)
+                continue;
+            int d = (int)(e / L), first = 1;
+            for (int k2 = 0; k2 < k; k2++) {
+                int64_t e2 = topk_idx[g * K + k2];
+                if (e2 >= 0 && e2 < E && e2 / L == d)
+                    first = 0;
+            }
+            if (!first)
+                continue;
+            int64_t row = rbase[d] + fill[d];
+            fill[d]++;
+            rank_slot[g * K + k] = (int32_t)row;
+            if (row >= rows)
+                continue;
+            src_info[row] = (int32_t)(g * K + k);
+            for (int k2 = 0; k2 < K; k2++) {
+                int64_t e2 = topk_idx[g * K + k2];
+                int on_d = e2 >= 0 && e2 < E && e2 / L == d;
+                recv_topk_idx[row * K + k2] = on_d ? (int32_t)(e2 - (int64_t)d * L) : -1;
+                recv_topk_w[row * K + k2] = on_d ? (w ? w[g * K + k2] : 1.0f) : 0.0f;
+            }
+        }
+    }
+    free(fill);
+}
+
+/* ------------------------------------------------------------------ */
 /* FP8 cast  [ANN] native FP8 dispatch; [LL] FP8 dispatch               */
 /* ------------------------------------------------------------------ */
 

@@ -64,6 +64,15 @@ MUTANTS = {
     "layout: invalid ids not reported": (
         "                bad++;\n",
         ""),
+    "rank layout: every entry carries its token": (
+        "            if (!first)\n                continue;\n            int64_t row = rbase[d] + fill[d];",
+        "            int64_t row = rbase[d] + fill[d];"),
+    "rank layout: weights of other ranks' experts kept": (
+        "recv_topk_w[row * K + k2] = on_d ? (w ? w[g * K + k2] : 1.0f) : 0.0f;",
+        "recv_topk_w[row * K + k2] = w ? w[g * K + k2] : 1.0f;"),
+    "rank layout: rank buffers sized by T instead of Tmax": (
+        "rbase[d] = layout == ORC_LAYOUT_PADDED ? (int64_t)d * R * Tmax : acc;",
+        "rbase[d] = layout == ORC_LAYOUT_PADDED ? (int64_t)d * R * T : acc;"),
     "layout: padded overflow not dropped": (
         "            if (layout == ORC_LAYOUT_PADDED && pos >= cap) {",
         "            if (0) {"),
@@ -77,8 +86,11 @@ def _pins():
              pins.test_e4m3_decode_matches_torch, pins.test_combine_special_cases]
     for f in cheap:
         yield f.__name__, (lambda f=f: f(oracle))
+    yield "rank_golden", lambda: pins.test_rank_layout_golden(oracle)
     for seed in range(30):
         yield f"brute_force[{seed}]", (lambda seed=seed: pins.test_layout_brute_force(oracle, seed))
+    for seed in range(20):
+        yield f"rank_brute_force[{seed}]", (lambda seed=seed: pins.test_rank_layout_brute_force(oracle, seed))
     for name in ("tiny", "skew"):
         yield f"invariants[{name}]", (lambda name=name: pins.test_layout_invariants(oracle, name))
     yield "bf16_torch", lambda: pins.test_bf16_matches_torch(oracle)

@@ -207,6 +207,86 @@ def test_layout_brute_force(orc, seed):
         assert np.array_equal(o["src_info"][b["slot"][v]], b["src"][v])
 
 
+def test_rank_layout_golden(orc):
+    g, _ = _read_golden("layout_small.txt")
+    iv = lambda k: np.array([int(v) for v in g[k][0]])
+    R, T, Tmax, K, E = (int(g[k][0][0]) for k in ("R", "T", "Tmax", "K", "E"))
+    idx = iv("topk_idx").reshape(R, T, K)
+    for lay, pfx in ((orc.LAYOUT_PACKED, "rank_packed"), (orc.LAYOUT_PADDED, "rank_padded")):
+        o = orc.rank_layout(idx, None, E, Tmax, lay)
+        assert np.array_equal(o["tokens_per_rank"], iv("rank_tokens_per_rank"))
+        assert np.array_equal(o["rbase"], iv(pfx + "_rbase"))
+        assert np.array_equal(o["rank_slot"].ravel(), iv(pfx + "_slot"))
+    o = orc.rank_layout(idx, None, E, Tmax, orc.LAYOUT_PACKED)
+    assert np.array_equal(o["recv_topk_idx"][:5].ravel(), iv("rank_packed_recv_topk_idx"))
+    assert np.array_equal(o["src_info"][:5], iv("rank_packed_src_info"))
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_rank_layout_brute_force(orc, seed):
+    rng = np.random.default_rng(700 + seed)
+    R = int(rng.integers(1, 4))
+    L = int(rng.integers(1, 4))
+    E = R * L
+    Tmax = int(rng.integers(1, 5))
+    T = int(rng.integers(1, Tmax + 1))
+    K = int(rng.integers(1, 5))
+    idx = rng.integers(-1, E, size=(R, T, K))
+    w = rng.random((R, T, K)).astype(np.float32)
+    N = R * T
+    flat = idx.reshape(N, K)
+    for packed in (False, True):
+        lay = orc.LAYOUT_PACKED if packed else orc.LAYOUT_PADDED
+        o = orc.rank_layout(idx, w, E, Tmax, lay)
+        # enumerate (token, rank) pairs: the carrying k is the first on that rank
+        carry = {}
+        for gg in range(N):
+            for k in range(K):
+                e = flat[gg, k]
+                if 0 <= e < E and (gg, e // L) not in carry:
+                    carry[(gg, e // L)] = k
+        counts = np.bincount([d for (_, d) in carry], minlength=R)
+        rbase = np.concatenate([[0], np.cumsum(counts)[:-1]]) if packed else np.arange(R) * R * Tmax
+        assert np.array_equal(o["tokens_per_rank"], counts)
+        assert np.array_equal(o["rbase"], rbase)
+        slot = np.full((N, K), -1)
+        for d in range(R):
+            toks = sorted(gg for (gg, dd) in carry if dd == d)
+            for j, gg in enumerate(toks):
+                row = rbase[d] + j
+                slot[gg, carry[(gg, d)]] = row
+                assert o["src_info"][row] == gg * K + carry[(gg, d)]
+                for k in range(K):
+                    e = flat[gg, k]
+                    on_d = 0 <= e < E and e // L == d
+                    assert o["recv_topk_idx"][row, k] == (e - d * L if on_d else -1)
+                    assert o["recv_topk_weights"][row, k] == (w.reshape(N, K)[gg, k] if on_d else 0.0)
+        assert np.array_equal(o["rank_slot"], slot)
+        # the same tokens per rank as the expert layout's membership
+        assert np.array_equal(o["tokens_per_rank"], orc.layout(idx, E, Tmax, lay)["tokens_per_rank"])
+
+
+def test_rank_round_trip_bf16(orc):
+    """Rank dispatch, an identity expert per rank that returns the token times
+    the sum of its local weights, rank combine: weights summing to one give x
+    back within two bf16 roundings."""
+    w = wl.NORMAL.with_(tokens_per_rank=64, max_tokens_per_rank=64, hidden=256)
+    d = wl.generate(w)
+    N, K, H = w.num_tokens, w.topk, w.hidden
+    o = orc.rank_layout(d["topk_idx"], d["topk_weights"], w.num_experts, w.max_tokens_per_rank)
+    x = d["x_bits"].reshape(N, H)
+    recv = orc.dispatch(x, o["rank_slot"], o["rows"], use_fp8=False)
+    used = o["rank_slot"][o["rank_slot"] >= 0]
+    scale = o["recv_topk_weights"][used].sum(axis=1, dtype=np.float64)
+    y = np.zeros((o["rows"], H), np.uint16)
+    y[used] = _torch_bf16_bits((orc.bf16_to_f32(recv[used]) * scale[:, None]).astype(np.float32))
+    out = orc.combine(y, o["rank_slot"], None)
+    xf = _bits_to_bf16_float(x).astype(np.float64)
+    of = _bits_to_bf16_float(out).astype(np.float64)
+    nr = (o["rank_slot"] >= 0).sum(axis=1)[:, None]
+    assert np.all(np.abs(of - xf) <= (nr + 2) * _ulp_bf16(xf))
+
+
 def test_layout_identity_case(orc):
     idx = np.zeros((1, 9, 1), np.int64)  # R = 1, E = 1, K = 1
     for lay in (orc.LAYOUT_PADDED, orc.LAYOUT_PACKED):
