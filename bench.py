@@ -50,6 +50,8 @@ def _args():
     ap.add_argument("--breakdown-reps", type=int, default=200)
     ap.add_argument("--layout", choices=["padded", "packed"], default=None,
                     help="override the workload's receive layout (packed keeps a profiled run small)")
+    ap.add_argument("--rank", action="store_true",
+                    help="rank-deduplicated transport (each token sent once per destination rank)")
     ap.add_argument("--sweep", action="store_true",
                     help="time the sweep grid (one JSON line per point) instead of the bench step")
     ap.add_argument("--sweep-filter", default="", help="only sweep points whose name contains this")
@@ -282,19 +284,34 @@ def run_ours(args):
     x = to_dev(np.ascontiguousarray(d["x_bits"]).view(np.int16)).view(torch.bfloat16)
     idx = to_dev(d["topk_idx"])
     wts = to_dev(d["topk_weights"].reshape(N, K))
-    recv, scales = buf.alloc_recv(w.use_fp8)
+    recv, scales = buf.alloc_rank_recv(w.use_fp8) if args.rank else buf.alloc_recv(w.use_fp8)
     cnt = torch.empty(w.num_experts, dtype=torch.int32, device="cuda")
     out = torch.empty(N, H, dtype=torch.bfloat16, device="cuda")
     h = buf.new_handle()
     ctx = buf.ctx
     stream = torch.cuda.current_stream()
 
+    def enqueue(xb, idxb, wb, outb, s):
+        """One step: layout + dispatch, then combine (on stream s)."""
+        if args.rank:
+            ep.ep_get_rank_layout(ctx, idxb, wb, w.tokens_per_rank, None, None, None, h.raw, s)
+            ep.ep_dispatch(ctx, xb, None, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales, cnt, s)
+        else:
+            ep.ep_dispatch(ctx, xb, idxb, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales, cnt, s)
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(s)
+        ep.ep_combine(ctx, y, None if args.rank else wb, h.raw, outb, s)
+        return ev
+
     # expert outputs (combine input) at the rows the layout assigns
-    ep.ep_get_dispatch_layout(ctx, idx, w.tokens_per_rank, None, None, None, h.raw)
+    if args.rank:
+        ep.ep_get_rank_layout(ctx, idx, wts, w.tokens_per_rank, None, None, None, h.raw)
+    else:
+        ep.ep_get_dispatch_layout(ctx, idx, w.tokens_per_rank, None, None, None, h.raw)
     slot = h.tensors()["slot"].view(-1).long()
     valid = slot >= 0
     M = int(valid.sum().item())
-    y = torch.zeros(buf.rows, H, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(buf.rank_rows if args.rank else buf.rows, H, dtype=torch.bfloat16, device="cuda")
     ye = wl.expert_outputs(w)
     y[slot[valid]] = to_dev(ye.reshape(-1, H).view(np.int16)).view(torch.bfloat16)[valid]
     del ye
@@ -312,11 +329,7 @@ def run_ours(args):
         torch.sum(flush_r, dim=0, keepdim=True, out=flush_sink)
 
     def step():
-        ep.ep_dispatch(ctx, x, idx, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales, cnt, stream)
-        ev_mid = torch.cuda.Event(enable_timing=True)
-        ev_mid.record(stream)
-        ep.ep_combine(ctx, y, wts, h.raw, out, stream)
-        return ev_mid
+        return enqueue(x, idx, wts, out, stream)
 
     for _ in range(args.warmup):
         flush_l2()
@@ -368,10 +381,12 @@ def run_ours(args):
         v = [a.elapsed_time(b) * 1e3 for a, b in ts]
         return statistics.median(v), statistics.mean(v)
 
-    lay_us = timed(lambda: ep.ep_get_dispatch_layout(ctx, idx, w.tokens_per_rank, None, None, None, h.raw, stream))
+    lay_us = timed(lambda: ep.ep_get_rank_layout(ctx, idx, wts, w.tokens_per_rank, None, None, None, h.raw, stream)
+                   if args.rank else
+                   ep.ep_get_dispatch_layout(ctx, idx, w.tokens_per_rank, None, None, None, h.raw, stream))
     disp_us = timed(lambda: ep.ep_dispatch(ctx, x, None, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales,
                                            None, stream))
-    comb_us = timed(lambda: ep.ep_combine(ctx, y, wts, h.raw, out, stream))
+    comb_us = timed(lambda: ep.ep_combine(ctx, y, None if args.rank else wts, h.raw, out, stream))
 
     # the same step captured once in a CUDA graph and replayed (no host
     # launch overhead; programmatic dependent launch becomes a graph edge)
@@ -381,13 +396,11 @@ def run_ours(args):
         s_cap.wait_stream(stream)
         with torch.cuda.stream(s_cap):
             for _ in range(2):
-                ep.ep_dispatch(ctx, x, idx, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales, cnt, s_cap)
-                ep.ep_combine(ctx, y, wts, h.raw, out, s_cap)
+                enqueue(x, idx, wts, out, s_cap)
         stream.wait_stream(s_cap)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=s_cap):
-            ep.ep_dispatch(ctx, x, idx, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales, cnt, s_cap)
-            ep.ep_combine(ctx, y, wts, h.raw, out, s_cap)
+            enqueue(x, idx, wts, out, s_cap)
         graph_us = timed(graph.replay)
     except Exception as exc:  # report, do not hide, a capture failure
         graph_us = (f"capture failed: {exc}", None)
@@ -399,7 +412,7 @@ def run_ours(args):
     del cbuf, cdst
 
     # end to end through the public API with host buffers
-    e2e = None if args.no_e2e else _e2e(args, w, d, x, idx, wts, out, ctx, h, recv, scales, cnt, y, stream)
+    e2e = None if args.no_e2e else _e2e(args, w, d, x, idx, wts, out, enqueue, stream)
     if buf.device_status() != ep.EP_OK:
         raise RuntimeError("device status error")
 
@@ -413,7 +426,7 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def _e2e(args, w, d, x, idx, wts, out, ctx, h, recv, scales, cnt, y, stream):
+def _e2e(args, w, d, x, idx, wts, out, enqueue, stream):
     """End to end through the public calls with host buffers: every step
     copies its inputs (x, topk_idx, topk_weights) from pinned host memory,
     runs ep_dispatch + ep_combine and copies the combined tokens back.
@@ -423,7 +436,6 @@ def _e2e(args, w, d, x, idx, wts, out, ctx, h, recv, scales, cnt, y, stream):
     synchronised on both sides) still contains every step's copies.  The
     same loop run serially on one stream is reported beside it."""
     import torch
-    from combine_get_dispatch_02_gb300 import ep
     N, K, H = w.num_tokens, w.topk, w.hidden
     ws = _dist()[0]
     xh = torch.from_numpy(np.ascontiguousarray(d["x_bits"]).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -454,8 +466,7 @@ def _e2e(args, w, d, x, idx, wts, out, ctx, h, recv, scales, cnt, y, stream):
             ev_in[b].record(cin)
             stream.wait_event(ev_in[b])
             stream.wait_event(ev_out[b])
-            ep.ep_dispatch(ctx, xs[b], idxs[b], w.tokens_per_rank, w.use_fp8, h.raw, recv, scales, cnt, stream)
-            ep.ep_combine(ctx, y, wss[b], h.raw, outs[b], stream)
+            enqueue(xs[b], idxs[b], wss[b], outs[b], stream)
             ev_comp[b].record(stream)
             cout.wait_event(ev_comp[b])
             with torch.cuda.stream(cout):
@@ -494,7 +505,8 @@ def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, la
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "payload": {"dispatch": "e4m3 + f32 scales" if w.use_fp8 else "bf16", "combine": "bf16"},
         "data": "synthetic",
-        "config": {"workload": _workload_desc(w), "tokens_per_step": N, "rows_received": M,
+        "config": {"workload": _workload_desc(w) + ("; rank-deduplicated transport" if args.rank else ""),
+                   "tokens_per_step": N, "rows_received": M,
                    "l2": "flushed between steps (write of 2x L2, then read of 2x L2; outside the timed events)",
                    "parallelism": f"{ws} replica(s), one per GPU" if ws > 1 else "1 GPU, 32 virtual EP ranks"},
         "us_per_call": {

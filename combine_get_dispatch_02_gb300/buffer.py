@@ -127,6 +127,38 @@ class Buffer:
     def new_handle(self) -> Handle:
         return Handle(self)
 
+    @property
+    def rank_rows(self) -> int:
+        """Rows of a rank-deduplicated receive buffer (ep_rank_recv_rows)."""
+        return ep.ep_rank_recv_rows(self.cfg)
+
+    def alloc_rank_recv(self, use_fp8: bool):
+        """Receive buffers for the rank-deduplicated layout: (recv_x, recv_scales or None)."""
+        dev = torch.device("cuda", torch.cuda.current_device())
+        rows = self.rank_rows
+        if use_fp8:
+            return (torch.empty(rows, self.hidden, dtype=torch.float8_e4m3fn, device=dev),
+                    torch.empty(rows, self.hidden // 128, dtype=torch.float32, device=dev))
+        return torch.empty(rows, self.hidden, dtype=torch.bfloat16, device=dev), None
+
+    def get_rank_layout(self, topk_idx: torch.Tensor, topk_weights: torch.Tensor | None = None,
+                        handle: Handle | None = None):
+        """Rank-deduplicated (normal-mode) layout: (num_tokens_per_rank [R],
+        recv_topk_idx [rows, K] local expert ids or -1, recv_topk_weights
+        [rows, K], handle).  The handle then serves low_latency_dispatch
+        (topk_idx=None, buffers from alloc_rank_recv) and low_latency_combine
+        (topk_weights=None: the expert side applies the weights)."""
+        T = self._tokens_per_rank(topk_idx)
+        dev = topk_idx.device
+        ntr = torch.empty(self.num_ranks, dtype=torch.int32, device=dev)
+        rows = self.rank_rows
+        ridx = torch.empty(rows, self.topk, dtype=torch.int32, device=dev)
+        rw = torch.empty(rows, self.topk, dtype=torch.float32, device=dev)
+        handle = handle or Handle(self)
+        w = None if topk_weights is None else topk_weights.reshape(-1, self.topk)
+        ep.ep_get_rank_layout(self._ctx, topk_idx, w, T, ntr, ridx, rw, handle.raw)
+        return ntr, ridx, rw, handle
+
     # -------------------------------------------------------- operations
     def _tokens_per_rank(self, topk_idx: torch.Tensor) -> int:
         if topk_idx.dim() != 3 or topk_idx.shape[0] != self.num_ranks or topk_idx.shape[2] != self.topk:

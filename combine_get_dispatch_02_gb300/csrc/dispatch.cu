@@ -258,12 +258,36 @@ int blocks_per_sm() {
 
 int dispatch_blocks_per_sm(bool fp8) { return fp8 ? blocks_per_sm<true>() : blocks_per_sm<false>(); }
 
+namespace {
+int g_smem_per_sm = 0;        // shared memory per SM
+int g_smem_reserved = 0;      // shared memory the system reserves per CTA
+int g_smem_per_block = 0;     // largest dynamic shared memory of one CTA
+
+// Dynamic shared memory that lets at most `blocks` CTAs of the row kernel
+// share an SM.  The grid is persistent with a fixed share of tokens per CTA,
+// so the CTAs must spread evenly: when the kernel starts early behind the
+// layout kernel (programmatic dependent launch) the scheduler would
+// otherwise pack extra CTAs onto the free SMs and those SMs would finish
+// last.
+size_t row_smem_for_occupancy(bool fp8, int H, int blocks) {
+    const size_t need = row_smem_bytes(fp8, H);
+    if (g_smem_per_sm <= 0) return need;
+    const int64_t cap = (int64_t)g_smem_per_sm / (blocks + 1) - g_smem_reserved + 16;
+    size_t s = cap > (int64_t)need ? (size_t)cap : need;
+    s = (s + 15) / 16 * 16;
+    return s > (size_t)g_smem_per_block ? need : s;
+}
+}  // namespace
+
 void dispatch_init() {
-    // the row kernel's shared memory can exceed the 48 KB default (BF16, H > 6144)
-    cudaFuncSetAttribute(dispatch_row_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)row_smem_bytes(false, 16384));
-    cudaFuncSetAttribute(dispatch_row_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)row_smem_bytes(true, 16384));
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&g_smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    cudaDeviceGetAttribute(&g_smem_per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    // the row kernel asks for more than the 48 KB default (see above)
+    cudaFuncSetAttribute(dispatch_row_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
+    cudaFuncSetAttribute(dispatch_row_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
     cudaGetLastError();
 }
 
@@ -273,13 +297,14 @@ cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks, b
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     if (row_kernel_fits(p.H) && p.row_sms > 0) {
-        int64_t blocks = (int64_t)p.row_sms * row_blocks_per_sm(p.H);
+        const int bps = row_blocks_per_sm(p.H);
+        int64_t blocks = (int64_t)p.row_sms * bps;
         if (blocks > p.N) blocks = p.N;
         if (blocks < 1) blocks = 1;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)blocks, 1, 1);
         cfg.blockDim = dim3(p.H / 16, 1, 1);
-        cfg.dynamicSmemBytes = row_smem_bytes(fp8, p.H);
+        cfg.dynamicSmemBytes = row_smem_for_occupancy(fp8, p.H, bps);
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = pdl ? 1 : 0;

@@ -34,6 +34,8 @@ struct ep_handle {
     int32_t *tokens_per_expert;
     int32_t tokens_per_rank;  // -1: no layout yet
     int32_t has_rank_ranges;  // cnt_er / off_er hold the current layout's ranges
+    int32_t rank_mode;        // the layout is rank-deduplicated (keys are ranks)
+    int32_t num_keys;         // experts, or ranks in rank mode
 };
 
 namespace {
@@ -89,6 +91,11 @@ ep_status enqueue_layout(ep_ctx *ctx, const int64_t *topk_idx, int32_t T, int32_
     p.K = c.topk;
     p.E = c.num_experts;
     p.L = c.num_experts / c.num_ranks;
+    p.num_experts = c.num_experts;
+    p.rank_mode = 0;
+    p.topk_weights = nullptr;
+    p.recv_topk_idx = nullptr;
+    p.recv_topk_weights = nullptr;
     p.layout = c.layout;
     p.N = (int64_t)c.num_ranks * T;
     p.cap = c.layout == EP_LAYOUT_PADDED ? (int64_t)c.num_ranks * c.max_tokens_per_rank
@@ -110,7 +117,15 @@ ep_status enqueue_layout(ep_ctx *ctx, const int64_t *topk_idx, int32_t T, int32_
     }
     h->tokens_per_rank = T;
     h->has_rank_ranges = want_ranges ? 1 : 0;
+    h->rank_mode = 0;
+    h->num_keys = c.num_experts;
     return EP_OK;
+}
+
+int64_t rank_rows_of(const ep_config *c) {
+    const int64_t n = (int64_t)c->num_ranks * c->max_tokens_per_rank;
+    const int64_t kr = c->topk < c->num_ranks ? c->topk : c->num_ranks;
+    return c->layout == EP_LAYOUT_PADDED ? n * c->num_ranks : n * kr;
 }
 
 }  // namespace
@@ -207,6 +222,7 @@ ep_status ep_handle_create(ep_ctx *ctx, ep_handle **out) {
     if (h == nullptr) return EP_ERR_OOM;
     h->ctx = ctx;
     h->tokens_per_rank = -1;
+    h->num_keys = c.num_experts;
     const size_t nk = (size_t)c.num_ranks * c.max_tokens_per_rank * c.topk;
     const size_t er = (size_t)c.num_experts * c.num_ranks;
     bool ok = cudaMalloc(&h->slot, nk * sizeof(int32_t)) == cudaSuccess &&
@@ -248,6 +264,7 @@ ep_status ep_handle_get_info(const ep_handle *h, ep_handle_info *out) {
     out->base = h->base;
     out->tokens_per_expert = h->tokens_per_expert;
     out->has_rank_ranges = h->has_rank_ranges;
+    out->rank_mode = h->rank_mode;
     return EP_OK;
 }
 
@@ -262,6 +279,63 @@ ep_status ep_get_dispatch_layout(ep_ctx *ctx, const int64_t *d_topk_idx, int32_t
     if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
     return enqueue_layout(ctx, d_topk_idx, tokens_per_rank, d_num_tokens_per_rank, d_num_tokens_per_expert,
                           d_is_token_in_rank, /*want_ranges=*/true, handle, (cudaStream_t)stream);
+}
+
+ep_status ep_rank_recv_rows(const ep_config *cfg, int64_t *rows) {
+    const ep_status s = check_config(cfg);
+    if (s != EP_OK) return s;
+    if (rows == nullptr) return EP_ERR_INVALID_ARG;
+    *rows = rank_rows_of(cfg);
+    return EP_OK;
+}
+
+ep_status ep_get_rank_layout(ep_ctx *ctx, const int64_t *d_topk_idx, const float *d_topk_weights,
+                             int32_t tokens_per_rank, int32_t *d_num_tokens_per_rank, int32_t *d_recv_topk_idx,
+                             float *d_recv_topk_weights, ep_handle *handle, void *stream) {
+    if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
+    const ep_config &c = ctx->cfg;
+    if (tokens_per_rank < 0 || tokens_per_rank > c.max_tokens_per_rank) return EP_ERR_INVALID_ARG;
+    if (d_topk_idx == nullptr && tokens_per_rank > 0) return EP_ERR_INVALID_ARG;
+    if (d_recv_topk_weights != nullptr && d_recv_topk_idx == nullptr) return EP_ERR_INVALID_ARG;
+    if (!aligned(d_topk_idx, 8) || !aligned(d_topk_weights, 4) || !aligned(d_num_tokens_per_rank, 4) ||
+        !aligned(d_recv_topk_idx, 4) || !aligned(d_recv_topk_weights, 4))
+        return EP_ERR_INVALID_ARG;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    ep::LayoutParams p;
+    p.topk_idx = d_topk_idx;
+    p.R = c.num_ranks;
+    p.T = tokens_per_rank;
+    p.K = c.topk;
+    p.E = c.num_ranks;  // keys are destination ranks
+    p.L = c.num_experts / c.num_ranks;
+    p.num_experts = c.num_experts;
+    p.rank_mode = 1;
+    p.topk_weights = d_topk_weights;
+    p.recv_topk_idx = d_recv_topk_idx;
+    p.recv_topk_weights = d_recv_topk_weights;
+    p.layout = c.layout;
+    p.N = (int64_t)c.num_ranks * tokens_per_rank;
+    p.cap = c.layout == EP_LAYOUT_PADDED ? (int64_t)c.num_ranks * c.max_tokens_per_rank : rank_rows_of(&c);
+    p.slot = handle->slot;
+    p.src_info = handle->src_info;
+    p.cnt_er = nullptr;
+    p.off_er = nullptr;
+    p.base = handle->base;
+    p.tokens_per_expert = handle->tokens_per_expert;
+    p.user_tokens_per_expert = d_num_tokens_per_rank;
+    p.tokens_per_rank = nullptr;
+    p.is_token_in_rank = nullptr;
+    p.status = ctx->d_status;
+    const cudaError_t err = ep::launch_layout(p, ctx->layout_cluster, ctx->layout_threads, (cudaStream_t)stream);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return err == cudaErrorInvalidConfiguration ? EP_ERR_UNSUPPORTED : EP_ERR_CUDA;
+    }
+    handle->tokens_per_rank = tokens_per_rank;
+    handle->has_rank_ranges = 0;
+    handle->rank_mode = 1;
+    handle->num_keys = c.num_ranks;
+    return EP_OK;
 }
 
 ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, int32_t tokens_per_rank,
@@ -293,7 +367,7 @@ ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, i
     }
     if (N == 0) {
         if (!fresh && d_recv_count != nullptr &&
-            cudaMemcpyAsync(d_recv_count, handle->tokens_per_expert, (size_t)c.num_experts * sizeof(int32_t),
+            cudaMemcpyAsync(d_recv_count, handle->tokens_per_expert, (size_t)handle->num_keys * sizeof(int32_t),
                             cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
             cudaGetLastError();
             return EP_ERR_CUDA;
@@ -310,7 +384,7 @@ ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, i
     p.H = c.hidden;
     p.count_src = handle->tokens_per_expert;
     p.count_dst = fresh ? nullptr : d_recv_count;
-    p.E = c.num_experts;
+    p.E = handle->num_keys;
     p.row_sms = (c.max_sms > 0 && c.max_sms < ctx->num_sms) ? c.max_sms : ctx->num_sms;
     const int cap = grid_cap(ctx, use_fp8 ? ctx->dispatch_bps_fp8 : ctx->dispatch_bps_bf16);
     if (ep::launch_dispatch(p, use_fp8 != 0, cap, /*pdl=*/true, st) != cudaSuccess) {

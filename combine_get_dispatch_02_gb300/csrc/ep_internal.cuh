@@ -17,7 +17,12 @@ constexpr int kLayoutPacked = 1;
 // ------------------------------------------------------------------ layout
 struct LayoutParams {
     const int64_t *topk_idx;   // [N*K]
-    int32_t R, T, K, E, L;     // L = E / R
+    int32_t R, T, K, E, L;     // E = keys (experts, or ranks in rank mode); L = experts per rank
+    int32_t num_experts;       // valid ids are [0, num_experts)
+    int32_t rank_mode;         // 1: keys are destination ranks, one entry per (token, rank)
+    const float *topk_weights; // [N*K] or nullptr (rank mode: weights of the received rows)
+    int32_t *recv_topk_idx;    // rank mode: [rows*K] local expert ids or -1, or nullptr
+    float *recv_topk_weights;  // rank mode: [rows*K] or nullptr
     int32_t layout;
     int64_t N;                 // R*T
     int64_t cap;               // rows per expert buffer (padded) or N*K (packed)

@@ -97,11 +97,21 @@ __device__ __forceinline__ int64_t load_raw(const int64_t *idx, int i, int i1) {
     return i < i1 ? __ldg(idx + i) : -1;
 }
 
-// Expert id of a raw entry, -1 for "none"; ids outside [-1, E) are flagged.
-__device__ __forceinline__ int to_expert(int64_t e, int E, uint32_t *status) {
-    if (e >= 0 && e < E) return (int)e;
-    if (e != -1) atomicOr(status, kStatusBadExpert);
-    return -1;
+// Key of entry i with raw id e: its expert, or in rank mode the rank that
+// owns the expert when no earlier k of the same token goes to that rank; -1
+// for none.  Ids outside [-1, num_experts) are flagged and skipped.
+__device__ __forceinline__ int to_key(const LayoutParams &p, int64_t e, int i) {
+    if (e < 0 || e >= p.num_experts) {
+        if (e != -1) atomicOr(p.status, kStatusBadExpert);
+        return -1;
+    }
+    if (!p.rank_mode) return (int)e;
+    const int d = (int)e / p.L;
+    for (int j = (i / p.K) * p.K; j < i; ++j) {
+        const int64_t e2 = __ldg(p.topk_idx + j);
+        if (e2 >= 0 && e2 < p.num_experts && (int)e2 / p.L == d) return -1;
+    }
+    return d;
 }
 
 template <int NT>
@@ -178,7 +188,7 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
         for (int u = 0; u < kU; ++u) {
             if (ib + u * 32 >= i1) break;  // warp-uniform
             const int i = ib + u * 32 + lane;
-            const int e = to_expert(raw[u], E, p.status);
+            const int e = to_key(p, raw[u], i);
             const uint32_t peers = warp_match(e < 0 ? E : e, ebits);
             // position of this entry among the warp's entries of expert e
             int local = 0;
@@ -199,12 +209,12 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
             const int64_t *row = p.topk_idx + (int64_t)g * K;
             for (int k = 0; k < K; ++k) {
                 const int64_t e = row[k];
-                if (e < 0 || e >= E) continue;
+                if (e < 0 || e >= p.num_experts) continue;
                 const int d = (int)e / p.L;
                 bool seen = false;
                 for (int k2 = 0; k2 < k && !seen; ++k2) {
                     const int64_t e2 = row[k2];
-                    seen = e2 >= 0 && e2 < E && (int)e2 / p.L == d;
+                    seen = e2 >= 0 && e2 < p.num_experts && (int)e2 / p.L == d;
                 }
                 if (seen) continue;
                 atomicAdd(&tok_rank[d], 1);
@@ -294,6 +304,17 @@ __global__ void __launch_bounds__(NT, 1) layout_kernel(const LayoutParams p) {
             if (pos < cap) {
                 s = ebase[e] + pos;
                 p.src_info[s] = i;
+                if (p.recv_topk_idx != nullptr) {  // rank mode: the token's experts on rank e
+                    const int g0 = (i / K) * K;
+                    for (int k2 = 0; k2 < K; ++k2) {
+                        const int64_t e2 = __ldg(p.topk_idx + g0 + k2);
+                        const bool on = e2 >= 0 && e2 < p.num_experts && (int)e2 / p.L == e;
+                        p.recv_topk_idx[(int64_t)s * K + k2] = on ? (int)e2 - e * p.L : -1;
+                        if (p.recv_topk_weights != nullptr)
+                            p.recv_topk_weights[(int64_t)s * K + k2] =
+                                on ? (p.topk_weights != nullptr ? __ldg(p.topk_weights + g0 + k2) : 1.0f) : 0.0f;
+                    }
+                }
             } else {
                 atomicOr(p.status, kStatusCapacity);
             }

@@ -123,6 +123,11 @@ extern "C" ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, 
     lp.K = c.topk;
     lp.E = c.num_experts;
     lp.L = c.num_experts / c.num_ranks;
+    lp.num_experts = c.num_experts;
+    lp.rank_mode = 0;
+    lp.topk_weights = nullptr;
+    lp.recv_topk_idx = nullptr;
+    lp.recv_topk_weights = nullptr;
     lp.layout = c.layout;
     lp.N = N;
     lp.cap = c.layout == EP_LAYOUT_PADDED ? (int64_t)c.num_ranks * c.max_tokens_per_rank

@@ -34,7 +34,7 @@ ENTRY_POINTS = (
     "ep_status_str", "ep_config_check", "ep_recv_rows", "ep_recv_bytes",
     "ep_create", "ep_destroy", "ep_handle_create", "ep_handle_destroy",
     "ep_handle_get_info", "ep_get_dispatch_layout", "ep_dispatch", "ep_combine",
-    "ep_get_device_status", "ep_dispatch_noalloc",
+    "ep_get_device_status", "ep_dispatch_noalloc", "ep_get_rank_layout", "ep_rank_recv_rows",
 )
 
 
@@ -56,7 +56,8 @@ class ep_handle_info(ctypes.Structure):
                 ("rows", ctypes.c_int64), ("slot", ctypes.c_void_p),
                 ("src_info", ctypes.c_void_p), ("cnt_er", ctypes.c_void_p),
                 ("off_er", ctypes.c_void_p), ("base", ctypes.c_void_p),
-                ("tokens_per_expert", ctypes.c_void_p), ("has_rank_ranges", ctypes.c_int32)]
+                ("tokens_per_expert", ctypes.c_void_p), ("has_rank_ranges", ctypes.c_int32),
+                ("rank_mode", ctypes.c_int32)]
 
 
 _lib = None
@@ -88,6 +89,8 @@ def lib() -> ctypes.CDLL:
             "ep_combine": (I32, [P, P, P, P, P, P]),
             "ep_get_device_status": (I32, [P, P]),
             "ep_dispatch_noalloc": (I32, [CFG, P, P, I32, I32, P, P, P, P]),
+            "ep_get_rank_layout": (I32, [P, P, P, I32, P, P, P, P, P]),
+            "ep_rank_recv_rows": (I32, [CFG, ctypes.POINTER(I64)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -182,6 +185,24 @@ def ep_get_dispatch_layout(ctx, topk_idx: torch.Tensor | None, tokens_per_rank: 
         _ptr(num_tokens_per_expert, torch.int32, "num_tokens_per_expert"),
         _ptr(is_token_in_rank, None, "is_token_in_rank"), handle, _stream(stream)),
         "ep_get_dispatch_layout")
+
+
+def ep_rank_recv_rows(cfg: ep_config) -> int:
+    rows = ctypes.c_int64()
+    _check(lib().ep_rank_recv_rows(ctypes.byref(cfg), ctypes.byref(rows)), "ep_rank_recv_rows")
+    return rows.value
+
+
+def ep_get_rank_layout(ctx, topk_idx: torch.Tensor | None, topk_weights: torch.Tensor | None,
+                       tokens_per_rank: int, num_tokens_per_rank: torch.Tensor | None,
+                       recv_topk_idx: torch.Tensor | None, recv_topk_weights: torch.Tensor | None,
+                       handle, stream=None) -> None:
+    _check(lib().ep_get_rank_layout(
+        ctx, _ptr(topk_idx, torch.int64, "topk_idx"), _ptr(topk_weights, torch.float32, "topk_weights"),
+        int(tokens_per_rank), _ptr(num_tokens_per_rank, torch.int32, "num_tokens_per_rank"),
+        _ptr(recv_topk_idx, torch.int32, "recv_topk_idx"),
+        _ptr(recv_topk_weights, torch.float32, "recv_topk_weights"), handle, _stream(stream)),
+        "ep_get_rank_layout")
 
 
 def ep_dispatch(ctx, x: torch.Tensor, topk_idx: torch.Tensor | None, tokens_per_rank: int,

@@ -126,6 +126,9 @@ typedef struct ep_handle_info {
     int32_t has_rank_ranges;   /* 1: cnt_er / off_er belong to the layout held
                                   (ep_get_dispatch_layout computes them; the
                                   layout computed inside ep_dispatch does not) */
+    int32_t rank_mode;         /* 1: a rank-deduplicated layout (ep_get_rank_layout):
+                                  slot / src_info / base / tokens_per_expert are
+                                  per destination rank ([R] instead of [E]) */
 } ep_handle_info;
 
 /* Human-readable name of a status code (static string). */
@@ -173,6 +176,37 @@ ep_status ep_get_dispatch_layout(ep_ctx *ctx, const int64_t *d_topk_idx,
                                  int32_t *d_num_tokens_per_expert,
                                  uint8_t *d_is_token_in_rank,
                                  ep_handle *handle, void *stream);
+
+/* Rank-deduplicated layout, the transport of DeepEP's normal (high-
+ * throughput) kernels (DeepTech announcement, 010bt.com: tokens forwarded per
+ * destination domain; group-limited gating keeps the ranks per token low):
+ * every token is sent ONCE to each rank that owns at least one of its experts
+ * instead of once per expert.  The entry (g, k) that carries token g to rank
+ * d is the first k of the token whose expert lives on d; the rows of rank d
+ * start at d*R*Tmax (padded) or at the prefix of the per-rank counts
+ * (packed) and hold its tokens in ascending g.  The handle then serves
+ * ep_dispatch (topk_idx NULL; receive buffer of ep_rank_recv_rows rows, and
+ * d_recv_count [R] gets the rows per rank) and ep_combine (weights NULL: the
+ * token's rank rows are summed in the order their first expert appears in
+ * its top-k row, fp32, one bf16 rounding; the expert side is expected to
+ * have applied the weights of its local experts).
+ *   d_topk_idx             device int64 [R, T, K]
+ *   d_topk_weights         device fp32 [R*T, K] or NULL (all ones)
+ *   d_num_tokens_per_rank  device int32 [R] or NULL: rows each rank receives
+ *   d_recv_topk_idx        device int32 [rows, K] or NULL: per received row,
+ *                          the token's local expert ids on that rank (e - d*E/R)
+ *                          or -1 for experts on other ranks
+ *   d_recv_topk_weights    device fp32 [rows, K] or NULL (needs d_recv_topk_idx):
+ *                          the matching weights, 0 for other ranks' experts
+ * Rows that receive nothing are not written. */
+ep_status ep_get_rank_layout(ep_ctx *ctx, const int64_t *d_topk_idx, const float *d_topk_weights,
+                             int32_t tokens_per_rank, int32_t *d_num_tokens_per_rank,
+                             int32_t *d_recv_topk_idx, float *d_recv_topk_weights,
+                             ep_handle *handle, void *stream);
+
+/* Receive rows of the rank-deduplicated layout: R*R*Tmax (padded, every rank
+ * can receive every token) or R*Tmax*min(K, R) (packed).  Touches no GPU. */
+ep_status ep_rank_recv_rows(const ep_config *cfg, int64_t *rows);
 
 /* low_latency_dispatch: scatter every token row to the receive rows of its
  * top-k experts, BF16 (bit copy) or FP8 (cast once per token, stored K times).
