@@ -483,9 +483,23 @@ def _e2e(args, w, d, x, idx, wts, out, enqueue, stream):
         res[pipelined] = (time.perf_counter() - t0) / args.e2e_steps * 1e3
     h2d = xh.numel() * 2 + idxh.numel() * 8 + wh.numel() * 4
     d2h = outh[0].numel() * 2
+
+    # the host link alone: the step's H2D and D2H copies, each timed by itself
+    def link_gbs(fn, nbytes, reps=10):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return nbytes * reps / (time.perf_counter() - t0) / 1e9
+
+    h2d_gbs = link_gbs(lambda: xs[0].copy_(xh, non_blocking=True), xh.numel() * 2)
+    d2h_gbs = link_gbs(lambda: outh[0].copy_(outs[0], non_blocking=True), d2h)
     return {"value": N / (res[True] / 1e3) * ws, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": res[True], "ms_per_step_serial": res[False],
-            "pipelining": "H2D / compute / D2H on three streams, two buffer sets"}
+            "pipelining": "H2D / compute / D2H on three streams, two buffer sets",
+            "host_link_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs}}
 
 
 def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,

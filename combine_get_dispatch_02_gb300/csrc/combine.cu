@@ -9,12 +9,16 @@
 // so the result is identical to the oracle's bit for bit.
 //
 // Design: the work item is (token, CPI 256-channel chunks) for one warp, 8
-// channels (one 16-byte row segment) per lane and chunk.  For each group of
-// 8/CPI entries the warp loads the slots and weights once (one lane each,
-// then shuffles) and issues all of the group's 16-byte row loads before the
-// first FMA, so each lane has 8 loads (128 bytes) in flight for any K; the
-// rows are read-only and bypass L1.  One 16-byte store per lane and chunk
-// writes the bf16 result.
+// channels (one 16-byte row segment) per lane and chunk.  The warp loads the
+// token's K slots and weights once (one lane each), keeps the entries that
+// received a row (when some are masked, each lane with a row writes it to a
+// per-warp list at its rank among them), and for
+// each group of 8/CPI of them issues all the group's 16-byte row loads
+// before the first FMA, so each lane has up to 8 loads (128 bytes) in
+// flight however many entries are masked (CPI follows the most entries a
+// token can have rows for: K, or min(K, R) in the rank-deduplicated
+// layout).  Rows are read-only and bypass L1.  One 16-byte
+// store per lane and chunk writes the bf16 result.
 #include <cuda_bf16.h>
 
 #include "ep_internal.cuh"
@@ -28,8 +32,7 @@ constexpr int kChunk = 256;  // channels per lane-row segment (8 per lane)
 constexpr int kLoads = 8;    // 16-byte row loads in flight per lane
 
 // CPI = 256-channel chunks per warp item; entries are taken kLoads / CPI at a
-// time, so every group keeps kLoads loads in flight whatever K is (CPI = 1
-// for K > 4, 2 for K 3..4, 4 for K <= 2).
+// time (CPI = 2 for more than two entries per token, 4 otherwise).
 template <int CPI>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p) {
     constexpr int G = kLoads / CPI;  // entries per group
@@ -41,6 +44,11 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     const int nch = (H + kChunk * CPI - 1) / (kChunk * CPI);
     const int64_t items = p.N * nch;
     const __nv_bfloat16 *y = static_cast<const __nv_bfloat16 *>(p.y);
+    // per-warp list of a token's entries that have rows (when some are masked)
+    __shared__ int32_t list_s[kThreads / 32][32];
+    __shared__ float list_w[kThreads / 32][32];
+    const int wib = threadIdx.x >> 5;
+    const uint32_t all_k = K >= 32 ? 0xFFFFFFFFu : ((1u << K) - 1u);
 
     for (int64_t it = warp; it < items; it += nwarp) {
         const int64_t g = it / nch;
@@ -51,20 +59,40 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[q][j] = 0.0f;
 
-        for (int k0 = 0; k0 < K; k0 += G) {
-            int32_t s_l = -1;
-            float w_l = 1.0f;
-            if (lane < G && k0 + lane < K) {
-                s_l = p.slot[g * K + k0 + lane];
-                if (p.weights != nullptr) w_l = p.weights[g * K + k0 + lane];
+        // the token's entries that received a row, in ascending k, are
+        // taken G at a time (masked entries never occupy a load slot)
+        int32_t s_all = -1;
+        float w_all = 1.0f;
+        if (lane < K) {
+            s_all = p.slot[g * K + lane];
+            if (p.weights != nullptr) w_all = p.weights[g * K + lane];
+        }
+        const uint32_t valid = __ballot_sync(0xFFFFFFFFu, s_all >= 0);
+        const int nv = __popc(valid);
+        const bool dense = valid == all_k;  // warp-uniform
+        if (!dense) {
+            if (s_all >= 0) {
+                const int r = __popc(valid & lanemask_lt());
+                list_s[wib][r] = s_all;
+                list_w[wib][r] = w_all;
             }
+            __syncwarp();
+        }
+        for (int k0 = 0; k0 < nv; k0 += G) {
             int32_t s[G];
             float w[G];
             uint4 v[G][CPI];
 #pragma unroll
             for (int j = 0; j < G; ++j) {
-                s[j] = __shfl_sync(0xFFFFFFFFu, s_l, j);
-                w[j] = __shfl_sync(0xFFFFFFFFu, w_l, j);
+                const int n = k0 + j < nv ? k0 + j : 0;
+                if (dense) {
+                    s[j] = __shfl_sync(0xFFFFFFFFu, s_all, n);
+                    w[j] = __shfl_sync(0xFFFFFFFFu, w_all, n);
+                } else {
+                    s[j] = list_s[wib][n];
+                    w[j] = list_w[wib][n];
+                }
+                if (k0 + j >= nv) s[j] = -1;
             }
 #pragma unroll
             for (int j = 0; j < G; ++j)
@@ -88,6 +116,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
                 }
             }
         }
+        if (!dense) __syncwarp();  // the list is rewritten for the next token
 #pragma unroll
         for (int q = 0; q < CPI; ++q) {
             const int c = c0 + q * kChunk;
@@ -107,7 +136,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
 }  // namespace
 
 namespace {
-int cpi_for(int K) { return K <= 2 ? 4 : (K <= 4 ? 2 : 1); }
+// chunks per item from the most entries a token can have rows for (two
+// chunks measured best from top-3 to top-8, four for top-1 and top-2)
+int cpi_for(int valid) { return valid <= 2 ? 4 : 2; }
 
 template <int CPI>
 int occupancy() {
@@ -120,8 +151,8 @@ int occupancy() {
 }
 }  // namespace
 
-int combine_blocks_per_sm(int K) {
-    switch (cpi_for(K)) {
+int combine_blocks_per_sm(int max_valid) {
+    switch (cpi_for(max_valid)) {
         case 4: return occupancy<4>();
         case 2: return occupancy<2>();
         default: return occupancy<1>();
@@ -129,7 +160,7 @@ int combine_blocks_per_sm(int K) {
 }
 
 cudaError_t launch_combine(const CombineParams &p, int max_blocks, bool pdl, cudaStream_t stream) {
-    const int cpi = cpi_for(p.K);
+    const int cpi = cpi_for(p.max_valid);
     const int nch = (p.H + kChunk * cpi - 1) / (kChunk * cpi);
     const int64_t warps = p.N * nch;
     int64_t blocks = (warps + (kThreads / 32) - 1) / (kThreads / 32);

@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "ep.h"
 #include "ep_internal.cuh"
@@ -21,7 +22,8 @@ struct ep_ctx {
     int layout_threads;
     int dispatch_bps_bf16;
     int dispatch_bps_fp8;
-    int combine_bps;
+    int combine_bps;       // resident combine CTAs per SM, expert layout
+    int combine_bps_rank;  // and rank-deduplicated layout
 };
 
 struct ep_handle {
@@ -41,6 +43,12 @@ struct ep_handle {
 namespace {
 
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// NVTX range around each enqueueing call (free unless a profiler is attached)
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 ep_status check_config(const ep_config *c) {
     if (c == nullptr) return EP_ERR_INVALID_ARG;
@@ -190,6 +198,7 @@ ep_status ep_create(const ep_config *cfg, ep_ctx **out) {
     ctx->dispatch_bps_bf16 = ep::dispatch_blocks_per_sm(false);
     ctx->dispatch_bps_fp8 = ep::dispatch_blocks_per_sm(true);
     ctx->combine_bps = ep::combine_blocks_per_sm(cfg->topk);
+    ctx->combine_bps_rank = ep::combine_blocks_per_sm(cfg->topk < cfg->num_ranks ? cfg->topk : cfg->num_ranks);
     ep::dispatch_init();
     if (cudaMalloc(&ctx->d_status, sizeof(uint32_t)) != cudaSuccess) {
         cudaGetLastError();
@@ -271,6 +280,7 @@ ep_status ep_handle_get_info(const ep_handle *h, ep_handle_info *out) {
 ep_status ep_get_dispatch_layout(ep_ctx *ctx, const int64_t *d_topk_idx, int32_t tokens_per_rank,
                                  int32_t *d_num_tokens_per_rank, int32_t *d_num_tokens_per_expert,
                                  uint8_t *d_is_token_in_rank, ep_handle *handle, void *stream) {
+    NvtxRange nvtx("ep_get_dispatch_layout");
     if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
     if (tokens_per_rank < 0 || tokens_per_rank > ctx->cfg.max_tokens_per_rank) return EP_ERR_INVALID_ARG;
     if (d_topk_idx == nullptr && tokens_per_rank > 0) return EP_ERR_INVALID_ARG;
@@ -292,6 +302,7 @@ ep_status ep_rank_recv_rows(const ep_config *cfg, int64_t *rows) {
 ep_status ep_get_rank_layout(ep_ctx *ctx, const int64_t *d_topk_idx, const float *d_topk_weights,
                              int32_t tokens_per_rank, int32_t *d_num_tokens_per_rank, int32_t *d_recv_topk_idx,
                              float *d_recv_topk_weights, ep_handle *handle, void *stream) {
+    NvtxRange nvtx("ep_get_rank_layout");
     if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
     const ep_config &c = ctx->cfg;
     if (tokens_per_rank < 0 || tokens_per_rank > c.max_tokens_per_rank) return EP_ERR_INVALID_ARG;
@@ -341,6 +352,7 @@ ep_status ep_get_rank_layout(ep_ctx *ctx, const int64_t *d_topk_idx, const float
 ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, int32_t tokens_per_rank,
                       int32_t use_fp8, ep_handle *handle, void *d_recv_x, float *d_recv_scales,
                       int32_t *d_recv_count, void *stream) {
+    NvtxRange nvtx("ep_dispatch");
     if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
     const ep_config &c = ctx->cfg;
     if (tokens_per_rank < 0 || tokens_per_rank > c.max_tokens_per_rank) return EP_ERR_INVALID_ARG;
@@ -396,6 +408,7 @@ ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, i
 
 ep_status ep_combine(ep_ctx *ctx, const void *d_y, const float *d_topk_weights, const ep_handle *handle,
                      void *d_out, void *stream) {
+    NvtxRange nvtx("ep_combine");
     if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
     if (handle->tokens_per_rank < 0) return EP_ERR_NO_LAYOUT;
     const ep_config &c = ctx->cfg;
@@ -412,7 +425,9 @@ ep_status ep_combine(ep_ctx *ctx, const void *d_y, const float *d_topk_weights, 
     p.N = N;
     p.K = c.topk;
     p.H = c.hidden;
-    if (ep::launch_combine(p, grid_cap(ctx, ctx->combine_bps), /*pdl=*/true, (cudaStream_t)stream) !=
+    p.max_valid = handle->rank_mode ? (c.topk < c.num_ranks ? c.topk : c.num_ranks) : c.topk;
+    const int bps = handle->rank_mode ? ctx->combine_bps_rank : ctx->combine_bps;
+    if (ep::launch_combine(p, grid_cap(ctx, bps), /*pdl=*/true, (cudaStream_t)stream) !=
         cudaSuccess) {
         cudaGetLastError();
         return EP_ERR_CUDA;

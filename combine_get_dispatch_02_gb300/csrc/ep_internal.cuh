@@ -79,11 +79,12 @@ struct CombineParams {
     void *out;                 // bf16 [N, H]
     int64_t N;
     int32_t K, H;
+    int32_t max_valid;         // most entries of one token that have rows (K, or min(K, R) by rank)
 };
 
 cudaError_t launch_combine(const CombineParams &p, int max_blocks, bool pdl,
                            cudaStream_t stream);
-int combine_blocks_per_sm(int K);
+int combine_blocks_per_sm(int max_valid);
 
 // ------------------------------------------------------------------ device helpers
 #ifdef __CUDACC__

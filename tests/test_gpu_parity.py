@@ -151,6 +151,9 @@ DISPATCH_CASES = {
     "h384_fp8": wl.TINY.with_(hidden=384, use_fp8=True, x_scale="loguniform"),  # chunk tail
     "h200_bf16": wl.TINY.with_(hidden=200),                                     # half-segment tail
     "k32_fp8": wl.TINY.with_(num_experts=64, topk=32, use_fp8=True),
+    "h16384_bf16": wl.TINY.with_(hidden=16384),                                 # row kernel, 64 KB smem
+    "h32768_fp8": wl.TINY.with_(hidden=32768, use_fp8=True, tokens_per_rank=8,
+                                max_tokens_per_rank=8),                          # warp-item kernel
     "packed_fp8": wl.SKEW.with_(layout=wl.PACKED),
 }
 
@@ -264,6 +267,8 @@ COMBINE_CASES = {
     "k32": (wl.TINY.with_(num_experts=64, topk=32), True),
     "k1": (wl.TINY.with_(topk=1), True),
     "h200": (wl.TINY.with_(hidden=200), True),
+    "h32768_k2": (wl.TINY.with_(hidden=32768, topk=2, tokens_per_rank=8, max_tokens_per_rank=8), True),
+    "k3": (wl.TINY.with_(topk=3), True),
     "skew_packed": (wl.SKEW.with_(layout=wl.PACKED), True),
 }
 
