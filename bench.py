@@ -56,6 +56,8 @@ def _args():
                     help="time the sweep grid (one JSON line per point) instead of the bench step")
     ap.add_argument("--sweep-filter", default="", help="only sweep points whose name contains this")
     ap.add_argument("--sweep-reps", type=int, default=10)
+    ap.add_argument("--round-trip-reps", type=int, default=50,
+                    help="reps per chunk size of the dispatch -> identity expert -> combine round trip (0: skip)")
     return ap.parse_args()
 
 
@@ -258,6 +260,15 @@ def _algorithmic_bytes(w, M):
     return disp, disp_kernel, comb
 
 
+def _identity_bytes(w, M):
+    """Identity expert: read each received row (and its FP8 scales) and the
+    entries' slots, write the row as bf16."""
+    N, K, H = w.num_tokens, w.topk, w.hidden
+    if w.use_fp8:
+        return M * (H + (H // 128) * 4) + M * H * 2 + N * K * 4
+    return M * H * 2 * 2 + N * K * 4
+
+
 def run_ours(args):
     import torch
     ws, rank, local = _dist()
@@ -405,6 +416,32 @@ def run_ours(args):
     except Exception as exc:  # report, do not hide, a capture failure
         graph_us = (f"capture failed: {exc}", None)
 
+    # the round trip with the identity expert between dispatch and combine,
+    # pipelined over token chunks (layout included), and the identity
+    # expert alone
+    round_trip = None
+    if args.round_trip_reps > 0 and not args.rank:
+        y_rt = recv if not w.use_fp8 else torch.empty(buf.rows, H, dtype=torch.bfloat16, device="cuda")
+        ident_us = timed(lambda: ep.ep_expert_identity(ctx, h.raw, w.use_fp8, recv, scales, y_rt, 0, N, stream))
+        chunks = sorted({0} | {c for c in (N // 16, N // 8, N // 4, N // 2) if c > 0})
+        per_chunk = {}
+        for c in chunks:
+            per_chunk[str(c)] = timed(lambda: ep.ep_round_trip(ctx, x, idx, w.tokens_per_rank, wts, w.use_fp8,
+                                                               h.raw, recv, scales, y_rt, out, c, stream),
+                                      reps=args.round_trip_reps)[0]
+        best = min(chunks, key=lambda c: per_chunk[str(c)])
+        ident_bytes = _identity_bytes(w, M)
+        ident_gbs = ident_bytes / (ident_us[0] / 1e6) / 1e9 if ident_us[0] == ident_us[0] else None
+        round_trip = {
+            "chunk_tokens_us_median": per_chunk, "best_chunk_tokens": best,
+            "tokens_per_s_best": N / (per_chunk[str(best)] / 1e6),
+            "identity_expert_alone_median_us": ident_us[0],
+            "identity_expert_roofline": {"bound": "hbm", "achieved": ident_gbs, "algorithmic_bytes": ident_bytes,
+                                         "frac": ident_gbs / _peaks()[0] if ident_gbs else None},
+            "note": "chunk 0 = one chunk; layout computed in every call",
+        }
+        del y_rt
+
     # HBM copy bandwidth of this GPU through torch (context for the fractions)
     cbuf = torch.empty(2 << 30, dtype=torch.uint8, device="cuda")
     cdst = torch.empty_like(cbuf)
@@ -421,7 +458,7 @@ def run_ours(args):
             torch.distributed.destroy_process_group()
         return
     _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
-            e2e, clk, graph_us, copy_gbs)
+            e2e, clk, graph_us, copy_gbs, round_trip)
     if ws > 1:
         torch.distributed.destroy_process_group()
 
@@ -503,7 +540,7 @@ def _e2e(args, w, d, x, idx, wts, out, enqueue, stream):
 
 
 def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
-            e2e, clk, graph_us=None, copy_gbs=None):
+            e2e, clk, graph_us=None, copy_gbs=None, round_trip=None):
     peak, peak_kind = _peaks()
     disp_bytes, disp_kernel_bytes, comb_bytes = _algorithmic_bytes(w, M)
     comb_avg_s = statistics.mean(comb_ms) / 1e3
@@ -541,6 +578,7 @@ def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, la
                               "traffic": _traffic("dispatch", DISPATCH_SRC, w.name),
                               "algorithmic_bytes": disp_kernel_bytes},
         "e2e": e2e,
+        "round_trip": round_trip,
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
         "host_cores": os.cpu_count(),

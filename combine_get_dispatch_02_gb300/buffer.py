@@ -218,6 +218,31 @@ class Buffer:
         ep.ep_combine(self._ctx, hidden_states, topk_weights, handle.raw, out)
         return out
 
+    def round_trip(self, hidden_states: torch.Tensor, topk_idx: torch.Tensor | None,
+                   topk_weights: torch.Tensor | None, use_fp8: bool = True, chunk_tokens: int = 0,
+                   handle: Handle | None = None, recv=None, y: torch.Tensor | None = None,
+                   out: torch.Tensor | None = None):
+        """Dispatch -> identity expert -> combine over chunks of ``chunk_tokens``
+        tokens (0: one chunk); topk_idx=None reuses the layout in ``handle``.
+        Returns (out [R*T, H] bf16, handle)."""
+        T = hidden_states.numel() // (self.num_ranks * self.hidden)
+        if hidden_states.numel() != self.num_ranks * T * self.hidden:
+            raise ValueError("hidden_states must be [R, T, H]")
+        if topk_idx is not None and self._tokens_per_rank(topk_idx) != T:
+            raise ValueError("topk_idx and hidden_states disagree on T")
+        if topk_idx is None and handle is None:
+            raise ValueError("reusing a layout needs a handle")
+        handle = handle or Handle(self)
+        recv_x, recv_scales = recv if recv is not None else self.alloc_recv(use_fp8)
+        dev = hidden_states.device
+        if y is None:
+            y = recv_x if not use_fp8 else torch.empty(self.rows, self.hidden, dtype=torch.bfloat16, device=dev)
+        if out is None:
+            out = torch.empty(self.num_ranks * T, self.hidden, dtype=torch.bfloat16, device=dev)
+        ep.ep_round_trip(self._ctx, hidden_states, topk_idx, T, topk_weights, use_fp8, handle.raw,
+                         recv_x, recv_scales if use_fp8 else None, y, out, chunk_tokens)
+        return out, handle
+
     def device_status(self) -> int:
         """Synchronise the current stream; return and clear the device status."""
         return ep.ep_get_device_status(self._ctx)

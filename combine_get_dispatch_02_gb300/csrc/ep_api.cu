@@ -24,6 +24,8 @@ struct ep_ctx {
     int dispatch_bps_fp8;
     int combine_bps;       // resident combine CTAs per SM, expert layout
     int combine_bps_rank;  // and rank-deduplicated layout
+    int identity_bps_bf16;
+    int identity_bps_fp8;
 };
 
 struct ep_handle {
@@ -136,6 +138,81 @@ int64_t rank_rows_of(const ep_config *c) {
     return c->layout == EP_LAYOUT_PADDED ? n * c->num_ranks : n * kr;
 }
 
+// The dispatch kernel over tokens [g0, g1) of the handle's layout (g1 > g0).
+ep_status enqueue_dispatch(ep_ctx *ctx, const ep_handle *h, const void *x, int64_t g0, int64_t g1, bool fp8,
+                           void *recv, float *recv_scales, int32_t *count_dst, cudaStream_t st) {
+    const ep_config &c = ctx->cfg;
+    ep::DispatchParams p;
+    p.x = static_cast<const uint16_t *>(x) + g0 * c.hidden;
+    p.slot = h->slot + g0 * c.topk;
+    p.recv = recv;
+    p.recv_scales = recv_scales;
+    p.N = g1 - g0;
+    p.K = c.topk;
+    p.H = c.hidden;
+    p.count_src = h->tokens_per_expert;
+    p.count_dst = count_dst;
+    p.E = h->num_keys;
+    p.row_sms = (c.max_sms > 0 && c.max_sms < ctx->num_sms) ? c.max_sms : ctx->num_sms;
+    const int cap = grid_cap(ctx, fp8 ? ctx->dispatch_bps_fp8 : ctx->dispatch_bps_bf16);
+    if (ep::launch_dispatch(p, fp8, cap, /*pdl=*/true, st) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    return EP_OK;
+}
+
+// The identity expert over the rows received by entries of tokens [g0, g1).
+ep_status enqueue_identity(ep_ctx *ctx, const ep_handle *h, bool fp8, const void *recv, const float *recv_scales,
+                           void *y, int64_t g0, int64_t g1, cudaStream_t st) {
+    const ep_config &c = ctx->cfg;
+    ep::IdentityParams p;
+    p.recv = recv;
+    p.recv_scales = recv_scales;
+    p.slot = h->slot + g0 * c.topk;
+    p.n = (g1 - g0) * c.topk;
+    p.H = c.hidden;
+    p.y = y;
+    const int cap = grid_cap(ctx, fp8 ? ctx->identity_bps_fp8 : ctx->identity_bps_bf16);
+    if (ep::launch_identity(p, fp8, cap, /*pdl=*/true, st) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    return EP_OK;
+}
+
+// The combine kernel over tokens [g0, g1) (g1 > g0).
+ep_status enqueue_combine(ep_ctx *ctx, const ep_handle *h, const void *y, const float *w, int64_t g0, int64_t g1,
+                          void *out, cudaStream_t st) {
+    const ep_config &c = ctx->cfg;
+    ep::CombineParams p;
+    p.y = y;
+    p.weights = w != nullptr ? w + g0 * c.topk : nullptr;
+    p.slot = h->slot + g0 * c.topk;
+    p.out = static_cast<uint16_t *>(out) + g0 * c.hidden;
+    p.N = g1 - g0;
+    p.K = c.topk;
+    p.H = c.hidden;
+    p.max_valid = h->rank_mode ? (c.topk < c.num_ranks ? c.topk : c.num_ranks) : c.topk;
+    const int bps = h->rank_mode ? ctx->combine_bps_rank : ctx->combine_bps;
+    if (ep::launch_combine(p, grid_cap(ctx, bps), /*pdl=*/true, st) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    return EP_OK;
+}
+
+// Checks shared by the calls that run on a handle's cached layout over a
+// token range: 0 <= g0 <= g1 <= R*T of the layout.
+ep_status check_range(const ep_ctx *ctx, const ep_handle *h, int64_t g0, int64_t g1) {
+    if (ctx == nullptr || h == nullptr || h->ctx != ctx) return EP_ERR_INVALID_ARG;
+    if (h->tokens_per_rank < 0) return EP_ERR_NO_LAYOUT;
+    const int64_t N = (int64_t)ctx->cfg.num_ranks * h->tokens_per_rank;
+    if (g0 < 0 || g1 < g0 || g1 > N) return EP_ERR_INVALID_ARG;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    return EP_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -199,6 +276,8 @@ ep_status ep_create(const ep_config *cfg, ep_ctx **out) {
     ctx->dispatch_bps_fp8 = ep::dispatch_blocks_per_sm(true);
     ctx->combine_bps = ep::combine_blocks_per_sm(cfg->topk);
     ctx->combine_bps_rank = ep::combine_blocks_per_sm(cfg->topk < cfg->num_ranks ? cfg->topk : cfg->num_ranks);
+    ctx->identity_bps_bf16 = ep::identity_blocks_per_sm(false);
+    ctx->identity_bps_fp8 = ep::identity_blocks_per_sm(true);
     ep::dispatch_init();
     if (cudaMalloc(&ctx->d_status, sizeof(uint32_t)) != cudaSuccess) {
         cudaGetLastError();
@@ -386,24 +465,8 @@ ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, i
         }
         return EP_OK;
     }
-    ep::DispatchParams p;
-    p.x = d_x;
-    p.slot = handle->slot;
-    p.recv = d_recv_x;
-    p.recv_scales = d_recv_scales;
-    p.N = N;
-    p.K = c.topk;
-    p.H = c.hidden;
-    p.count_src = handle->tokens_per_expert;
-    p.count_dst = fresh ? nullptr : d_recv_count;
-    p.E = handle->num_keys;
-    p.row_sms = (c.max_sms > 0 && c.max_sms < ctx->num_sms) ? c.max_sms : ctx->num_sms;
-    const int cap = grid_cap(ctx, use_fp8 ? ctx->dispatch_bps_fp8 : ctx->dispatch_bps_bf16);
-    if (ep::launch_dispatch(p, use_fp8 != 0, cap, /*pdl=*/true, st) != cudaSuccess) {
-        cudaGetLastError();
-        return EP_ERR_CUDA;
-    }
-    return EP_OK;
+    return enqueue_dispatch(ctx, handle, d_x, 0, N, use_fp8 != 0, d_recv_x, d_recv_scales,
+                            fresh ? nullptr : d_recv_count, st);
 }
 
 ep_status ep_combine(ep_ctx *ctx, const void *d_y, const float *d_topk_weights, const ep_handle *handle,
@@ -417,20 +480,83 @@ ep_status ep_combine(ep_ctx *ctx, const void *d_y, const float *d_topk_weights, 
     if (d_y == nullptr || d_out == nullptr) return EP_ERR_INVALID_ARG;
     if (!aligned(d_y, 16) || !aligned(d_out, 16) || !aligned(d_topk_weights, 4)) return EP_ERR_INVALID_ARG;
     if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
-    ep::CombineParams p;
-    p.y = d_y;
-    p.weights = d_topk_weights;
-    p.slot = handle->slot;
-    p.out = d_out;
-    p.N = N;
-    p.K = c.topk;
-    p.H = c.hidden;
-    p.max_valid = handle->rank_mode ? (c.topk < c.num_ranks ? c.topk : c.num_ranks) : c.topk;
-    const int bps = handle->rank_mode ? ctx->combine_bps_rank : ctx->combine_bps;
-    if (ep::launch_combine(p, grid_cap(ctx, bps), /*pdl=*/true, (cudaStream_t)stream) !=
-        cudaSuccess) {
-        cudaGetLastError();
-        return EP_ERR_CUDA;
+    return enqueue_combine(ctx, handle, d_y, d_topk_weights, 0, N, d_out, (cudaStream_t)stream);
+}
+
+ep_status ep_dispatch_range(ep_ctx *ctx, const void *d_x, int32_t use_fp8, const ep_handle *handle,
+                            int64_t token_begin, int64_t token_end, void *d_recv_x, float *d_recv_scales,
+                            void *stream) {
+    NvtxRange nvtx("ep_dispatch_range");
+    const ep_status s = check_range(ctx, handle, token_begin, token_end);
+    if (s != EP_OK) return s;
+    if (use_fp8 != 0 && use_fp8 != 1) return EP_ERR_INVALID_ARG;
+    if (use_fp8 && ctx->cfg.hidden % 128 != 0) return EP_ERR_UNSUPPORTED;
+    if (token_end == token_begin) return EP_OK;
+    if (d_x == nullptr || d_recv_x == nullptr || (use_fp8 && d_recv_scales == nullptr)) return EP_ERR_INVALID_ARG;
+    if (!aligned(d_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_recv_scales, 4)) return EP_ERR_INVALID_ARG;
+    return enqueue_dispatch(ctx, handle, d_x, token_begin, token_end, use_fp8 != 0, d_recv_x, d_recv_scales,
+                            nullptr, (cudaStream_t)stream);
+}
+
+ep_status ep_combine_range(ep_ctx *ctx, const void *d_y, const float *d_topk_weights, const ep_handle *handle,
+                           int64_t token_begin, int64_t token_end, void *d_out, void *stream) {
+    NvtxRange nvtx("ep_combine_range");
+    const ep_status s = check_range(ctx, handle, token_begin, token_end);
+    if (s != EP_OK) return s;
+    if (token_end == token_begin) return EP_OK;
+    if (d_y == nullptr || d_out == nullptr) return EP_ERR_INVALID_ARG;
+    if (!aligned(d_y, 16) || !aligned(d_out, 16) || !aligned(d_topk_weights, 4)) return EP_ERR_INVALID_ARG;
+    return enqueue_combine(ctx, handle, d_y, d_topk_weights, token_begin, token_end, d_out, (cudaStream_t)stream);
+}
+
+ep_status ep_expert_identity(ep_ctx *ctx, const ep_handle *handle, int32_t use_fp8, const void *d_recv_x,
+                             const float *d_recv_scales, void *d_y, int64_t token_begin, int64_t token_end,
+                             void *stream) {
+    NvtxRange nvtx("ep_expert_identity");
+    const ep_status s = check_range(ctx, handle, token_begin, token_end);
+    if (s != EP_OK) return s;
+    if (use_fp8 != 0 && use_fp8 != 1) return EP_ERR_INVALID_ARG;
+    if (use_fp8 && ctx->cfg.hidden % 128 != 0) return EP_ERR_UNSUPPORTED;
+    if (token_end == token_begin || (!use_fp8 && d_y == d_recv_x)) return EP_OK;
+    if (d_recv_x == nullptr || d_y == nullptr || (use_fp8 && d_recv_scales == nullptr)) return EP_ERR_INVALID_ARG;
+    if (!aligned(d_recv_x, 16) || !aligned(d_y, 16) || !aligned(d_recv_scales, 4)) return EP_ERR_INVALID_ARG;
+    return enqueue_identity(ctx, handle, use_fp8 != 0, d_recv_x, d_recv_scales, d_y, token_begin, token_end,
+                            (cudaStream_t)stream);
+}
+
+ep_status ep_round_trip(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, int32_t tokens_per_rank,
+                        const float *d_topk_weights, int32_t use_fp8, ep_handle *handle, void *d_recv_x,
+                        float *d_recv_scales, void *d_y, void *d_out, int32_t chunk_tokens, void *stream) {
+    NvtxRange nvtx("ep_round_trip");
+    if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
+    const ep_config &c = ctx->cfg;
+    if (tokens_per_rank < 0 || tokens_per_rank > c.max_tokens_per_rank) return EP_ERR_INVALID_ARG;
+    if (use_fp8 != 0 && use_fp8 != 1) return EP_ERR_INVALID_ARG;
+    if (use_fp8 && c.hidden % 128 != 0) return EP_ERR_UNSUPPORTED;
+    const int64_t N = (int64_t)c.num_ranks * tokens_per_rank;
+    if (N > 0 && (d_x == nullptr || d_recv_x == nullptr || d_y == nullptr || d_out == nullptr ||
+                  (use_fp8 && d_recv_scales == nullptr)))
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(d_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_recv_scales, 4) || !aligned(d_y, 16) ||
+        !aligned(d_out, 16) || !aligned(d_topk_weights, 4) || !aligned(d_topk_idx, 8))
+        return EP_ERR_INVALID_ARG;
+    if (d_topk_idx == nullptr && tokens_per_rank > 0 && handle->tokens_per_rank != tokens_per_rank)
+        return EP_ERR_NO_LAYOUT;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (d_topk_idx != nullptr || tokens_per_rank == 0) {
+        const ep_status s = enqueue_layout(ctx, d_topk_idx, tokens_per_rank, nullptr, nullptr, nullptr,
+                                           /*want_ranges=*/false, handle, st);
+        if (s != EP_OK) return s;
+    }
+    const int64_t chunk = (chunk_tokens <= 0 || chunk_tokens > N) ? N : chunk_tokens;
+    for (int64_t g0 = 0; g0 < N; g0 += chunk) {
+        const int64_t g1 = g0 + chunk < N ? g0 + chunk : N;
+        ep_status s = enqueue_dispatch(ctx, handle, d_x, g0, g1, use_fp8 != 0, d_recv_x, d_recv_scales, nullptr, st);
+        if (s == EP_OK && (use_fp8 || d_y != d_recv_x))
+            s = enqueue_identity(ctx, handle, use_fp8 != 0, d_recv_x, d_recv_scales, d_y, g0, g1, st);
+        if (s == EP_OK) s = enqueue_combine(ctx, handle, d_y, d_topk_weights, g0, g1, d_out, st);
+        if (s != EP_OK) return s;
     }
     return EP_OK;
 }

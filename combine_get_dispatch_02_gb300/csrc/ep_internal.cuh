@@ -86,6 +86,20 @@ cudaError_t launch_combine(const CombineParams &p, int max_blocks, bool pdl,
                            cudaStream_t stream);
 int combine_blocks_per_sm(int max_valid);
 
+// ------------------------------------------------------------------ identity expert
+struct IdentityParams {
+    const void *recv;          // e4m3 or bf16 [rows, H]
+    const float *recv_scales;  // [rows, H/128] (FP8)
+    const int32_t *slot;       // the range's entries [n]
+    int64_t n;
+    int32_t H;
+    void *y;                   // bf16 [rows, H]
+};
+
+cudaError_t launch_identity(const IdentityParams &p, bool fp8, int max_blocks, bool pdl,
+                            cudaStream_t stream);
+int identity_blocks_per_sm(bool fp8);
+
 // ------------------------------------------------------------------ device helpers
 #ifdef __CUDACC__
 // Programmatic dependent launch: let the next kernel in the stream start, and

@@ -35,6 +35,7 @@ ENTRY_POINTS = (
     "ep_create", "ep_destroy", "ep_handle_create", "ep_handle_destroy",
     "ep_handle_get_info", "ep_get_dispatch_layout", "ep_dispatch", "ep_combine",
     "ep_get_device_status", "ep_dispatch_noalloc", "ep_get_rank_layout", "ep_rank_recv_rows",
+    "ep_dispatch_range", "ep_combine_range", "ep_expert_identity", "ep_round_trip",
 )
 
 
@@ -91,6 +92,10 @@ def lib() -> ctypes.CDLL:
             "ep_dispatch_noalloc": (I32, [CFG, P, P, I32, I32, P, P, P, P]),
             "ep_get_rank_layout": (I32, [P, P, P, I32, P, P, P, P, P]),
             "ep_rank_recv_rows": (I32, [CFG, ctypes.POINTER(I64)]),
+            "ep_dispatch_range": (I32, [P, P, I32, P, I64, I64, P, P, P]),
+            "ep_combine_range": (I32, [P, P, P, P, I64, I64, P, P]),
+            "ep_expert_identity": (I32, [P, P, I32, P, P, P, I64, I64, P]),
+            "ep_round_trip": (I32, [P, P, P, I32, P, I32, P, P, P, P, P, I32, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -220,6 +225,42 @@ def ep_combine(ctx, y: torch.Tensor, topk_weights: torch.Tensor | None, handle,
     _check(lib().ep_combine(
         ctx, _ptr(y, torch.bfloat16, "y"), _ptr(topk_weights, torch.float32, "topk_weights"),
         handle, _ptr(out, torch.bfloat16, "out"), _stream(stream)), "ep_combine")
+
+
+def ep_dispatch_range(ctx, x: torch.Tensor, use_fp8: bool, handle, token_begin: int, token_end: int,
+                      recv_x: torch.Tensor, recv_scales: torch.Tensor | None, stream=None) -> None:
+    _check(lib().ep_dispatch_range(
+        ctx, _ptr(x, torch.bfloat16, "x"), int(bool(use_fp8)), handle, int(token_begin), int(token_end),
+        _ptr(recv_x, None, "recv_x"), _ptr(recv_scales, torch.float32, "recv_scales"),
+        _stream(stream)), "ep_dispatch_range")
+
+
+def ep_combine_range(ctx, y: torch.Tensor, topk_weights: torch.Tensor | None, handle,
+                     token_begin: int, token_end: int, out: torch.Tensor, stream=None) -> None:
+    _check(lib().ep_combine_range(
+        ctx, _ptr(y, torch.bfloat16, "y"), _ptr(topk_weights, torch.float32, "topk_weights"),
+        handle, int(token_begin), int(token_end), _ptr(out, torch.bfloat16, "out"),
+        _stream(stream)), "ep_combine_range")
+
+
+def ep_expert_identity(ctx, handle, use_fp8: bool, recv_x: torch.Tensor, recv_scales: torch.Tensor | None,
+                       y: torch.Tensor, token_begin: int, token_end: int, stream=None) -> None:
+    _check(lib().ep_expert_identity(
+        ctx, handle, int(bool(use_fp8)), _ptr(recv_x, None, "recv_x"),
+        _ptr(recv_scales, torch.float32, "recv_scales"), _ptr(y, torch.bfloat16, "y"),
+        int(token_begin), int(token_end), _stream(stream)), "ep_expert_identity")
+
+
+def ep_round_trip(ctx, x: torch.Tensor, topk_idx: torch.Tensor | None, tokens_per_rank: int,
+                  topk_weights: torch.Tensor | None, use_fp8: bool, handle, recv_x: torch.Tensor,
+                  recv_scales: torch.Tensor | None, y: torch.Tensor, out: torch.Tensor,
+                  chunk_tokens: int = 0, stream=None) -> None:
+    _check(lib().ep_round_trip(
+        ctx, _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int64, "topk_idx"), int(tokens_per_rank),
+        _ptr(topk_weights, torch.float32, "topk_weights"), int(bool(use_fp8)), handle,
+        _ptr(recv_x, None, "recv_x"), _ptr(recv_scales, torch.float32, "recv_scales"),
+        _ptr(y, torch.bfloat16, "y"), _ptr(out, torch.bfloat16, "out"), int(chunk_tokens),
+        _stream(stream)), "ep_round_trip")
 
 
 def ep_get_device_status(ctx, stream=None) -> int:

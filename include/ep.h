@@ -239,6 +239,57 @@ ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
 ep_status ep_combine(ep_ctx *ctx, const void *d_y, const float *d_topk_weights,
                      const ep_handle *handle, void *d_out, void *stream);
 
+/* Token-range forms of ep_dispatch and ep_combine on the layout already in
+ * handle (the layout reuse of "如何突破MoE通信瓶颈：DeepEP跨节点优化技术终极指南",
+ * section 技术解析: computed once, then reused by every later call), for a
+ * caller that pipelines a step over chunks of tokens.  Global tokens are
+ * g = r*T + t; a range [token_begin, token_end) must satisfy
+ * 0 <= token_begin <= token_end <= R*T of the layout (else
+ * EP_ERR_INVALID_ARG; no layout: EP_ERR_NO_LAYOUT); an empty range enqueues
+ * nothing.  d_x, d_topk_weights and d_out are the full [R*T, ...] arrays, as
+ * for ep_dispatch / ep_combine.  ep_dispatch_range writes the receive rows of
+ * the range's entries (and nothing else; no counts); ep_combine_range writes
+ * rows [token_begin, token_end) of d_out.  Ranges that together cover every
+ * token give results identical, bit for bit, to one ep_dispatch (topk_idx
+ * NULL) or ep_combine call.  One kernel each. */
+ep_status ep_dispatch_range(ep_ctx *ctx, const void *d_x, int32_t use_fp8, const ep_handle *handle,
+                            int64_t token_begin, int64_t token_end, void *d_recv_x,
+                            float *d_recv_scales, void *stream);
+ep_status ep_combine_range(ep_ctx *ctx, const void *d_y, const float *d_topk_weights,
+                           const ep_handle *handle, int64_t token_begin, int64_t token_end,
+                           void *d_out, void *stream);
+
+/* Identity expert, the stand-in for the expert computation between dispatch
+ * and combine in a round trip (FP8 dispatch / BF16 combine, same page,
+ * section 核心优势).  For every receive row that an entry of a token in
+ * [token_begin, token_end) received, writes that row of d_y with the BF16
+ * value the row holds:
+ *   use_fp8 = 1:  y[row, c] = bf16(e4m3(q[row, c]) * scale[row, c / 128])
+ *                 (exact fp32 product, nearest-even bf16)
+ *   use_fp8 = 0:  y[row] = recv[row] (bit copy; nothing to do when
+ *                 d_y == d_recv_x)
+ *   d_recv_x, d_recv_scales  what ep_dispatch wrote (read only)
+ *   d_y            device bf16 [rows, H] (16-byte aligned); other rows are
+ *                  not written
+ * Range rules as for ep_dispatch_range.  One kernel. */
+ep_status ep_expert_identity(ep_ctx *ctx, const ep_handle *handle, int32_t use_fp8,
+                             const void *d_recv_x, const float *d_recv_scales, void *d_y,
+                             int64_t token_begin, int64_t token_end, void *stream);
+
+/* One dispatch -> identity expert -> combine round trip, pipelined over
+ * chunks of chunk_tokens global tokens: the layout (when d_topk_idx is
+ * given, as in ep_dispatch), then for each chunk ep_dispatch_range,
+ * ep_expert_identity and ep_combine_range, each kernel started early behind
+ * the one before it (programmatic dependent launch).  A chunk's receive
+ * rows are read back soon after they are written, while they can still be
+ * in L2.  chunk_tokens <= 0 (or >= R*T) is one chunk.  d_out is identical,
+ * bit for bit, for every chunk size.  Arguments as for the calls it makes;
+ * d_y may equal d_recv_x for BF16. */
+ep_status ep_round_trip(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
+                        int32_t tokens_per_rank, const float *d_topk_weights, int32_t use_fp8,
+                        ep_handle *handle, void *d_recv_x, float *d_recv_scales, void *d_y,
+                        void *d_out, int32_t chunk_tokens, void *stream);
+
 /* Dispatch for callers that cannot allocate device memory (no counterpart on
  * the pages: it is this library's own addition).  Same operation and output as
  * ep_dispatch with d_topk_idx given (layout, then BF16 copy or FP8 cast into

@@ -78,6 +78,7 @@ def use_library(path: str | None):
     lib.orc_quant_token.argtypes = [P, I32, P, P]
     lib.orc_dispatch.argtypes = [I64, I32, I32, I32, P, P, P, P]
     lib.orc_combine.argtypes = [I64, I32, I32, P, P, P, P]
+    lib.orc_dequant_rows.argtypes = [I64, I32, I32, P, P, P, P]
     for name in ("orc_f32_to_bf16_n", "orc_bf16_to_f32_n",
                  "orc_f32_to_e4m3_n", "orc_e4m3_to_f32_n"):
         getattr(lib, name).argtypes = [P, P, I64]
@@ -228,6 +229,22 @@ def dispatch(x_bits: np.ndarray, slot: np.ndarray, rows: int, use_fp8: bool,
     recv = np.zeros((rows, H), np.uint16) if recv is None else recv
     _load().orc_dispatch(N, K, H, 0, _p(x), _p(sl), _p(recv), None)
     return recv
+
+
+# ---------------------------------------------------------------- identity expert
+
+def dequant_rows(q: np.ndarray, scales: np.ndarray, slot: np.ndarray,
+                 y: np.ndarray | None = None) -> np.ndarray:
+    """BF16 rows (uint16 bits) of the FP8 rows the entries of slot [N, K]
+    received: y[row] = bf16(e4m3(q[row]) * scale).  Other rows keep y's
+    contents (zeros when y is not given)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    sl = np.ascontiguousarray(slot, dtype=np.int32)
+    rows, H = q.shape
+    y = np.zeros((rows, H), np.uint16) if y is None else y
+    _load().orc_dequant_rows(sl.shape[0], sl.shape[1], H, _p(q), _p(sc), _p(sl), _p(y))
+    return y
 
 
 # ---------------------------------------------------------------- combine

@@ -408,6 +408,26 @@ void orc_dispatch(int64_t N, int K, int H, int use_fp8, const uint16_t *x,
 }
 
 /* ------------------------------------------------------------------ */
+/* Identity expert for FP8 rows: the BF16 value each code stands for   */
+/* ------------------------------------------------------------------ */
+
+/* For every entry with slot >= 0: y[slot, c] = bf16( e4m3(q[slot, c]) * scale[slot, c / 128] )
+ * (one IEEE binary32 multiply, one round to nearest-even bf16). */
+void orc_dequant_rows(int64_t N, int K, int H, const uint8_t *q, const float *scales,
+                      const int32_t *slot, uint16_t *y)
+{
+    for (int64_t i = 0; i < N * K; i++) {
+        int64_t s = slot[i];
+        if (s < 0)
+            continue;
+        for (int c = 0; c < H; c++) {
+            float v = orc_e4m3_to_f32(q[s * H + c]) * scales[s * (H / 128) + c / 128];
+            y[s * H + c] = orc_f32_to_bf16(v);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* Combine  [API] low_latency_combine; [LL] BF16 combine               */
 /* ------------------------------------------------------------------ */
 

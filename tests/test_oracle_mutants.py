@@ -73,6 +73,9 @@ MUTANTS = {
     "rank layout: rank buffers sized by T instead of Tmax": (
         "rbase[d] = layout == ORC_LAYOUT_PADDED ? (int64_t)d * R * Tmax : acc;",
         "rbase[d] = layout == ORC_LAYOUT_PADDED ? (int64_t)d * R * T : acc;"),
+    "identity expert: scale of the wrong block": (
+        "float v = orc_e4m3_to_f32(q[s * H + c]) * scales[s * (H / 128) + c / 128];",
+        "float v = orc_e4m3_to_f32(q[s * H + c]) * scales[s * (H / 128)];"),
     "layout: padded overflow not dropped": (
         "            if (layout == ORC_LAYOUT_PADDED && pos >= cap) {",
         "            if (0) {"),
@@ -93,6 +96,7 @@ def _pins():
         yield f"rank_brute_force[{seed}]", (lambda seed=seed: pins.test_rank_layout_brute_force(oracle, seed))
     for name in ("tiny", "skew"):
         yield f"invariants[{name}]", (lambda name=name: pins.test_layout_invariants(oracle, name))
+    yield "dequant", lambda: pins.test_dequant_rows_golden_and_bound(oracle)
     yield "bf16_torch", lambda: pins.test_bf16_matches_torch(oracle)
     yield "fp8_torch", lambda: pins.test_fp8_matches_torch_cast_of_products(oracle)
     yield "e4m3_torch", lambda: pins.test_e4m3_encode_matches_torch(oracle)

@@ -347,6 +347,25 @@ def test_fp8_golden_blocks(orc):
     assert n == 2
 
 
+def test_dequant_rows_golden_and_bound(orc):
+    # codes of the first golden FP8 block at scale 2^-7: 448 -> 3.5, -224 -> -1.75, 56 -> 0.4375
+    q = np.zeros((2, 128), np.uint8)
+    q[1, :3] = [0x7E, 0xF6, 0x66]
+    sc = np.array([[1.0], [0.0078125]], np.float32)
+    y = orc.dequant_rows(q, sc, np.array([[1, -1]], np.int32))
+    assert list(_bits_to_bf16_float(y[1, :4])) == [3.5, -1.75, 0.4375, 0.0]
+    assert np.all(y[0] == 0)  # a row no entry received is left alone
+    # dequantised rows are within the FP8 bound of the token they came from
+    rng = np.random.default_rng(15)
+    x = _random_tokens(rng, 16, 512)
+    qq, ss = orc.quant_token(x)
+    yy = orc.dequant_rows(qq, ss, np.arange(16, dtype=np.int32).reshape(16, 1))
+    xf = _bits_to_bf16_float(x).astype(np.float64)
+    s_full = np.repeat(ss, 128, axis=1).astype(np.float64)
+    bound = (2.0 ** -4 * np.abs(xf) + 2.0 ** -10 * s_full) * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(xf) * 1.07
+    assert np.all(np.abs(_bits_to_bf16_float(yy).astype(np.float64) - xf) <= bound)
+
+
 def test_fp8_zero_block_uses_floor(orc):
     q, s = orc.quant_token(np.zeros((1, 256), np.uint16))
     assert np.all(q == 0)
