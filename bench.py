@@ -422,8 +422,11 @@ def run_ours(args):
     round_trip = None
     if args.round_trip_reps > 0 and not args.rank:
         y_rt = recv if not w.use_fp8 else torch.empty(buf.rows, H, dtype=torch.bfloat16, device="cuda")
-        ident_us = timed(lambda: ep.ep_expert_identity(ctx, h.raw, w.use_fp8, recv, scales, y_rt, 0, N, stream))
-        chunks = sorted({0} | {c for c in (N // 16, N // 8, N // 4, N // 2) if c > 0})
+        # BF16: the expert output is the receive buffer itself (nothing to time)
+        ident_us = (timed(lambda: ep.ep_expert_identity(ctx, h.raw, True, recv, scales, y_rt, 0, N, stream))
+                    if w.use_fp8 else (float("nan"), float("nan")))
+        auto = ep.ep_round_trip_auto_chunk(ctx, w.use_fp8)
+        chunks = [0, ep.EP_CHUNK_AUTO] + sorted({c for c in (N // 16, N // 8, N // 4, N // 2) if c > 0} - {auto})
         per_chunk = {}
         for c in chunks:
             per_chunk[str(c)] = timed(lambda: ep.ep_round_trip(ctx, x, idx, w.tokens_per_rank, wts, w.use_fp8,
@@ -432,13 +435,16 @@ def run_ours(args):
         best = min(chunks, key=lambda c: per_chunk[str(c)])
         ident_bytes = _identity_bytes(w, M)
         ident_gbs = ident_bytes / (ident_us[0] / 1e6) / 1e9 if ident_us[0] == ident_us[0] else None
+        if ident_gbs is None:
+            ident_us, ident_bytes = (None, None), None
         round_trip = {
             "chunk_tokens_us_median": per_chunk, "best_chunk_tokens": best,
             "tokens_per_s_best": N / (per_chunk[str(best)] / 1e6),
             "identity_expert_alone_median_us": ident_us[0],
             "identity_expert_roofline": {"bound": "hbm", "achieved": ident_gbs, "algorithmic_bytes": ident_bytes,
                                          "frac": ident_gbs / _peaks()[0] if ident_gbs else None},
-            "note": "chunk 0 = one chunk; layout computed in every call",
+            "auto_chunk_tokens": auto,
+            "note": "chunk 0 = one chunk, -1 = automatic (L2-sized); layout computed in every call",
         }
         del y_rt
 

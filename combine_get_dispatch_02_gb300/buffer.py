@@ -223,8 +223,8 @@ class Buffer:
                    handle: Handle | None = None, recv=None, y: torch.Tensor | None = None,
                    out: torch.Tensor | None = None):
         """Dispatch -> identity expert -> combine over chunks of ``chunk_tokens``
-        tokens (0: one chunk); topk_idx=None reuses the layout in ``handle``.
-        Returns (out [R*T, H] bf16, handle)."""
+        tokens (0: one chunk, -1: the L2-sized automatic chunk); topk_idx=None
+        reuses the layout in ``handle``.  Returns (out [R*T, H] bf16, handle)."""
         T = hidden_states.numel() // (self.num_ranks * self.hidden)
         if hidden_states.numel() != self.num_ranks * T * self.hidden:
             raise ValueError("hidden_states must be [R, T, H]")

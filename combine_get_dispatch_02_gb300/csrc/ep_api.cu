@@ -3,6 +3,7 @@
 // the host except ep_get_device_status, and none allocates except
 // ep_create / ep_handle_create, so a dispatch + combine sequence can be
 // captured in a CUDA graph.
+#include <limits.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -26,6 +27,7 @@ struct ep_ctx {
     int combine_bps_rank;  // and rank-deduplicated layout
     int identity_bps_bf16;
     int identity_bps_fp8;
+    int64_t l2_bytes;
 };
 
 struct ep_handle {
@@ -202,6 +204,19 @@ ep_status enqueue_combine(ep_ctx *ctx, const ep_handle *h, const void *y, const 
     return EP_OK;
 }
 
+// Automatic chunk of ep_round_trip: the most tokens whose receive rows
+// (payload, FP8 scales, and the bf16 expert output unless it is written in
+// place) fill about 70% of L2, a multiple of 64 tokens and at least 64.
+int32_t auto_chunk(const ep_ctx *ctx, bool fp8, bool rank_mode) {
+    const ep_config &c = ctx->cfg;
+    const int64_t rows_per_token = rank_mode ? (c.topk < c.num_ranks ? c.topk : c.num_ranks) : c.topk;
+    const int64_t row_bytes = fp8 ? (int64_t)c.hidden + c.hidden / 32 + 2 * (int64_t)c.hidden : 2 * (int64_t)c.hidden;
+    const int64_t per_token = rows_per_token * row_bytes;
+    int64_t chunk = ctx->l2_bytes * 7 / 10 / per_token / 64 * 64;
+    if (chunk < 64) chunk = 64;
+    return chunk > INT32_MAX ? INT32_MAX : (int32_t)chunk;
+}
+
 // Checks shared by the calls that run on a handle's cached layout over a
 // token range: 0 <= g0 <= g1 <= R*T of the layout.
 ep_status check_range(const ep_ctx *ctx, const ep_handle *h, int64_t g0, int64_t g1) {
@@ -276,6 +291,12 @@ ep_status ep_create(const ep_config *cfg, ep_ctx **out) {
     ctx->dispatch_bps_fp8 = ep::dispatch_blocks_per_sm(true);
     ctx->combine_bps = ep::combine_blocks_per_sm(cfg->topk);
     ctx->combine_bps_rank = ep::combine_blocks_per_sm(cfg->topk < cfg->num_ranks ? cfg->topk : cfg->num_ranks);
+    int l2 = 0;
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, ctx->device) != cudaSuccess) {
+        cudaGetLastError();
+        l2 = 0;
+    }
+    ctx->l2_bytes = l2;
     ctx->identity_bps_bf16 = ep::identity_blocks_per_sm(false);
     ctx->identity_bps_fp8 = ep::identity_blocks_per_sm(true);
     ep::dispatch_init();
@@ -542,6 +563,7 @@ ep_status ep_round_trip(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
         return EP_ERR_INVALID_ARG;
     if (d_topk_idx == nullptr && tokens_per_rank > 0 && handle->tokens_per_rank != tokens_per_rank)
         return EP_ERR_NO_LAYOUT;
+    if (chunk_tokens < EP_CHUNK_AUTO) return EP_ERR_INVALID_ARG;
     if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     if (d_topk_idx != nullptr || tokens_per_rank == 0) {
@@ -549,7 +571,9 @@ ep_status ep_round_trip(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
                                            /*want_ranges=*/false, handle, st);
         if (s != EP_OK) return s;
     }
-    const int64_t chunk = (chunk_tokens <= 0 || chunk_tokens > N) ? N : chunk_tokens;
+    int64_t chunk = chunk_tokens == EP_CHUNK_AUTO ? auto_chunk(ctx, use_fp8 != 0, handle->rank_mode != 0)
+                                                  : chunk_tokens;
+    if (chunk <= 0 || chunk > N) chunk = N;
     for (int64_t g0 = 0; g0 < N; g0 += chunk) {
         const int64_t g1 = g0 + chunk < N ? g0 + chunk : N;
         ep_status s = enqueue_dispatch(ctx, handle, d_x, g0, g1, use_fp8 != 0, d_recv_x, d_recv_scales, nullptr, st);
@@ -558,6 +582,13 @@ ep_status ep_round_trip(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
         if (s == EP_OK) s = enqueue_combine(ctx, handle, d_y, d_topk_weights, g0, g1, d_out, st);
         if (s != EP_OK) return s;
     }
+    return EP_OK;
+}
+
+ep_status ep_round_trip_auto_chunk(const ep_ctx *ctx, int32_t use_fp8, int32_t rank_layout, int32_t *chunk_tokens) {
+    if (ctx == nullptr || chunk_tokens == nullptr) return EP_ERR_INVALID_ARG;
+    if (use_fp8 != 0 && use_fp8 != 1) return EP_ERR_INVALID_ARG;
+    *chunk_tokens = auto_chunk(ctx, use_fp8 != 0, rank_layout != 0);
     return EP_OK;
 }
 

@@ -121,6 +121,13 @@ __device__ __forceinline__ uint4 ld_nc_na_v4(const void *p) {
     return v;
 }
 
+// 8-byte form of the load above.
+__device__ __forceinline__ uint2 ld_nc_na_v2(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
 // 16-byte streaming store (evict-first): the written rows are not read again
 // by this kernel.
 __device__ __forceinline__ void st_cs_v4(void *p, uint4 v) {

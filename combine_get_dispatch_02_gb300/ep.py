@@ -36,7 +36,10 @@ ENTRY_POINTS = (
     "ep_handle_get_info", "ep_get_dispatch_layout", "ep_dispatch", "ep_combine",
     "ep_get_device_status", "ep_dispatch_noalloc", "ep_get_rank_layout", "ep_rank_recv_rows",
     "ep_dispatch_range", "ep_combine_range", "ep_expert_identity", "ep_round_trip",
+    "ep_round_trip_auto_chunk",
 )
+
+EP_CHUNK_AUTO = -1
 
 
 class EPError(RuntimeError):
@@ -96,6 +99,7 @@ def lib() -> ctypes.CDLL:
             "ep_combine_range": (I32, [P, P, P, P, I64, I64, P, P]),
             "ep_expert_identity": (I32, [P, P, I32, P, P, P, I64, I64, P]),
             "ep_round_trip": (I32, [P, P, P, I32, P, I32, P, P, P, P, P, I32, P]),
+            "ep_round_trip_auto_chunk": (I32, [P, I32, I32, ctypes.POINTER(I32)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -261,6 +265,13 @@ def ep_round_trip(ctx, x: torch.Tensor, topk_idx: torch.Tensor | None, tokens_pe
         _ptr(recv_x, None, "recv_x"), _ptr(recv_scales, torch.float32, "recv_scales"),
         _ptr(y, torch.bfloat16, "y"), _ptr(out, torch.bfloat16, "out"), int(chunk_tokens),
         _stream(stream)), "ep_round_trip")
+
+
+def ep_round_trip_auto_chunk(ctx, use_fp8: bool, rank_layout: bool = False) -> int:
+    n = ctypes.c_int32(0)
+    _check(lib().ep_round_trip_auto_chunk(ctx, int(bool(use_fp8)), int(bool(rank_layout)), ctypes.byref(n)),
+           "ep_round_trip_auto_chunk")
+    return n.value
 
 
 def ep_get_device_status(ctx, stream=None) -> int:

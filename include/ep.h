@@ -276,19 +276,31 @@ ep_status ep_expert_identity(ep_ctx *ctx, const ep_handle *handle, int32_t use_f
                              const void *d_recv_x, const float *d_recv_scales, void *d_y,
                              int64_t token_begin, int64_t token_end, void *stream);
 
+/* chunk_tokens of ep_round_trip that asks for the automatic chunk size. */
+#define EP_CHUNK_AUTO (-1)
+
 /* One dispatch -> identity expert -> combine round trip, pipelined over
  * chunks of chunk_tokens global tokens: the layout (when d_topk_idx is
  * given, as in ep_dispatch), then for each chunk ep_dispatch_range,
  * ep_expert_identity and ep_combine_range, each kernel started early behind
  * the one before it (programmatic dependent launch).  A chunk's receive
  * rows are read back soon after they are written, while they can still be
- * in L2.  chunk_tokens <= 0 (or >= R*T) is one chunk.  d_out is identical,
- * bit for bit, for every chunk size.  Arguments as for the calls it makes;
- * d_y may equal d_recv_x for BF16. */
+ * in L2.  chunk_tokens: 0 (or >= R*T) is one chunk, EP_CHUNK_AUTO the size
+ * ep_round_trip_auto_chunk gives, below -1 EP_ERR_INVALID_ARG.  d_out is
+ * identical, bit for bit, for every chunk size.  Arguments as for the calls
+ * it makes; d_y may equal d_recv_x for BF16. */
 ep_status ep_round_trip(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
                         int32_t tokens_per_rank, const float *d_topk_weights, int32_t use_fp8,
                         ep_handle *handle, void *d_recv_x, float *d_recv_scales, void *d_y,
                         void *d_out, int32_t chunk_tokens, void *stream);
+
+/* The chunk size EP_CHUNK_AUTO stands for: the most tokens whose receive
+ * rows (payload, FP8 scales and the bf16 expert output: K rows per token,
+ * min(K, R) for a rank-deduplicated layout when rank_layout != 0) take
+ * about 70% of the device's L2, rounded down to a multiple of 64 tokens, at
+ * least 64.  Host only. */
+ep_status ep_round_trip_auto_chunk(const ep_ctx *ctx, int32_t use_fp8, int32_t rank_layout,
+                                   int32_t *chunk_tokens);
 
 /* Dispatch for callers that cannot allocate device memory (no counterpart on
  * the pages: it is this library's own addition).  Same operation and output as

@@ -202,7 +202,7 @@ def test_round_trip_parity_every_chunk_size(name):
     recv = buf.alloc_recv(w.use_fp8)
     y = recv[0] if not w.use_fp8 else torch.empty(buf.rows, w.hidden, dtype=torch.bfloat16, device="cuda")
     h = None
-    for chunk in [0, 1, 7, 512, N - 1, N]:
+    for chunk in [0, 1, 7, 512, N - 1, N, ep.EP_CHUNK_AUTO]:
         out, h = buf.round_trip(x, idx_d if h is None else None, wts_d, use_fp8=w.use_fp8,
                                 chunk_tokens=chunk, handle=h, recv=recv, y=y)
         assert buf.device_status() == ep.EP_OK
@@ -256,3 +256,22 @@ def test_round_trip_graph_replay_matches_eager():
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
     assert buf.device_status() == ep.EP_OK
+
+
+def test_auto_chunk_fills_most_of_l2():
+    w = wl.LL
+    buf = make_buffer(w)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    H, K = w.hidden, w.topk
+    for fp8, row in ((True, H + H // 32 + 2 * H), (False, 2 * H)):
+        c = ep.ep_round_trip_auto_chunk(buf.ctx, fp8)
+        assert c % 64 == 0 and c >= 64
+        assert c * K * row <= 0.7 * l2 < (c + 64) * K * row
+    r = min(K, w.num_ranks)
+    assert ep.ep_round_trip_auto_chunk(buf.ctx, True, True) == \
+        max(64, int(l2 * 7 // 10 // (r * (H + H // 32 + 2 * H)) // 64 * 64))
+    h = buf.new_handle()  # kept alive across the call
+    with pytest.raises(ep.EPError) as e:
+        ep.ep_round_trip(buf.ctx, torch.empty(1, dtype=torch.bfloat16, device="cuda"), None, 0, None, True,
+                         h.raw, None, None, None, None, -2)
+    assert e.value.status == ep.EP_ERR_INVALID_ARG
