@@ -34,6 +34,7 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
 COMBINE_SRC = os.path.join(ROOT, "combine_get_dispatch_02_gb300", "csrc", "combine.cu")
 DISPATCH_SRC = os.path.join(ROOT, "combine_get_dispatch_02_gb300", "csrc", "dispatch.cu")
+EXPERT_SRC = os.path.join(ROOT, "combine_get_dispatch_02_gb300", "csrc", "expert.cu")
 
 
 def _args():
@@ -442,7 +443,8 @@ def run_ours(args):
             "tokens_per_s_best": N / (per_chunk[str(best)] / 1e6),
             "identity_expert_alone_median_us": ident_us[0],
             "identity_expert_roofline": {"bound": "hbm", "achieved": ident_gbs, "algorithmic_bytes": ident_bytes,
-                                         "frac": ident_gbs / _peaks()[0] if ident_gbs else None},
+                                         "frac": ident_gbs / _peaks()[0] if ident_gbs else None,
+                                         "traffic": _traffic("identity", EXPERT_SRC, w.name) if ident_gbs else None},
             "auto_chunk_tokens": auto,
             "note": "chunk 0 = one chunk, -1 = automatic (L2-sized); layout computed in every call",
         }
@@ -453,6 +455,7 @@ def run_ours(args):
     cdst = torch.empty_like(cbuf)
     copy_gbs = 2 * cbuf.numel() / (timed(lambda: cdst.copy_(cbuf), reps=10)[0] / 1e6) / 1e9
     del cbuf, cdst
+    torch.cuda.empty_cache()
 
     # end to end through the public API with host buffers
     e2e = None if args.no_e2e else _e2e(args, w, d, x, idx, wts, out, enqueue, stream)

@@ -118,10 +118,13 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const DispatchParams
 // thread issues K bulk asynchronous copies (cp.async.bulk) of the whole row
 // (and of its scale row) to the K receive rows.  Each destination row is
 // written as one contiguous transfer by the copy engine instead of 512-byte
-// pieces from many warps.  Two row buffers alternate, so the casts of the
-// next token overlap the copies of the previous one; the next token's row
-// and slots are loaded while the current one is cast.  Needs H % 512 == 0
-// and H <= 16384.
+// pieces from many warps.  NB row buffers form a ring, so the casts of the
+// next tokens overlap the copies of earlier ones; the next token's row is
+// loaded while the current one is cast.  Launched behind the layout kernel
+// (programmatic dependent launch), a CTA first casts up to NB of its tokens
+// into the ring and only then waits for the slots, so most of the layout's
+// run time is spent loading and casting rows.  Needs H % 512 == 0 and
+// H <= 16384.
 // CTAs per SM: about 1024 threads, at least 2 (measured best at H = 7168)
 int row_blocks_per_sm(int H) {
     const int b = 16384 / H;
@@ -136,21 +139,82 @@ __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t byt
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// wait until at most one committed group still reads shared memory
-__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// wait until at most N committed groups still read shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// FP8 cast of this thread's 16 channels (two 16-byte bf16 loads): codes and
+// the scale of their 128-channel block (8 lanes share a block).
+__device__ __forceinline__ void cast16(uint4 ca, uint4 cb, uint4 &q, float &scale) {
+    const uint32_t u[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+    float f[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        f[2 * j] = bf16_lo(u[j]);
+        f[2 * j + 1] = bf16_hi(u[j]);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+    const float ac = fmaxf(amax, 1e-4f);
+    scale = __fdiv_rn(ac, 448.0f);
+    const float inv = __fdiv_rn(448.0f, ac);
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = cast_pair(__fmul_rn(f[4 * j], inv), __fmul_rn(f[4 * j + 1], inv));
+        const uint32_t hi = cast_pair(__fmul_rn(f[4 * j + 2], inv), __fmul_rn(f[4 * j + 3], inv));
+        w[j] = lo | (hi << 16);
+    }
+    q = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// This thread's part of a row buffer: FP8 codes + scale, or the bf16 copy.
 template <bool FP8>
+__device__ __forceinline__ void put_row(uint8_t *row, int t, int H, uint4 ca, uint4 cb, uint4 q, float scale) {
+    if constexpr (FP8) {
+        *reinterpret_cast<uint4 *>(row + t * 16) = q;
+        if ((t & 7) == 0) reinterpret_cast<float *>(row + H)[t >> 3] = scale;
+    } else {
+        *reinterpret_cast<uint4 *>(row + t * 32) = ca;
+        *reinterpret_cast<uint4 *>(row + t * 32 + 16) = cb;
+    }
+}
+
+// Warp 0: the K copies of one row buffer (lane k < K holds slot k), as one
+// bulk group.
+template <bool FP8>
+__device__ __forceinline__ void send_row(const DispatchParams &p, int32_t my_slot, const uint8_t *row, int lane) {
+    const int H = p.H;
+    const int payload = FP8 ? H : 2 * H;
+#pragma unroll 1
+    for (int k = 0; k < p.K; ++k) {
+        const int32_t s = __shfl_sync(0xFFFFFFFFu, my_slot, k);
+        if (lane == 0 && s >= 0) {
+            bulk_store(static_cast<uint8_t *>(p.recv) + (int64_t)s * payload, smem_addr(row), payload);
+            if constexpr (FP8) bulk_store(p.recv_scales + (int64_t)s * (H / 128), smem_addr(row + H), H / 32);
+        }
+    }
+    if (lane == 0) bulk_commit();
+}
+
+template <bool FP8, int NB>
 __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchParams p) {
     extern __shared__ __align__(128) uint8_t row_smem[];
     const int H = p.H, K = p.K;
     const int t = threadIdx.x, lane = t & 31;
-    const int payload = FP8 ? H : 2 * H;             // bytes of one receive row
-    const int rowb = FP8 ? H + H / 32 : 2 * H;       // bytes of one buffer
+    const int rowb = FP8 ? H + H / 32 : 2 * H;  // bytes of one buffer
     const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(p.x);
+    const int64_t G = gridDim.x;
 
     int64_t g = blockIdx.x;
     uint4 a = make_uint4(0, 0, 0, 0), b = a;
@@ -158,85 +222,63 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
         a = ld_nc_na_v4(x + g * H + t * 16);
         b = ld_nc_na_v4(x + g * H + t * 16 + 8);
     }
-    // slots come from the layout kernel (launched just before with programmatic
-    // dependent launch): the first token is loaded, cast and laid out in
-    // shared memory before waiting for them
-    bool waited = false;
-    int32_t slot_next = -1;
 
-    for (int it = 0; g < p.N; g += gridDim.x, ++it) {
-        uint8_t *row = row_smem + (it & 1) * rowb;
+    // 1. Before the slots exist: cast up to `pre_max` tokens into the ring.
+    const int pre_max = p.prestage < NB ? p.prestage : NB;
+    int pre = 0;
+    for (; pre < pre_max && g < p.N; ++pre) {
         const uint4 ca = a, cb = b;
-        const int64_t gn = g + gridDim.x;
+        const int64_t gn = g + G;
         if (gn < p.N) {
             a = ld_nc_na_v4(x + gn * H + t * 16);
             b = ld_nc_na_v4(x + gn * H + t * 16 + 8);
         }
         uint4 q = make_uint4(0, 0, 0, 0);
         float scale = 0.0f;
-        if constexpr (FP8) {
-            const uint32_t u[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
-            float f[16];
+        if constexpr (FP8) cast16(ca, cb, q, scale);
+        put_row<FP8>(row_smem + pre * rowb, t, H, ca, cb, q, scale);
+        g = gn;
+    }
+    fence_proxy_async_smem();  // make the rows visible to the copy engine
+    pdl_wait();                // slots (and counts) of the layout kernel
+    if (p.count_dst != nullptr && blockIdx.x == 0)
+        for (int e = t; e < p.E; e += blockDim.x) p.count_dst[e] = p.count_src[e];
+    __syncthreads();
+    if (t < 32) {
+        int32_t my_slot[NB];  // all staged tokens' slots in flight at once
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                f[2 * j] = bf16_lo(u[j]);
-                f[2 * j + 1] = bf16_hi(u[j]);
-            }
-            float amax = 0.0f;
+        for (int j = 0; j < NB; ++j)
+            my_slot[j] = (j < pre && lane < K) ? p.slot[((int64_t)blockIdx.x + (int64_t)j * G) * K + lane] : -1;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-            const float ac = fmaxf(amax, 1e-4f);
-            scale = __fdiv_rn(ac, 448.0f);
-            const float inv = __fdiv_rn(448.0f, ac);
-            uint32_t w[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t lo = cast_pair(__fmul_rn(f[4 * j], inv), __fmul_rn(f[4 * j + 1], inv));
-                const uint32_t hi = cast_pair(__fmul_rn(f[4 * j + 2], inv), __fmul_rn(f[4 * j + 3], inv));
-                w[j] = lo | (hi << 16);
-            }
-            q = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        // this buffer was last filled two tokens ago: its copies must have read it
-        if (it >= 2 && t == 0) bulk_wait_read_1();
-        __syncthreads();
-        if constexpr (FP8) {
-            *reinterpret_cast<uint4 *>(row + t * 16) = q;
-            if ((lane & 7) == 0) reinterpret_cast<float *>(row + H)[t >> 3] = scale;
-        } else {
-            *reinterpret_cast<uint4 *>(row + t * 32) = ca;
-            *reinterpret_cast<uint4 *>(row + t * 32 + 16) = cb;
-        }
-        fence_proxy_async_smem();  // make the row visible to the copy engine
-        if (!waited) {
-            pdl_wait();
-            waited = true;
-            if (p.count_dst != nullptr && blockIdx.x == 0)
-                for (int e = t; e < p.E; e += blockDim.x) p.count_dst[e] = p.count_src[e];
-            slot_next = t < K ? p.slot[g * K + t] : -1;
+        for (int j = 0; j < NB; ++j)
+            if (j < pre) send_row<FP8>(p, my_slot[j], row_smem + j * rowb, lane);
+    }
+
+    // 2. The remaining tokens through the ring (one bulk group per token);
+    // each token's slots are loaded one token ahead.
+    int32_t slot_next = (t < K && g < p.N) ? p.slot[g * K + t] : -1;
+    for (int it = pre; g < p.N; ++it) {
+        uint8_t *row = row_smem + (it % NB) * rowb;
+        const uint4 ca = a, cb = b;
+        const int64_t gn = g + G;
+        if (gn < p.N) {
+            a = ld_nc_na_v4(x + gn * H + t * 16);
+            b = ld_nc_na_v4(x + gn * H + t * 16 + 8);
         }
         const int32_t my_slot = slot_next;
-        if (gn < p.N) slot_next = t < K ? p.slot[gn * K + t] : -1;
+        if (t < K && gn < p.N) slot_next = p.slot[gn * K + t];
+        uint4 q = make_uint4(0, 0, 0, 0);
+        float scale = 0.0f;
+        if constexpr (FP8) cast16(ca, cb, q, scale);
+        // this buffer was last filled NB tokens ago: its copies must have read it
+        if (t == 0) bulk_wait_read<NB - 1>();
         __syncthreads();
-        if (t < 32) {
-#pragma unroll 1
-            for (int k = 0; k < K; ++k) {
-                const int32_t s = __shfl_sync(0xFFFFFFFFu, my_slot, k);
-                if (lane == 0 && s >= 0) {
-                    bulk_store(static_cast<uint8_t *>(p.recv) + (int64_t)s * payload, smem_addr(row), payload);
-                    if constexpr (FP8)
-                        bulk_store(p.recv_scales + (int64_t)s * (H / 128), smem_addr(row + H), H / 32);
-                }
-            }
-            if (lane == 0) bulk_commit();
-        }
+        put_row<FP8>(row, t, H, ca, cb, q, scale);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (t < 32) send_row<FP8>(p, my_slot, row, lane);
+        g = gn;
     }
-    if (!waited) pdl_wait();  // a CTA without tokens still orders the count copy
-    if (!waited && p.count_dst != nullptr && blockIdx.x == 0)
-        for (int e = t; e < p.E; e += blockDim.x) p.count_dst[e] = p.count_src[e];
     if (t == 0) bulk_wait_all();  // copies read shared memory until they finish
 }
 
@@ -286,10 +328,32 @@ void dispatch_init() {
     cudaDeviceGetAttribute(&g_smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     cudaDeviceGetAttribute(&g_smem_per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     // the row kernel asks for more than the 48 KB default (see above)
-    cudaFuncSetAttribute(dispatch_row_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
-    cudaFuncSetAttribute(dispatch_row_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
+    cudaFuncSetAttribute(dispatch_row_kernel<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
+    cudaFuncSetAttribute(dispatch_row_kernel<false, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
+    cudaFuncSetAttribute(dispatch_row_kernel<false, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
+    cudaFuncSetAttribute(dispatch_row_kernel<true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
+    cudaFuncSetAttribute(dispatch_row_kernel<true, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
+    cudaFuncSetAttribute(dispatch_row_kernel<true, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
     cudaGetLastError();
 }
+
+namespace {
+// Row buffers in the ring: as many of 8, 4, 2 as the shared memory the
+// occupancy cap grants anyway holds.
+int ring_buffers(bool fp8, int H, size_t smem) {
+    const size_t rowb = fp8 ? (size_t)H + H / 32 : 2 * (size_t)H;
+    return smem >= 8 * rowb ? 8 : (smem >= 4 * rowb ? 4 : 2);
+}
+
+template <bool FP8>
+cudaError_t launch_row(const cudaLaunchConfig_t &cfg, int nb, const DispatchParams &p) {
+    switch (nb) {
+        case 8: return cudaLaunchKernelEx(&cfg, dispatch_row_kernel<FP8, 8>, p);
+        case 4: return cudaLaunchKernelEx(&cfg, dispatch_row_kernel<FP8, 4>, p);
+        default: return cudaLaunchKernelEx(&cfg, dispatch_row_kernel<FP8, 2>, p);
+    }
+}
+}  // namespace
 
 cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks, bool pdl,
                             cudaStream_t stream) {
@@ -304,12 +368,15 @@ cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks, b
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)blocks, 1, 1);
         cfg.blockDim = dim3(p.H / 16, 1, 1);
-        cfg.dynamicSmemBytes = row_smem_for_occupancy(fp8, p.H, bps);
+        const size_t smem = row_smem_for_occupancy(fp8, p.H, bps);
+        const int nb = ring_buffers(fp8, p.H, smem);
+        cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = pdl ? 1 : 0;
-        return fp8 ? cudaLaunchKernelEx(&cfg, dispatch_row_kernel<true>, p)
-                   : cudaLaunchKernelEx(&cfg, dispatch_row_kernel<false>, p);
+        DispatchParams q = p;
+        if (q.prestage < 1) q.prestage = 1;
+        return fp8 ? launch_row<true>(cfg, nb, q) : launch_row<false>(cfg, nb, q);
     }
     const int nch = (p.H + kChunk - 1) / kChunk;
     const int64_t warps = p.N * nch;

@@ -142,7 +142,8 @@ int64_t rank_rows_of(const ep_config *c) {
 
 // The dispatch kernel over tokens [g0, g1) of the handle's layout (g1 > g0).
 ep_status enqueue_dispatch(ep_ctx *ctx, const ep_handle *h, const void *x, int64_t g0, int64_t g1, bool fp8,
-                           void *recv, float *recv_scales, int32_t *count_dst, cudaStream_t st) {
+                           void *recv, float *recv_scales, int32_t *count_dst, bool behind_layout,
+                           cudaStream_t st) {
     const ep_config &c = ctx->cfg;
     ep::DispatchParams p;
     p.x = static_cast<const uint16_t *>(x) + g0 * c.hidden;
@@ -156,6 +157,7 @@ ep_status enqueue_dispatch(ep_ctx *ctx, const ep_handle *h, const void *x, int64
     p.count_dst = count_dst;
     p.E = h->num_keys;
     p.row_sms = (c.max_sms > 0 && c.max_sms < ctx->num_sms) ? c.max_sms : ctx->num_sms;
+    p.prestage = behind_layout ? 8 : 1;
     const int cap = grid_cap(ctx, fp8 ? ctx->dispatch_bps_fp8 : ctx->dispatch_bps_bf16);
     if (ep::launch_dispatch(p, fp8, cap, /*pdl=*/true, st) != cudaSuccess) {
         cudaGetLastError();
@@ -487,7 +489,7 @@ ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, i
         return EP_OK;
     }
     return enqueue_dispatch(ctx, handle, d_x, 0, N, use_fp8 != 0, d_recv_x, d_recv_scales,
-                            fresh ? nullptr : d_recv_count, st);
+                            fresh ? nullptr : d_recv_count, fresh, st);
 }
 
 ep_status ep_combine(ep_ctx *ctx, const void *d_y, const float *d_topk_weights, const ep_handle *handle,
@@ -516,7 +518,7 @@ ep_status ep_dispatch_range(ep_ctx *ctx, const void *d_x, int32_t use_fp8, const
     if (d_x == nullptr || d_recv_x == nullptr || (use_fp8 && d_recv_scales == nullptr)) return EP_ERR_INVALID_ARG;
     if (!aligned(d_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_recv_scales, 4)) return EP_ERR_INVALID_ARG;
     return enqueue_dispatch(ctx, handle, d_x, token_begin, token_end, use_fp8 != 0, d_recv_x, d_recv_scales,
-                            nullptr, (cudaStream_t)stream);
+                            nullptr, false, (cudaStream_t)stream);
 }
 
 ep_status ep_combine_range(ep_ctx *ctx, const void *d_y, const float *d_topk_weights, const ep_handle *handle,
@@ -566,7 +568,8 @@ ep_status ep_round_trip(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
     if (chunk_tokens < EP_CHUNK_AUTO) return EP_ERR_INVALID_ARG;
     if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
-    if (d_topk_idx != nullptr || tokens_per_rank == 0) {
+    const bool fresh = d_topk_idx != nullptr || tokens_per_rank == 0;
+    if (fresh) {
         const ep_status s = enqueue_layout(ctx, d_topk_idx, tokens_per_rank, nullptr, nullptr, nullptr,
                                            /*want_ranges=*/false, handle, st);
         if (s != EP_OK) return s;
@@ -576,7 +579,8 @@ ep_status ep_round_trip(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
     if (chunk <= 0 || chunk > N) chunk = N;
     for (int64_t g0 = 0; g0 < N; g0 += chunk) {
         const int64_t g1 = g0 + chunk < N ? g0 + chunk : N;
-        ep_status s = enqueue_dispatch(ctx, handle, d_x, g0, g1, use_fp8 != 0, d_recv_x, d_recv_scales, nullptr, st);
+        ep_status s = enqueue_dispatch(ctx, handle, d_x, g0, g1, use_fp8 != 0, d_recv_x, d_recv_scales, nullptr,
+                                       fresh && g0 == 0, st);
         if (s == EP_OK && (use_fp8 || d_y != d_recv_x))
             s = enqueue_identity(ctx, handle, use_fp8 != 0, d_recv_x, d_recv_scales, d_y, g0, g1, st);
         if (s == EP_OK) s = enqueue_combine(ctx, handle, d_y, d_topk_weights, g0, g1, d_out, st);

@@ -62,6 +62,8 @@ struct DispatchParams {
     int32_t *count_dst;
     int32_t E;
     int32_t row_sms;           // SMs for the row kernel (H % 512 == 0), 0 = use the warp-item kernel
+    int32_t prestage;          // row kernel: tokens per CTA cast before waiting for the slots (>= 1;
+                               // more than one pays when a layout kernel runs just before)
 };
 
 cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks,
