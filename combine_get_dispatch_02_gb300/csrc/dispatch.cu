@@ -115,8 +115,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const DispatchParams
 // ---------------------------------------------------------------- row kernel
 // One CTA per token at a time (H/16 threads, 16 channels each): the row is
 // loaded once, cast once (FP8) and laid out in shared memory, then one
-// thread issues K bulk asynchronous copies (cp.async.bulk) of the whole row
-// (and of its scale row) to the K receive rows.  Each destination row is
+// lane per top-k entry issues a bulk asynchronous copy (cp.async.bulk) of the
+// whole row (and of its scale row) to its receive row.  Each destination row is
 // written as one contiguous transfer by the copy engine instead of 512-byte
 // pieces from many warps.  NB row buffers form a ring, so the casts of the
 // next tokens overlap the copies of earlier ones; the next token's row is
@@ -190,21 +190,21 @@ __device__ __forceinline__ void put_row(uint8_t *row, int t, int H, uint4 ca, ui
     }
 }
 
-// Warp 0: the K copies of one row buffer (lane k < K holds slot k), as one
-// bulk group.
+// Warp 0: the K copies of one row buffer.  Lane k < K holds slot k and
+// issues that copy (and its scale row) itself, as its own bulk group, so
+// the K copies are issued in parallel; every lane k < K commits one group
+// per row (empty for a masked entry) and waits for its own groups.
 template <bool FP8>
 __device__ __forceinline__ void send_row(const DispatchParams &p, int32_t my_slot, const uint8_t *row, int lane) {
     const int H = p.H;
     const int payload = FP8 ? H : 2 * H;
-#pragma unroll 1
-    for (int k = 0; k < p.K; ++k) {
-        const int32_t s = __shfl_sync(0xFFFFFFFFu, my_slot, k);
-        if (lane == 0 && s >= 0) {
-            bulk_store(static_cast<uint8_t *>(p.recv) + (int64_t)s * payload, smem_addr(row), payload);
-            if constexpr (FP8) bulk_store(p.recv_scales + (int64_t)s * (H / 128), smem_addr(row + H), H / 32);
+    if (lane < p.K) {
+        if (my_slot >= 0) {
+            bulk_store(static_cast<uint8_t *>(p.recv) + (int64_t)my_slot * payload, smem_addr(row), payload);
+            if constexpr (FP8) bulk_store(p.recv_scales + (int64_t)my_slot * (H / 128), smem_addr(row + H), H / 32);
         }
+        bulk_commit();
     }
-    if (lane == 0) bulk_commit();
 }
 
 template <bool FP8, int NB>
@@ -270,8 +270,9 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
         uint4 q = make_uint4(0, 0, 0, 0);
         float scale = 0.0f;
         if constexpr (FP8) cast16(ca, cb, q, scale);
-        // this buffer was last filled NB tokens ago: its copies must have read it
-        if (t == 0) bulk_wait_read<NB - 1>();
+        // this buffer was last filled NB tokens ago: its copies (one group
+        // per lane k < K and token) must have read it
+        if (t < K) bulk_wait_read<NB - 1>();
         __syncthreads();
         put_row<FP8>(row, t, H, ca, cb, q, scale);
         fence_proxy_async_smem();
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
         if (t < 32) send_row<FP8>(p, my_slot, row, lane);
         g = gn;
     }
-    if (t == 0) bulk_wait_all();  // copies read shared memory until they finish
+    if (t < K) bulk_wait_all();  // copies read shared memory until they finish
 }
 
 bool row_kernel_fits(int H) { return H % 512 == 0 && H / 16 <= 1024; }
