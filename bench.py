@@ -57,6 +57,8 @@ def _args():
                     help="time the sweep grid (one JSON line per point) instead of the bench step")
     ap.add_argument("--sweep-filter", default="", help="only sweep points whose name contains this")
     ap.add_argument("--sweep-reps", type=int, default=10)
+    ap.add_argument("--split-reps", type=int, default=50,
+                    help="reps of each split (send / receive-hook) call (0: skip)")
     ap.add_argument("--round-trip-reps", type=int, default=50,
                     help="reps per chunk size of the dispatch -> identity expert -> combine round trip (0: skip)")
     return ap.parse_args()
@@ -450,6 +452,43 @@ def run_ours(args):
         }
         del y_rt
 
+    # split dispatch / combine: the send halves and the receive hooks (copy
+    # engine) on several SM budgets
+    split = None
+    if args.split_reps > 0 and not args.rank and (not w.use_fp8 or H % 512 == 0):
+        reps = args.split_reps
+        fp8 = w.use_fp8
+        if fp8:
+            send_x = torch.empty(N, H, dtype=torch.float8_e4m3fn, device="cuda")
+            send_sc = torch.empty(N, H // 128, dtype=torch.float32, device="cuda")
+        else:
+            send_x, send_sc = x, None
+        send_y = torch.empty(N * K, H, dtype=torch.bfloat16, device="cuda")
+        T = w.tokens_per_rank
+        send_us = timed(lambda: ep.ep_dispatch_send(ctx, x, idx, T, fp8, h.raw, send_x, send_sc, stream), reps)
+        row_b = H * (1 if fp8 else 2) + (H // 32 if fp8 else 0)
+        recv_bytes = N * row_b + M * row_b + N * K * 4
+        csend_bytes = 2 * M * H * 2 + N * K * 4
+        budgets = [b for b in (8, 16, 32, 76) if b < torch.cuda.get_device_properties(dev).multi_processor_count] + [0]
+        recv_us, csend_us = {}, {}
+        for b in budgets:
+            recv_us[str(b)] = timed(lambda: ep.ep_dispatch_recv(ctx, h.raw, fp8, send_x, send_sc, recv, scales, None,
+                                                                b, stream), reps)[0]
+            csend_us[str(b)] = timed(lambda: ep.ep_combine_send(ctx, h.raw, y, send_y, b, stream), reps)[0]
+        crecv_us = timed(lambda: ep.ep_combine_recv(ctx, h.raw, send_y, wts, out, stream), reps)
+        gbs = lambda nbytes, us: nbytes / us / 1e3
+        split = {
+            "dispatch_send_median_us": send_us[0],
+            "dispatch_recv_hook_median_us_by_sms": recv_us,
+            "dispatch_recv_hook_gbs_by_sms": {k: gbs(recv_bytes, v) for k, v in recv_us.items()},
+            "combine_send_median_us_by_sms": csend_us,
+            "combine_send_gbs_by_sms": {k: gbs(csend_bytes, v) for k, v in csend_us.items()},
+            "combine_recv_hook_median_us": crecv_us[0],
+            "note": "sms 0 = all SMs; dispatch_send includes the layout; the hooks' copy kernels only issue "
+                    "cp.async.bulk copies",
+        }
+        del send_y
+
     # HBM copy bandwidth of this GPU through torch (context for the fractions)
     cbuf = torch.empty(2 << 30, dtype=torch.uint8, device="cuda")
     cdst = torch.empty_like(cbuf)
@@ -467,7 +506,7 @@ def run_ours(args):
             torch.distributed.destroy_process_group()
         return
     _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
-            e2e, clk, graph_us, copy_gbs, round_trip)
+            e2e, clk, graph_us, copy_gbs, round_trip, split)
     if ws > 1:
         torch.distributed.destroy_process_group()
 
@@ -549,7 +588,7 @@ def _e2e(args, w, d, x, idx, wts, out, enqueue, stream):
 
 
 def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
-            e2e, clk, graph_us=None, copy_gbs=None, round_trip=None):
+            e2e, clk, graph_us=None, copy_gbs=None, round_trip=None, split=None):
     peak, peak_kind = _peaks()
     disp_bytes, disp_kernel_bytes, comb_bytes = _algorithmic_bytes(w, M)
     comb_avg_s = statistics.mean(comb_ms) / 1e3
@@ -588,6 +627,7 @@ def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, la
                               "algorithmic_bytes": disp_kernel_bytes},
         "e2e": e2e,
         "round_trip": round_trip,
+        "split": split,
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
         "host_cores": os.cpu_count(),

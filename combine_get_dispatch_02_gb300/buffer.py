@@ -80,7 +80,8 @@ class Buffer:
     dispatch / combine kernels use (0 = all)."""
 
     def __init__(self, num_ranks: int, num_max_dispatch_tokens_per_rank: int, hidden: int,
-                 num_experts: int, num_topk: int, low_latency_mode: bool = True, max_sms: int = 0):
+                 num_experts: int, num_topk: int, low_latency_mode: bool = True, max_sms: int = 0,
+                 num_hook_sms: int = 0):
         self.num_ranks = num_ranks
         self.max_tokens_per_rank = num_max_dispatch_tokens_per_rank
         self.hidden = hidden
@@ -92,6 +93,8 @@ class Buffer:
                                   max_sms)
         self._ctx = ep.ep_create(self.cfg)
         self.rows = ep.ep_recv_rows(self.cfg)
+        self.num_hook_sms = num_hook_sms   # SMs of the receive hooks' copy kernels (0: max_sms / all)
+        self._send = {}                    # send / staging buffers of the split calls, made on first use
 
     def __del__(self):
         ctx = getattr(self, "_ctx", None)
@@ -177,12 +180,32 @@ class Buffer:
         ep.ep_get_dispatch_layout(self._ctx, topk_idx, T, ntr, nte, itr, handle.raw)
         return ntr, nte, itr, handle
 
+    def _send_buffers(self, key: str, use_fp8: bool):
+        """Send buffer of a split dispatch ([R*Tmax, H] + scales) or staging
+        buffer of a split combine ([R*Tmax*K, H] bf16), kept for reuse."""
+        k = (key, use_fp8)
+        if k not in self._send:
+            dev = torch.device("cuda", torch.cuda.current_device())
+            n = self.num_ranks * self.max_tokens_per_rank
+            if key == "dispatch":
+                x = torch.empty(n, self.hidden, dtype=torch.float8_e4m3fn if use_fp8 else torch.bfloat16, device=dev)
+                sc = torch.empty(n, self.hidden // 128, dtype=torch.float32, device=dev) if use_fp8 else None
+                self._send[k] = (x, sc)
+            else:
+                self._send[k] = (torch.empty(n * self.topk, self.hidden, dtype=torch.bfloat16, device=dev), None)
+        return self._send[k]
+
     def low_latency_dispatch(self, hidden_states: torch.Tensor, topk_idx: torch.Tensor | None,
                              num_max_dispatch_tokens_per_rank: int, num_experts: int,
                              use_fp8: bool = True, handle: Handle | None = None,
-                             out=None, recv_count: torch.Tensor | None = None):
+                             out=None, recv_count: torch.Tensor | None = None,
+                             return_recv_hook: bool = False):
         """Returns ((recv_x, recv_scales) if use_fp8 else recv_x, recv_count, handle).
-        topk_idx=None reuses the layout cached in ``handle``."""
+        topk_idx=None reuses the layout cached in ``handle``.  With
+        return_recv_hook=True only the send half runs now and a fourth value,
+        ``hook``, is returned: calling it enqueues the receive (copy-engine
+        copies on ``num_hook_sms`` SMs); the receive buffers and counts hold
+        their values once the hook's work has run."""
         if num_max_dispatch_tokens_per_rank != self.max_tokens_per_rank or num_experts != self.num_experts:
             raise ValueError("num_max_dispatch_tokens_per_rank / num_experts differ from the Buffer's")
         T = hidden_states.numel() // (self.num_ranks * self.hidden)
@@ -196,17 +219,30 @@ class Buffer:
         recv_x, recv_scales = out if out is not None else self.alloc_recv(use_fp8)
         if recv_count is None:
             recv_count = torch.empty(self.num_experts, dtype=torch.int32, device=hidden_states.device)
+        if return_recv_hook:
+            send_x, send_sc = (hidden_states, None) if not use_fp8 else self._send_buffers("dispatch", True)
+            ep.ep_dispatch_send(self._ctx, hidden_states, topk_idx, T, use_fp8, handle.raw, send_x, send_sc)
+            sc = recv_scales if use_fp8 else None
+            hook_sms = self.num_hook_sms
+
+            def hook(stream=None):
+                ep.ep_dispatch_recv(self._ctx, handle.raw, use_fp8, send_x, send_sc, recv_x, sc, recv_count,
+                                    hook_sms, stream)
+            return ((recv_x, recv_scales) if use_fp8 else recv_x), recv_count, handle, hook
         ep.ep_dispatch(self._ctx, hidden_states, topk_idx, T, use_fp8, handle.raw,
                        recv_x, recv_scales if use_fp8 else None, recv_count)
         return ((recv_x, recv_scales) if use_fp8 else recv_x), recv_count, handle
 
     def low_latency_combine(self, hidden_states: torch.Tensor, topk_idx: torch.Tensor | None,
                             topk_weights: torch.Tensor | None, handle: Handle, num_experts: int,
-                            out: torch.Tensor | None = None) -> torch.Tensor:
+                            out: torch.Tensor | None = None, return_recv_hook: bool = False):
         """Weighted top-k reduce of expert outputs ``hidden_states`` [rows, H]
         bf16 (receive layout of ``handle``) back to [R*T, H] bf16 tokens.
         ``topk_idx`` is accepted for call compatibility; the handle's slots
-        decide which rows are read.  topk_weights=None means all ones."""
+        decide which rows are read.  topk_weights=None means all ones.  With
+        return_recv_hook=True the expert outputs are sent back now (copy
+        engine) and (out, hook) is returned: calling hook enqueues the
+        reduce."""
         if num_experts != self.num_experts:
             raise ValueError("num_experts differs from the Buffer's")
         info = handle.info()
@@ -215,6 +251,13 @@ class Buffer:
         N = info.num_tokens
         if out is None:
             out = torch.empty(N, self.hidden, dtype=torch.bfloat16, device=hidden_states.device)
+        if return_recv_hook:
+            send_y, _ = self._send_buffers("combine", False)
+            ep.ep_combine_send(self._ctx, handle.raw, hidden_states, send_y, self.num_hook_sms)
+
+            def hook(stream=None):
+                ep.ep_combine_recv(self._ctx, handle.raw, send_y, topk_weights, out, stream)
+            return out, hook
         ep.ep_combine(self._ctx, hidden_states, topk_weights, handle.raw, out)
         return out
 

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
         float w_all = 1.0f;
         if (lane < K) {
             s_all = p.slot[g * K + lane];
+            if (p.token_major && s_all >= 0) s_all = (int32_t)(g * K + lane);
             if (p.weights != nullptr) w_all = p.weights[g * K + lane];
         }
         const uint32_t valid = __ballot_sync(0xFFFFFFFFu, s_all >= 0);

@@ -36,6 +36,13 @@ __device__ __forceinline__ uint32_t cast_pair(float a, float b) {
     return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
+// Receive row of entry (g, lane), or -1 for none (lanes >= K).  Without a
+// slot array token g goes to row g (K == 1).
+__device__ __forceinline__ int32_t slot_of(const DispatchParams &p, int64_t g, int lane) {
+    if (lane >= p.K) return -1;
+    return p.slot != nullptr ? p.slot[g * p.K + lane] : (int32_t)g;
+}
+
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads) dispatch_kernel(const DispatchParams p) {
     const int lane = threadIdx.x & 31;
@@ -95,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const DispatchParams
             pdl_wait();
             waited = true;
         }
-        const int32_t my_slot = lane < K ? p.slot[g * K + lane] : -1;
+        const int32_t my_slot = slot_of(p, g, lane);
         for (int k = 0; k < K; ++k) {
             const int32_t s = __shfl_sync(0xFFFFFFFFu, my_slot, k);
             if (s < 0 || !act0) continue;
@@ -248,7 +255,7 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
         int32_t my_slot[NB];  // all staged tokens' slots in flight at once
 #pragma unroll
         for (int j = 0; j < NB; ++j)
-            my_slot[j] = (j < pre && lane < K) ? p.slot[((int64_t)blockIdx.x + (int64_t)j * G) * K + lane] : -1;
+            my_slot[j] = j < pre ? slot_of(p, (int64_t)blockIdx.x + (int64_t)j * G, lane) : -1;
 #pragma unroll
         for (int j = 0; j < NB; ++j)
             if (j < pre) send_row<FP8>(p, my_slot[j], row_smem + j * rowb, lane);
@@ -256,7 +263,7 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
 
     // 2. The remaining tokens through the ring (one bulk group per token);
     // each token's slots are loaded one token ahead.
-    int32_t slot_next = (t < K && g < p.N) ? p.slot[g * K + t] : -1;
+    int32_t slot_next = g < p.N ? slot_of(p, g, t) : -1;
     for (int it = pre; g < p.N; ++it) {
         uint8_t *row = row_smem + (it % NB) * rowb;
         const uint4 ca = a, cb = b;
@@ -266,7 +273,7 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
             b = ld_nc_na_v4(x + gn * H + t * 16 + 8);
         }
         const int32_t my_slot = slot_next;
-        if (t < K && gn < p.N) slot_next = p.slot[gn * K + t];
+        if (gn < p.N) slot_next = slot_of(p, gn, t);
         uint4 q = make_uint4(0, 0, 0, 0);
         float scale = 0.0f;
         if constexpr (FP8) cast16(ca, cb, q, scale);

@@ -143,15 +143,15 @@ int64_t rank_rows_of(const ep_config *c) {
 // The dispatch kernel over tokens [g0, g1) of the handle's layout (g1 > g0).
 ep_status enqueue_dispatch(ep_ctx *ctx, const ep_handle *h, const void *x, int64_t g0, int64_t g1, bool fp8,
                            void *recv, float *recv_scales, int32_t *count_dst, bool behind_layout,
-                           cudaStream_t st) {
+                           cudaStream_t st, bool identity_rows = false) {
     const ep_config &c = ctx->cfg;
     ep::DispatchParams p;
     p.x = static_cast<const uint16_t *>(x) + g0 * c.hidden;
-    p.slot = h->slot + g0 * c.topk;
+    p.slot = identity_rows ? nullptr : h->slot + g0 * c.topk;
     p.recv = recv;
     p.recv_scales = recv_scales;
     p.N = g1 - g0;
-    p.K = c.topk;
+    p.K = identity_rows ? 1 : c.topk;
     p.H = c.hidden;
     p.count_src = h->tokens_per_expert;
     p.count_dst = count_dst;
@@ -187,7 +187,7 @@ ep_status enqueue_identity(ep_ctx *ctx, const ep_handle *h, bool fp8, const void
 
 // The combine kernel over tokens [g0, g1) (g1 > g0).
 ep_status enqueue_combine(ep_ctx *ctx, const ep_handle *h, const void *y, const float *w, int64_t g0, int64_t g1,
-                          void *out, cudaStream_t st) {
+                          void *out, cudaStream_t st, bool token_major = false) {
     const ep_config &c = ctx->cfg;
     ep::CombineParams p;
     p.y = y;
@@ -198,6 +198,7 @@ ep_status enqueue_combine(ep_ctx *ctx, const ep_handle *h, const void *y, const 
     p.K = c.topk;
     p.H = c.hidden;
     p.max_valid = h->rank_mode ? (c.topk < c.num_ranks ? c.topk : c.num_ranks) : c.topk;
+    p.token_major = token_major ? 1 : 0;
     const int bps = h->rank_mode ? ctx->combine_bps_rank : ctx->combine_bps;
     if (ep::launch_combine(p, grid_cap(ctx, bps), /*pdl=*/true, st) != cudaSuccess) {
         cudaGetLastError();
@@ -217,6 +218,24 @@ int32_t auto_chunk(const ep_ctx *ctx, bool fp8, bool rank_mode) {
     int64_t chunk = ctx->l2_bytes * 7 / 10 / per_token / 64 * 64;
     if (chunk < 64) chunk = 64;
     return chunk > INT32_MAX ? INT32_MAX : (int32_t)chunk;
+}
+
+// SMs of a copy-engine (row mover) launch: num_sms if positive, else the
+// context's limit.
+int mover_sms(const ep_ctx *ctx, int32_t num_sms) {
+    int sms = ctx->num_sms;
+    if (ctx->cfg.max_sms > 0 && ctx->cfg.max_sms < sms) sms = ctx->cfg.max_sms;
+    if (num_sms > 0 && num_sms < sms) sms = num_sms;
+    return sms;
+}
+
+ep_status enqueue_move(ep::MoveParams &p, int sms, cudaStream_t st) {
+    const cudaError_t e = ep::launch_move(p, sms, /*pdl=*/true, st);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return e == cudaErrorInvalidConfiguration ? EP_ERR_UNSUPPORTED : EP_ERR_CUDA;
+    }
+    return EP_OK;
 }
 
 // Checks shared by the calls that run on a handle's cached layout over a
@@ -244,6 +263,7 @@ const char *ep_status_str(int32_t s) {
         case EP_ERR_BAD_EXPERT: return "expert id outside [-1, num_experts)";
         case EP_ERR_CAPACITY: return "padded expert buffer overflow";
         case EP_ERR_NO_LAYOUT: return "handle holds no layout for these sizes";
+        case EP_ERR_TIMEOUT: return "a bounded wait on the device gave up";
         default: return "unknown status";
     }
 }
@@ -302,6 +322,7 @@ ep_status ep_create(const ep_config *cfg, ep_ctx **out) {
     ctx->identity_bps_bf16 = ep::identity_blocks_per_sm(false);
     ctx->identity_bps_fp8 = ep::identity_blocks_per_sm(true);
     ep::dispatch_init();
+    ep::move_init();
     if (cudaMalloc(&ctx->d_status, sizeof(uint32_t)) != cudaSuccess) {
         cudaGetLastError();
         free(ctx);
@@ -463,7 +484,7 @@ ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, i
     const int64_t N = (int64_t)c.num_ranks * tokens_per_rank;
     if (N > 0 && (d_x == nullptr || d_recv_x == nullptr || (use_fp8 && d_recv_scales == nullptr)))
         return EP_ERR_INVALID_ARG;
-    if (!aligned(d_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_recv_scales, 4) ||
+    if (!aligned(d_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_recv_scales, 16) ||
         !aligned(d_recv_count, 4) || !aligned(d_topk_idx, 8))
         return EP_ERR_INVALID_ARG;
     if (d_topk_idx == nullptr && tokens_per_rank > 0 && handle->tokens_per_rank != tokens_per_rank)
@@ -516,7 +537,7 @@ ep_status ep_dispatch_range(ep_ctx *ctx, const void *d_x, int32_t use_fp8, const
     if (use_fp8 && ctx->cfg.hidden % 128 != 0) return EP_ERR_UNSUPPORTED;
     if (token_end == token_begin) return EP_OK;
     if (d_x == nullptr || d_recv_x == nullptr || (use_fp8 && d_recv_scales == nullptr)) return EP_ERR_INVALID_ARG;
-    if (!aligned(d_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_recv_scales, 4)) return EP_ERR_INVALID_ARG;
+    if (!aligned(d_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_recv_scales, 16)) return EP_ERR_INVALID_ARG;
     return enqueue_dispatch(ctx, handle, d_x, token_begin, token_end, use_fp8 != 0, d_recv_x, d_recv_scales,
                             nullptr, false, (cudaStream_t)stream);
 }
@@ -542,7 +563,7 @@ ep_status ep_expert_identity(ep_ctx *ctx, const ep_handle *handle, int32_t use_f
     if (use_fp8 && ctx->cfg.hidden % 128 != 0) return EP_ERR_UNSUPPORTED;
     if (token_end == token_begin || (!use_fp8 && d_y == d_recv_x)) return EP_OK;
     if (d_recv_x == nullptr || d_y == nullptr || (use_fp8 && d_recv_scales == nullptr)) return EP_ERR_INVALID_ARG;
-    if (!aligned(d_recv_x, 16) || !aligned(d_y, 16) || !aligned(d_recv_scales, 4)) return EP_ERR_INVALID_ARG;
+    if (!aligned(d_recv_x, 16) || !aligned(d_y, 16) || !aligned(d_recv_scales, 16)) return EP_ERR_INVALID_ARG;
     return enqueue_identity(ctx, handle, use_fp8 != 0, d_recv_x, d_recv_scales, d_y, token_begin, token_end,
                             (cudaStream_t)stream);
 }
@@ -560,7 +581,7 @@ ep_status ep_round_trip(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
     if (N > 0 && (d_x == nullptr || d_recv_x == nullptr || d_y == nullptr || d_out == nullptr ||
                   (use_fp8 && d_recv_scales == nullptr)))
         return EP_ERR_INVALID_ARG;
-    if (!aligned(d_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_recv_scales, 4) || !aligned(d_y, 16) ||
+    if (!aligned(d_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_recv_scales, 16) || !aligned(d_y, 16) ||
         !aligned(d_out, 16) || !aligned(d_topk_weights, 4) || !aligned(d_topk_idx, 8))
         return EP_ERR_INVALID_ARG;
     if (d_topk_idx == nullptr && tokens_per_rank > 0 && handle->tokens_per_rank != tokens_per_rank)
@@ -589,6 +610,124 @@ ep_status ep_round_trip(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
     return EP_OK;
 }
 
+ep_status ep_dispatch_send(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, int32_t tokens_per_rank,
+                           int32_t use_fp8, ep_handle *handle, void *d_send_x, float *d_send_scales, void *stream) {
+    NvtxRange nvtx("ep_dispatch_send");
+    if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
+    const ep_config &c = ctx->cfg;
+    if (tokens_per_rank < 0 || tokens_per_rank > c.max_tokens_per_rank) return EP_ERR_INVALID_ARG;
+    if (use_fp8 != 0 && use_fp8 != 1) return EP_ERR_INVALID_ARG;
+    if (use_fp8 && c.hidden % 512 != 0) return EP_ERR_UNSUPPORTED;
+    const int64_t N = (int64_t)c.num_ranks * tokens_per_rank;
+    if (N > 0 && (d_x == nullptr || d_send_x == nullptr || (use_fp8 && d_send_scales == nullptr)))
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(d_x, 16) || !aligned(d_send_x, 16) || !aligned(d_send_scales, 16) || !aligned(d_topk_idx, 8))
+        return EP_ERR_INVALID_ARG;
+    if (d_topk_idx == nullptr && tokens_per_rank > 0 && handle->tokens_per_rank != tokens_per_rank)
+        return EP_ERR_NO_LAYOUT;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool fresh = d_topk_idx != nullptr || tokens_per_rank == 0;
+    if (fresh) {
+        const ep_status s = enqueue_layout(ctx, d_topk_idx, tokens_per_rank, nullptr, nullptr, nullptr,
+                                           /*want_ranges=*/false, handle, st);
+        if (s != EP_OK) return s;
+    }
+    if (N == 0 || (!use_fp8 && d_send_x == d_x)) return EP_OK;  // BF16 rows are sent from x itself
+    return enqueue_dispatch(ctx, handle, d_x, 0, N, use_fp8 != 0, d_send_x, d_send_scales, nullptr, fresh, st,
+                            /*identity_rows=*/true);
+}
+
+ep_status ep_dispatch_recv(ep_ctx *ctx, const ep_handle *handle, int32_t use_fp8, const void *d_send_x,
+                           const float *d_send_scales, void *d_recv_x, float *d_recv_scales, int32_t *d_recv_count,
+                           int32_t num_sms, void *stream) {
+    NvtxRange nvtx("ep_dispatch_recv");
+    if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
+    if (handle->tokens_per_rank < 0) return EP_ERR_NO_LAYOUT;
+    const ep_config &c = ctx->cfg;
+    if (use_fp8 != 0 && use_fp8 != 1) return EP_ERR_INVALID_ARG;
+    if (use_fp8 && c.hidden % 512 != 0) return EP_ERR_UNSUPPORTED;
+    const int64_t N = (int64_t)c.num_ranks * handle->tokens_per_rank;
+    if (N > 0 && (d_send_x == nullptr || d_recv_x == nullptr ||
+                  (use_fp8 && (d_send_scales == nullptr || d_recv_scales == nullptr))))
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(d_send_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_send_scales, 16) ||
+        !aligned(d_recv_scales, 16) || !aligned(d_recv_count, 4))
+        return EP_ERR_INVALID_ARG;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (N == 0) {
+        if (d_recv_count != nullptr &&
+            cudaMemcpyAsync(d_recv_count, handle->tokens_per_expert, (size_t)handle->num_keys * sizeof(int32_t),
+                            cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
+            cudaGetLastError();
+            return EP_ERR_CUDA;
+        }
+        return EP_OK;
+    }
+    ep::MoveParams p;
+    p.src = static_cast<const uint8_t *>(d_send_x);
+    p.src_scales = use_fp8 ? reinterpret_cast<const uint8_t *>(d_send_scales) : nullptr;
+    p.dst = static_cast<uint8_t *>(d_recv_x);
+    p.dst_scales = use_fp8 ? reinterpret_cast<uint8_t *>(d_recv_scales) : nullptr;
+    p.slot = handle->slot;
+    p.n = N;
+    p.K = c.topk;
+    p.gather = 0;
+    p.row_bytes = use_fp8 ? c.hidden : 2 * c.hidden;
+    p.scale_bytes = use_fp8 ? c.hidden / 32 : 0;
+    p.ring = 0;
+    p.count_src = handle->tokens_per_expert;
+    p.count_dst = d_recv_count;
+    p.E = handle->num_keys;
+    p.status = ctx->d_status;
+    return enqueue_move(p, mover_sms(ctx, num_sms), st);
+}
+
+ep_status ep_combine_send(ep_ctx *ctx, const ep_handle *handle, const void *d_y, void *d_send_y, int32_t num_sms,
+                          void *stream) {
+    NvtxRange nvtx("ep_combine_send");
+    if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
+    if (handle->tokens_per_rank < 0) return EP_ERR_NO_LAYOUT;
+    const ep_config &c = ctx->cfg;
+    const int64_t N = (int64_t)c.num_ranks * handle->tokens_per_rank;
+    if (N == 0) return EP_OK;
+    if (d_y == nullptr || d_send_y == nullptr) return EP_ERR_INVALID_ARG;
+    if (!aligned(d_y, 16) || !aligned(d_send_y, 16)) return EP_ERR_INVALID_ARG;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    ep::MoveParams p;
+    p.src = static_cast<const uint8_t *>(d_y);
+    p.src_scales = nullptr;
+    p.dst = static_cast<uint8_t *>(d_send_y);
+    p.dst_scales = nullptr;
+    p.slot = handle->slot;
+    p.n = N * c.topk;
+    p.K = 1;
+    p.gather = 1;
+    p.row_bytes = 2 * c.hidden;
+    p.scale_bytes = 0;
+    p.ring = 0;
+    p.count_src = nullptr;
+    p.count_dst = nullptr;
+    p.E = 0;
+    p.status = ctx->d_status;
+    return enqueue_move(p, mover_sms(ctx, num_sms), (cudaStream_t)stream);
+}
+
+ep_status ep_combine_recv(ep_ctx *ctx, const ep_handle *handle, const void *d_send_y, const float *d_topk_weights,
+                          void *d_out, void *stream) {
+    NvtxRange nvtx("ep_combine_recv");
+    if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
+    if (handle->tokens_per_rank < 0) return EP_ERR_NO_LAYOUT;
+    const int64_t N = (int64_t)ctx->cfg.num_ranks * handle->tokens_per_rank;
+    if (N == 0) return EP_OK;
+    if (d_send_y == nullptr || d_out == nullptr) return EP_ERR_INVALID_ARG;
+    if (!aligned(d_send_y, 16) || !aligned(d_out, 16) || !aligned(d_topk_weights, 4)) return EP_ERR_INVALID_ARG;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    return enqueue_combine(ctx, handle, d_send_y, d_topk_weights, 0, N, d_out, (cudaStream_t)stream,
+                           /*token_major=*/true);
+}
+
 ep_status ep_round_trip_auto_chunk(const ep_ctx *ctx, int32_t use_fp8, int32_t rank_layout, int32_t *chunk_tokens) {
     if (ctx == nullptr || chunk_tokens == nullptr) return EP_ERR_INVALID_ARG;
     if (use_fp8 != 0 && use_fp8 != 1) return EP_ERR_INVALID_ARG;
@@ -608,6 +747,7 @@ ep_status ep_get_device_status(ep_ctx *ctx, void *stream) {
     }
     if (bits & ep::kStatusBadExpert) return EP_ERR_BAD_EXPERT;
     if (bits & ep::kStatusCapacity) return EP_ERR_CAPACITY;
+    if (bits & ep::kStatusTimeout) return EP_ERR_TIMEOUT;
     return EP_OK;
 }
 

@@ -10,6 +10,7 @@ namespace ep {
 // Bits of the per-context device status word.
 constexpr uint32_t kStatusBadExpert = 1u;  // topk_idx entry outside [-1, E)
 constexpr uint32_t kStatusCapacity = 2u;   // padded expert buffer offered > R*Tmax entries
+constexpr uint32_t kStatusTimeout = 4u;    // a bounded wait of a copy kernel gave up
 
 constexpr int kLayoutPadded = 0;
 constexpr int kLayoutPacked = 1;
@@ -64,6 +65,7 @@ struct DispatchParams {
     int32_t row_sms;           // SMs for the row kernel (H % 512 == 0), 0 = use the warp-item kernel
     int32_t prestage;          // row kernel: tokens per CTA cast before waiting for the slots (>= 1;
                                // more than one pays when a layout kernel runs just before)
+    // slot == nullptr: token g goes to row g (K must be 1): the send buffer of a split dispatch
 };
 
 cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks,
@@ -82,11 +84,43 @@ struct CombineParams {
     int64_t N;
     int32_t K, H;
     int32_t max_valid;         // most entries of one token that have rows (K, or min(K, R) by rank)
+    int32_t token_major;       // 1: entry (g, k) with slot >= 0 reads row g*K + k of y (a staging
+                               // buffer in token order) instead of row slot
 };
 
 cudaError_t launch_combine(const CombineParams &p, int max_blocks, bool pdl,
                            cudaStream_t stream);
 int combine_blocks_per_sm(int max_valid);
+
+// ------------------------------------------------------------------ row mover (copy engine)
+// Moves rows with bulk asynchronous copies only (global -> shared ->
+// global); the SM threads just issue them.
+//   fan-out (gather == 0): item g = source row g, copied to the rows
+//            slot[g*K + k] >= 0 of dst (the receive half of a split dispatch)
+//   gather  (gather == 1): item i = entry, row slot[i] >= 0 of src copied to
+//            row i of dst, K = 1 (the send half of a split combine)
+// Each row is row_bytes (+ scale_bytes of scales when scales are given).
+struct MoveParams {
+    const uint8_t *src;
+    const uint8_t *src_scales;  // or nullptr
+    uint8_t *dst;
+    uint8_t *dst_scales;
+    const int32_t *slot;
+    int64_t n;                  // items
+    int32_t K;
+    int32_t gather;
+    int32_t row_bytes, scale_bytes;   // multiples of 16
+    int32_t ring;               // buffers per CTA (2..8), set by launch_move
+    const int32_t *count_src;   // [E] copied to count_dst by block 0, or nullptr
+    int32_t *count_dst;
+    int32_t E;
+    uint32_t *status;
+};
+
+// Launch on `sms` SMs (as many CTAs per SM as shared memory allows).
+cudaError_t launch_move(MoveParams p, int sms, bool pdl, cudaStream_t stream);
+// One-time set-up with the device current (shared memory limits).
+void move_init();
 
 // ------------------------------------------------------------------ identity expert
 struct IdentityParams {

@@ -75,7 +75,7 @@ extern "C" ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, 
     if (N > 0 && (d_x == nullptr || d_topk_idx == nullptr || d_recv_x == nullptr ||
                   (use_fp8 && d_recv_scales == nullptr)))
         return EP_ERR_INVALID_ARG;
-    if (!aligned(d_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_recv_scales, 4) || !aligned(d_recv_count, 4) ||
+    if (!aligned(d_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_recv_scales, 16) || !aligned(d_recv_count, 4) ||
         !aligned(d_topk_idx, 8))
         return EP_ERR_INVALID_ARG;
 

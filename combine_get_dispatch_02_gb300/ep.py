@@ -24,6 +24,7 @@ EP_ERR_CUDA = 4
 EP_ERR_BAD_EXPERT = 5
 EP_ERR_CAPACITY = 6
 EP_ERR_NO_LAYOUT = 7
+EP_ERR_TIMEOUT = 8
 
 EP_LAYOUT_PADDED = 0
 EP_LAYOUT_PACKED = 1
@@ -36,7 +37,7 @@ ENTRY_POINTS = (
     "ep_handle_get_info", "ep_get_dispatch_layout", "ep_dispatch", "ep_combine",
     "ep_get_device_status", "ep_dispatch_noalloc", "ep_get_rank_layout", "ep_rank_recv_rows",
     "ep_dispatch_range", "ep_combine_range", "ep_expert_identity", "ep_round_trip",
-    "ep_round_trip_auto_chunk",
+    "ep_round_trip_auto_chunk", "ep_dispatch_send", "ep_dispatch_recv", "ep_combine_send", "ep_combine_recv",
 )
 
 EP_CHUNK_AUTO = -1
@@ -100,6 +101,10 @@ def lib() -> ctypes.CDLL:
             "ep_expert_identity": (I32, [P, P, I32, P, P, P, I64, I64, P]),
             "ep_round_trip": (I32, [P, P, P, I32, P, I32, P, P, P, P, P, I32, P]),
             "ep_round_trip_auto_chunk": (I32, [P, I32, I32, ctypes.POINTER(I32)]),
+            "ep_dispatch_send": (I32, [P, P, P, I32, I32, P, P, P, P]),
+            "ep_dispatch_recv": (I32, [P, P, I32, P, P, P, P, P, I32, P]),
+            "ep_combine_send": (I32, [P, P, P, P, I32, P]),
+            "ep_combine_recv": (I32, [P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -272,6 +277,36 @@ def ep_round_trip_auto_chunk(ctx, use_fp8: bool, rank_layout: bool = False) -> i
     _check(lib().ep_round_trip_auto_chunk(ctx, int(bool(use_fp8)), int(bool(rank_layout)), ctypes.byref(n)),
            "ep_round_trip_auto_chunk")
     return n.value
+
+
+def ep_dispatch_send(ctx, x: torch.Tensor, topk_idx: torch.Tensor | None, tokens_per_rank: int, use_fp8: bool,
+                     handle, send_x: torch.Tensor, send_scales: torch.Tensor | None, stream=None) -> None:
+    _check(lib().ep_dispatch_send(
+        ctx, _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int64, "topk_idx"), int(tokens_per_rank),
+        int(bool(use_fp8)), handle, _ptr(send_x, None, "send_x"), _ptr(send_scales, torch.float32, "send_scales"),
+        _stream(stream)), "ep_dispatch_send")
+
+
+def ep_dispatch_recv(ctx, handle, use_fp8: bool, send_x: torch.Tensor, send_scales: torch.Tensor | None,
+                     recv_x: torch.Tensor, recv_scales: torch.Tensor | None, recv_count: torch.Tensor | None,
+                     num_sms: int = 0, stream=None) -> None:
+    _check(lib().ep_dispatch_recv(
+        ctx, handle, int(bool(use_fp8)), _ptr(send_x, None, "send_x"),
+        _ptr(send_scales, torch.float32, "send_scales"), _ptr(recv_x, None, "recv_x"),
+        _ptr(recv_scales, torch.float32, "recv_scales"), _ptr(recv_count, torch.int32, "recv_count"),
+        int(num_sms), _stream(stream)), "ep_dispatch_recv")
+
+
+def ep_combine_send(ctx, handle, y: torch.Tensor, send_y: torch.Tensor, num_sms: int = 0, stream=None) -> None:
+    _check(lib().ep_combine_send(ctx, handle, _ptr(y, torch.bfloat16, "y"), _ptr(send_y, torch.bfloat16, "send_y"),
+                                 int(num_sms), _stream(stream)), "ep_combine_send")
+
+
+def ep_combine_recv(ctx, handle, send_y: torch.Tensor, topk_weights: torch.Tensor | None, out: torch.Tensor,
+                    stream=None) -> None:
+    _check(lib().ep_combine_recv(ctx, handle, _ptr(send_y, torch.bfloat16, "send_y"),
+                                 _ptr(topk_weights, torch.float32, "topk_weights"),
+                                 _ptr(out, torch.bfloat16, "out"), _stream(stream)), "ep_combine_recv")
 
 
 def ep_get_device_status(ctx, stream=None) -> int:

@@ -78,7 +78,8 @@ typedef enum ep_status {
     EP_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
     EP_ERR_BAD_EXPERT = 5,   /* device: a topk_idx entry was outside [-1, E) */
     EP_ERR_CAPACITY = 6,     /* device: padded layout, an expert was offered more than R*Tmax entries */
-    EP_ERR_NO_LAYOUT = 7     /* the handle holds no layout yet, or one for other sizes */
+    EP_ERR_NO_LAYOUT = 7,    /* the handle holds no layout yet, or one for other sizes */
+    EP_ERR_TIMEOUT = 8       /* device: a bounded wait of a copy kernel gave up (about 1 s) */
 } ep_status;
 
 typedef enum ep_layout {
@@ -218,7 +219,7 @@ ep_status ep_rank_recv_rows(const ep_config *cfg, int64_t *rows);
  *   tokens_per_rank T (must match the handle when reusing)
  *   use_fp8        0 = BF16 payload, 1 = FP8 payload + scales
  *   d_recv_x       device [rows, H] bf16 or uint8 (16-byte aligned)
- *   d_recv_scales  device fp32 [rows, H/128] when use_fp8, else ignored
+ *   d_recv_scales  device fp32 [rows, H/128] (16-byte aligned) when use_fp8, else ignored
  *   d_recv_count   device int32 [E] or NULL: rows each expert received
  * Rows that receive nothing are not written. */
 ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
@@ -276,6 +277,45 @@ ep_status ep_expert_identity(ep_ctx *ctx, const ep_handle *handle, int32_t use_f
                              const void *d_recv_x, const float *d_recv_scales, void *d_y,
                              int64_t token_begin, int64_t token_end, void *stream);
 
+/* Split dispatch and combine: the send half returns and a later "hook" call
+ * finishes the receive (the hook-based communication-computation overlap of
+ * "如何突破MoE通信瓶颈：DeepEP跨节点优化技术终极指南", section 技术解析,
+ * 通信-计算重叠技术: the receive occupies no SM; the DeepTech announcement of
+ * DeepEP, 010bt.com, says the same).  On one GPU the wire is HBM and the
+ * engine that moves rows without SM work is the bulk-copy (TMA) unit: the
+ * receive hooks and the combine send are copy kernels whose threads only
+ * issue cp.async.bulk copies, so they can run on num_sms SMs (<= 0: the
+ * context's limit) while other work uses the rest.  The results are
+ * identical, bit for bit, to ep_dispatch / ep_combine; the price is that
+ * every row crosses HBM once more (through a send buffer).
+ *
+ * ep_dispatch_send: the layout (when d_topk_idx is given, as in ep_dispatch),
+ *   then each token cast once (FP8) into its row of the send buffer:
+ *     d_send_x       device [R*T, H] e4m3 (FP8) or bf16, 16-byte aligned; for
+ *                    BF16 it may be d_x itself (then only the layout runs)
+ *     d_send_scales  device fp32 [R*T, H/128], 16-byte aligned (FP8)
+ * ep_dispatch_recv (the hook): every sent row copied to its receive rows,
+ *   receive buffers and d_recv_count as ep_dispatch writes them.
+ * ep_combine_send: the expert output of every received row copied back to the
+ *   token-major buffer d_send_y [R*T*K, H] bf16 (row g*K + k for entry
+ *   (g, k); rows of masked entries are not written).
+ * ep_combine_recv (the hook): ep_combine over d_send_y (row g*K + k instead of
+ *   the receive row), into d_out [R*T, H].
+ * FP8 needs H % 512 == 0 here (EP_ERR_UNSUPPORTED otherwise).  A copy kernel's
+ * waits for its row loads are bounded; if one gives up, the kernel stops and
+ * ep_get_device_status reports EP_ERR_TIMEOUT. */
+ep_status ep_dispatch_send(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
+                           int32_t tokens_per_rank, int32_t use_fp8, ep_handle *handle,
+                           void *d_send_x, float *d_send_scales, void *stream);
+ep_status ep_dispatch_recv(ep_ctx *ctx, const ep_handle *handle, int32_t use_fp8,
+                           const void *d_send_x, const float *d_send_scales, void *d_recv_x,
+                           float *d_recv_scales, int32_t *d_recv_count, int32_t num_sms,
+                           void *stream);
+ep_status ep_combine_send(ep_ctx *ctx, const ep_handle *handle, const void *d_y, void *d_send_y,
+                          int32_t num_sms, void *stream);
+ep_status ep_combine_recv(ep_ctx *ctx, const ep_handle *handle, const void *d_send_y,
+                          const float *d_topk_weights, void *d_out, void *stream);
+
 /* chunk_tokens of ep_round_trip that asks for the automatic chunk size. */
 #define EP_CHUNK_AUTO (-1)
 
@@ -327,7 +367,7 @@ ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, const int64
                               float *d_recv_scales, int32_t *d_recv_count, void *stream);
 
 /* Synchronise `stream`, read and clear the context's device status word.
- * Returns EP_OK, EP_ERR_BAD_EXPERT, EP_ERR_CAPACITY or EP_ERR_CUDA. */
+ * Returns EP_OK, EP_ERR_BAD_EXPERT, EP_ERR_CAPACITY, EP_ERR_TIMEOUT or EP_ERR_CUDA. */
 ep_status ep_get_device_status(ep_ctx *ctx, void *stream);
 
 #ifdef __cplusplus
