@@ -57,6 +57,8 @@ def _args():
                     help="time the sweep grid (one JSON line per point) instead of the bench step")
     ap.add_argument("--sweep-filter", default="", help="only sweep points whose name contains this")
     ap.add_argument("--sweep-reps", type=int, default=10)
+    ap.add_argument("--autotune", action="store_true",
+                    help="time the launch-shape candidates on the workload first (ep_autotune) and use the best")
     ap.add_argument("--split-reps", type=int, default=50,
                     help="reps of each split (send / receive-hook) call (0: skip)")
     ap.add_argument("--round-trip-reps", type=int, default=50,
@@ -342,6 +344,18 @@ def run_ours(args):
         flush_w.fill_(1)
         torch.sum(flush_r, dim=0, keepdim=True, out=flush_sink)
 
+    tuning = None
+    if args.autotune and args.rank:
+        raise SystemExit("--autotune times the expert-major layout; run it without --rank")
+    if args.autotune:
+        # the bench's BF16 round trip writes the expert output in place
+        y_tune = recv if not w.use_fp8 else torch.empty(buf.rows, H, dtype=torch.bfloat16, device="cuda")
+        t = ep.ep_autotune(ctx, x, idx, w.tokens_per_rank, wts, w.use_fp8, recv, scales, y_tune, out, reps=20)
+        tuning = t.as_dict()
+        tuning["candidates_us"] = [f"{k}={v}: {us:.1f}" for k, v, us in ep.ep_get_autotune_log(ctx)]
+        del y_tune
+        torch.cuda.empty_cache()
+
     def step():
         return enqueue(x, idx, wts, out, stream)
 
@@ -506,7 +520,7 @@ def run_ours(args):
             torch.distributed.destroy_process_group()
         return
     _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
-            e2e, clk, graph_us, copy_gbs, round_trip, split)
+            e2e, clk, graph_us, copy_gbs, round_trip, split, tuning)
     if ws > 1:
         torch.distributed.destroy_process_group()
 
@@ -588,7 +602,7 @@ def _e2e(args, w, d, x, idx, wts, out, enqueue, stream):
 
 
 def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
-            e2e, clk, graph_us=None, copy_gbs=None, round_trip=None, split=None):
+            e2e, clk, graph_us=None, copy_gbs=None, round_trip=None, split=None, tuning=None):
     peak, peak_kind = _peaks()
     disp_bytes, disp_kernel_bytes, comb_bytes = _algorithmic_bytes(w, M)
     comb_avg_s = statistics.mean(comb_ms) / 1e3
@@ -606,6 +620,7 @@ def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, la
         "data": "synthetic",
         "config": {"workload": _workload_desc(w) + ("; rank-deduplicated transport" if args.rank else ""),
                    "tokens_per_step": N, "rows_received": M,
+                   "launch_shapes": tuning if tuning is not None else "built-in rules",
                    "l2": "flushed between steps (write of 2x L2, then read of 2x L2; outside the timed events)",
                    "parallelism": f"{ws} replica(s), one per GPU" if ws > 1 else "1 GPU, 32 virtual EP ranks"},
         "us_per_call": {

@@ -152,8 +152,10 @@ int occupancy() {
 }
 }  // namespace
 
-int combine_blocks_per_sm(int max_valid) {
-    switch (cpi_for(max_valid)) {
+int combine_cpi_rule(int max_valid) { return cpi_for(max_valid); }
+
+int combine_blocks_per_sm(int max_valid, int cpi) {
+    switch (cpi > 0 ? cpi : cpi_for(max_valid)) {
         case 4: return occupancy<4>();
         case 2: return occupancy<2>();
         default: return occupancy<1>();
@@ -161,7 +163,7 @@ int combine_blocks_per_sm(int max_valid) {
 }
 
 cudaError_t launch_combine(const CombineParams &p, int max_blocks, bool pdl, cudaStream_t stream) {
-    const int cpi = cpi_for(p.max_valid);
+    const int cpi = p.cpi > 0 ? p.cpi : cpi_for(p.max_valid);
     const int nch = (p.H + kChunk * cpi - 1) / (kChunk * cpi);
     const int64_t warps = p.N * nch;
     int64_t blocks = (warps + (kThreads / 32) - 1) / (kThreads / 32);

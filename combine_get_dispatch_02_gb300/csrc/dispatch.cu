@@ -306,6 +306,8 @@ int blocks_per_sm() {
 
 }  // namespace
 
+int dispatch_row_ctas_rule(int H) { return row_blocks_per_sm(H); }
+
 int dispatch_blocks_per_sm(bool fp8) { return fp8 ? blocks_per_sm<true>() : blocks_per_sm<false>(); }
 
 namespace {
@@ -369,7 +371,7 @@ cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks, b
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     if (row_kernel_fits(p.H) && p.row_sms > 0) {
-        const int bps = row_blocks_per_sm(p.H);
+        const int bps = p.row_bps > 0 ? p.row_bps : row_blocks_per_sm(p.H);
         int64_t blocks = (int64_t)p.row_sms * bps;
         if (blocks > p.N) blocks = p.N;
         if (blocks < 1) blocks = 1;

@@ -7,6 +7,9 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
+#include <vector>
+
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 
@@ -28,6 +31,10 @@ struct ep_ctx {
     int identity_bps_bf16;
     int identity_bps_fp8;
     int64_t l2_bytes;
+    ep_tuning tune;        // launch shapes set by ep_set_tuning / ep_autotune (0: built-in rules)
+    int combine_bps_tuned; // resident combine CTAs per SM for tune.combine_chunks
+    ep_tune_record tune_log[16];  // the candidates the last ep_autotune timed
+    int tune_log_n;
 };
 
 struct ep_handle {
@@ -158,6 +165,7 @@ ep_status enqueue_dispatch(ep_ctx *ctx, const ep_handle *h, const void *x, int64
     p.E = h->num_keys;
     p.row_sms = (c.max_sms > 0 && c.max_sms < ctx->num_sms) ? c.max_sms : ctx->num_sms;
     p.prestage = behind_layout ? 8 : 1;
+    p.row_bps = ctx->tune.dispatch_ctas_per_sm;
     const int cap = grid_cap(ctx, fp8 ? ctx->dispatch_bps_fp8 : ctx->dispatch_bps_bf16);
     if (ep::launch_dispatch(p, fp8, cap, /*pdl=*/true, st) != cudaSuccess) {
         cudaGetLastError();
@@ -199,7 +207,8 @@ ep_status enqueue_combine(ep_ctx *ctx, const ep_handle *h, const void *y, const 
     p.H = c.hidden;
     p.max_valid = h->rank_mode ? (c.topk < c.num_ranks ? c.topk : c.num_ranks) : c.topk;
     p.token_major = token_major ? 1 : 0;
-    const int bps = h->rank_mode ? ctx->combine_bps_rank : ctx->combine_bps;
+    p.cpi = ctx->tune.combine_chunks;
+    const int bps = p.cpi > 0 ? ctx->combine_bps_tuned : (h->rank_mode ? ctx->combine_bps_rank : ctx->combine_bps);
     if (ep::launch_combine(p, grid_cap(ctx, bps), /*pdl=*/true, st) != cudaSuccess) {
         cudaGetLastError();
         return EP_ERR_CUDA;
@@ -211,6 +220,7 @@ ep_status enqueue_combine(ep_ctx *ctx, const ep_handle *h, const void *y, const 
 // (payload, FP8 scales, and the bf16 expert output unless it is written in
 // place) fill about 70% of L2, a multiple of 64 tokens and at least 64.
 int32_t auto_chunk(const ep_ctx *ctx, bool fp8, bool rank_mode) {
+    if (ctx->tune.round_trip_chunk > 0) return ctx->tune.round_trip_chunk;
     const ep_config &c = ctx->cfg;
     const int64_t rows_per_token = rank_mode ? (c.topk < c.num_ranks ? c.topk : c.num_ranks) : c.topk;
     const int64_t row_bytes = fp8 ? (int64_t)c.hidden + c.hidden / 32 + 2 * (int64_t)c.hidden : 2 * (int64_t)c.hidden;
@@ -238,6 +248,22 @@ ep_status enqueue_move(ep::MoveParams &p, int sms, cudaStream_t st) {
     return EP_OK;
 }
 
+// Dispatch -> identity expert -> combine over chunks of `chunk` tokens (<= 0
+// or > N: one chunk) on the handle's layout.
+ep_status enqueue_round_trip(ep_ctx *ctx, const ep_handle *h, const void *x, const float *w, bool fp8, void *recv,
+                             float *recv_scales, void *y, void *out, int64_t N, int64_t chunk, bool fresh,
+                             cudaStream_t st) {
+    if (chunk <= 0 || chunk > N) chunk = N;
+    for (int64_t g0 = 0; g0 < N; g0 += chunk) {
+        const int64_t g1 = g0 + chunk < N ? g0 + chunk : N;
+        ep_status s = enqueue_dispatch(ctx, h, x, g0, g1, fp8, recv, recv_scales, nullptr, fresh && g0 == 0, st);
+        if (s == EP_OK && (fp8 || y != recv)) s = enqueue_identity(ctx, h, fp8, recv, recv_scales, y, g0, g1, st);
+        if (s == EP_OK) s = enqueue_combine(ctx, h, y, w, g0, g1, out, st);
+        if (s != EP_OK) return s;
+    }
+    return EP_OK;
+}
+
 // Checks shared by the calls that run on a handle's cached layout over a
 // token range: 0 <= g0 <= g1 <= R*T of the layout.
 ep_status check_range(const ep_ctx *ctx, const ep_handle *h, int64_t g0, int64_t g1) {
@@ -246,6 +272,53 @@ ep_status check_range(const ep_ctx *ctx, const ep_handle *h, int64_t g0, int64_t
     const int64_t N = (int64_t)ctx->cfg.num_ranks * h->tokens_per_rank;
     if (g0 < 0 || g1 < g0 || g1 > N) return EP_ERR_INVALID_ARG;
     if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    return EP_OK;
+}
+
+}  // namespace
+
+namespace {
+
+void log_candidate(ep_ctx *ctx, int32_t knob, int32_t value, float us) {
+    if (ctx->tune_log_n < 16) ctx->tune_log[ctx->tune_log_n++] = ep_tune_record{knob, value, us};
+}
+
+// Median CUDA-event time (µs) of `reps` runs of enqueue().  Before each,
+// the first half of `flush` (each half twice the L2 size) is written and the
+// second half read: the run starts as it would behind kernels that wrote a
+// lot (the write-back of their lines is still draining), the usual place of
+// a dispatch or combine in a step — measured, the condition that separates
+// the launch shapes (a read-only flush hides differences the step shows).
+template <typename F>
+ep_status median_us(F enqueue, int reps, void *flush, size_t flush_bytes, int sms, cudaStream_t st, float *us) {
+    std::vector<cudaEvent_t> ev(2 * (size_t)reps, nullptr);
+    ep_status s = EP_OK;
+    for (auto &e : ev)
+        if (cudaEventCreate(&e) != cudaSuccess) s = EP_ERR_CUDA;
+    for (int r = 0; s == EP_OK && r < reps; ++r) {
+        if (flush != nullptr && (cudaMemsetAsync(flush, r & 0xFF, flush_bytes / 2, st) != cudaSuccess ||
+                                 ep::launch_l2_evict(static_cast<uint8_t *>(flush) + flush_bytes / 2, flush_bytes / 2,
+                                                     sms, st) != cudaSuccess))
+            s = EP_ERR_CUDA;
+        if (s == EP_OK && cudaEventRecord(ev[2 * r], st) != cudaSuccess) s = EP_ERR_CUDA;
+        if (s == EP_OK) s = enqueue();
+        if (s == EP_OK && cudaEventRecord(ev[2 * r + 1], st) != cudaSuccess) s = EP_ERR_CUDA;
+    }
+    if (cudaStreamSynchronize(st) != cudaSuccess && s == EP_OK) s = EP_ERR_CUDA;
+    std::vector<float> t;
+    for (int r = 0; s == EP_OK && r < reps; ++r) {
+        float ms = 0.0f;
+        if (cudaEventElapsedTime(&ms, ev[2 * r], ev[2 * r + 1]) != cudaSuccess) s = EP_ERR_CUDA;
+        t.push_back(ms * 1000.0f);
+    }
+    for (auto &e : ev)
+        if (e != nullptr) cudaEventDestroy(e);
+    if (s != EP_OK) {
+        cudaGetLastError();
+        return s;
+    }
+    std::sort(t.begin(), t.end());
+    *us = t[t.size() / 2];
     return EP_OK;
 }
 
@@ -595,19 +668,10 @@ ep_status ep_round_trip(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
                                            /*want_ranges=*/false, handle, st);
         if (s != EP_OK) return s;
     }
-    int64_t chunk = chunk_tokens == EP_CHUNK_AUTO ? auto_chunk(ctx, use_fp8 != 0, handle->rank_mode != 0)
-                                                  : chunk_tokens;
-    if (chunk <= 0 || chunk > N) chunk = N;
-    for (int64_t g0 = 0; g0 < N; g0 += chunk) {
-        const int64_t g1 = g0 + chunk < N ? g0 + chunk : N;
-        ep_status s = enqueue_dispatch(ctx, handle, d_x, g0, g1, use_fp8 != 0, d_recv_x, d_recv_scales, nullptr,
-                                       fresh && g0 == 0, st);
-        if (s == EP_OK && (use_fp8 || d_y != d_recv_x))
-            s = enqueue_identity(ctx, handle, use_fp8 != 0, d_recv_x, d_recv_scales, d_y, g0, g1, st);
-        if (s == EP_OK) s = enqueue_combine(ctx, handle, d_y, d_topk_weights, g0, g1, d_out, st);
-        if (s != EP_OK) return s;
-    }
-    return EP_OK;
+    const int64_t chunk = chunk_tokens == EP_CHUNK_AUTO ? auto_chunk(ctx, use_fp8 != 0, handle->rank_mode != 0)
+                                                        : chunk_tokens;
+    return enqueue_round_trip(ctx, handle, d_x, d_topk_weights, use_fp8 != 0, d_recv_x, d_recv_scales, d_y, d_out,
+                              N, chunk, fresh, st);
 }
 
 ep_status ep_dispatch_send(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, int32_t tokens_per_rank,
@@ -732,6 +796,164 @@ ep_status ep_round_trip_auto_chunk(const ep_ctx *ctx, int32_t use_fp8, int32_t r
     if (ctx == nullptr || chunk_tokens == nullptr) return EP_ERR_INVALID_ARG;
     if (use_fp8 != 0 && use_fp8 != 1) return EP_ERR_INVALID_ARG;
     *chunk_tokens = auto_chunk(ctx, use_fp8 != 0, rank_layout != 0);
+    return EP_OK;
+}
+
+ep_status ep_get_tuning(const ep_ctx *ctx, ep_tuning *out) {
+    if (ctx == nullptr || out == nullptr) return EP_ERR_INVALID_ARG;
+    *out = ctx->tune;
+    return EP_OK;
+}
+
+ep_status ep_set_tuning(ep_ctx *ctx, const ep_tuning *t) {
+    if (ctx == nullptr || t == nullptr) return EP_ERR_INVALID_ARG;
+    if (t->dispatch_ctas_per_sm < 0 || t->dispatch_ctas_per_sm > 16) return EP_ERR_INVALID_ARG;
+    if (t->combine_chunks != 0 && t->combine_chunks != 1 && t->combine_chunks != 2 && t->combine_chunks != 4)
+        return EP_ERR_INVALID_ARG;
+    if (t->round_trip_chunk < 0) return EP_ERR_INVALID_ARG;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    ctx->tune = *t;
+    ctx->combine_bps_tuned = t->combine_chunks > 0 ? ep::combine_blocks_per_sm(0, t->combine_chunks) : 0;
+    return EP_OK;
+}
+
+
+ep_status ep_autotune(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, int32_t tokens_per_rank,
+                      const float *d_topk_weights, int32_t use_fp8, void *d_recv_x, float *d_recv_scales, void *d_y,
+                      void *d_out, int32_t reps, ep_tuning *out, void *stream) {
+    if (ctx == nullptr || out == nullptr) return EP_ERR_INVALID_ARG;
+    const ep_config &c = ctx->cfg;
+    if (tokens_per_rank < 1 || tokens_per_rank > c.max_tokens_per_rank || reps < 1 || reps > 1000)
+        return EP_ERR_INVALID_ARG;
+    if (use_fp8 != 0 && use_fp8 != 1) return EP_ERR_INVALID_ARG;
+    if (use_fp8 && c.hidden % 128 != 0) return EP_ERR_UNSUPPORTED;
+    if (d_x == nullptr || d_topk_idx == nullptr || d_recv_x == nullptr || d_y == nullptr || d_out == nullptr ||
+        (use_fp8 && d_recv_scales == nullptr))
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(d_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_recv_scales, 16) || !aligned(d_y, 16) ||
+        !aligned(d_out, 16) || !aligned(d_topk_weights, 4) || !aligned(d_topk_idx, 8))
+        return EP_ERR_INVALID_ARG;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool fp8 = use_fp8 != 0;
+    const int64_t N = (int64_t)c.num_ranks * tokens_per_rank;
+
+    ep_handle *h = nullptr;
+    ep_status s = ep_handle_create(ctx, &h);
+    if (s != EP_OK) return s;
+    void *flush = nullptr;
+    const size_t flush_bytes = (size_t)(ctx->l2_bytes > 0 ? 4 * ctx->l2_bytes : 0);
+    if (flush_bytes > 0 && (cudaMalloc(&flush, flush_bytes) != cudaSuccess ||
+                            cudaMemsetAsync(flush, 0, flush_bytes, st) != cudaSuccess)) {
+        cudaGetLastError();
+        if (flush != nullptr) cudaFree(flush);
+        flush = nullptr;  // tune without evicting L2
+    }
+    const int sms = ctx->num_sms;
+    const ep_tuning saved = ctx->tune;
+    ep_tuning best = saved;
+    ctx->tune_log_n = 0;
+    s = enqueue_layout(ctx, d_topk_idx, tokens_per_rank, nullptr, nullptr, nullptr, false, h, st);
+
+    // Each knob: the built-in rule's choice is timed first and kept unless
+    // another candidate is at least kMargin faster (the medians of runs that
+    // start behind a large write differ by a few per cent from run to run).
+    constexpr float kMargin = 0.97f;
+
+    // dispatch: row-kernel CTAs per SM, timed as the common call runs it
+    // (layout kernel, then the dispatch behind it)
+    if (s == EP_OK && c.hidden % 512 == 0 && c.hidden <= 16384) {
+        const int rule = ep::dispatch_row_ctas_rule(c.hidden);
+        std::vector<int> cands = {rule};
+        for (int b = 1; b <= 4; ++b)
+            if (b != rule) cands.push_back(b);
+        float best_us = 0.0f;
+        for (size_t j = 0; s == EP_OK && j < cands.size(); ++j) {
+            ep_tuning t = best;
+            t.dispatch_ctas_per_sm = cands[j];
+            s = ep_set_tuning(ctx, &t);
+            float us = 0.0f;
+            if (s == EP_OK)
+                s = median_us(
+                    [&] {
+                        ep_status e = enqueue_layout(ctx, d_topk_idx, tokens_per_rank, nullptr, nullptr, nullptr,
+                                                     false, h, st);
+                        return e != EP_OK ? e
+                                          : enqueue_dispatch(ctx, h, d_x, 0, N, fp8, d_recv_x, d_recv_scales,
+                                                             nullptr, true, st);
+                    },
+                    reps, flush, flush_bytes, sms, st, &us);
+            if (s == EP_OK) log_candidate(ctx, EP_TUNE_DISPATCH_CTAS_PER_SM, cands[j], us);
+            if (s == EP_OK && (j == 0 || us < kMargin * best_us)) {
+                best_us = us;
+                best.dispatch_ctas_per_sm = cands[j];
+            }
+        }
+    }
+    // combine: chunks per work item
+    if (s == EP_OK) {
+        const int rule = ep::combine_cpi_rule(c.topk);
+        std::vector<int> cands = {rule};
+        for (int v : {1, 2, 4})
+            if (v != rule) cands.push_back(v);
+        float best_us = 0.0f;
+        for (size_t j = 0; s == EP_OK && j < cands.size(); ++j) {
+            ep_tuning t = best;
+            t.combine_chunks = cands[j];
+            s = ep_set_tuning(ctx, &t);
+            float us = 0.0f;
+            if (s == EP_OK)
+                s = median_us([&] { return enqueue_combine(ctx, h, d_y, d_topk_weights, 0, N, d_out, st); }, reps,
+                              flush, flush_bytes, sms, st, &us);
+            if (s == EP_OK) log_candidate(ctx, EP_TUNE_COMBINE_CHUNKS, cands[j], us);
+            if (s == EP_OK && (j == 0 || us < kMargin * best_us)) {
+                best_us = us;
+                best.combine_chunks = cands[j];
+            }
+        }
+    }
+    // round trip: the L2 rule's chunk, half and twice that, and one chunk
+    if (s == EP_OK) {
+        ep_tuning t = best;
+        t.round_trip_chunk = 0;
+        s = ep_set_tuning(ctx, &t);
+        const int64_t rule = auto_chunk(ctx, fp8, false);
+        std::vector<int64_t> cands = {rule >= N ? N : rule, N, rule / 2 / 64 * 64, 2 * rule};
+        float best_us = 0.0f;
+        bool first = true;
+        std::vector<int64_t> done;
+        for (int64_t ch : cands) {
+            if (s != EP_OK) break;
+            if (ch < 64 && ch != N) continue;
+            if (ch > N) ch = N;
+            if (std::find(done.begin(), done.end(), ch) != done.end()) continue;
+            done.push_back(ch);
+            float us = 0.0f;
+            s = median_us([&] { return enqueue_round_trip(ctx, h, d_x, d_topk_weights, fp8, d_recv_x, d_recv_scales,
+                                                          d_y, d_out, N, ch, false, st); },
+                          reps, flush, flush_bytes, sms, st, &us);
+            const int32_t value = ch >= N ? INT32_MAX : (int32_t)ch;  // INT32_MAX: one chunk
+            if (s == EP_OK) log_candidate(ctx, EP_TUNE_ROUND_TRIP_CHUNK, value, us);
+            if (s == EP_OK && (first || us < kMargin * best_us)) {
+                best_us = us;
+                best.round_trip_chunk = value;
+                first = false;
+            }
+        }
+    }
+    if (flush != nullptr) cudaFree(flush);
+    ep_handle_destroy(h);
+    if (s == EP_OK) s = ep_set_tuning(ctx, &best);
+    else ep_set_tuning(ctx, &saved);
+    if (s == EP_OK) *out = best;
+    return s;
+}
+
+ep_status ep_get_autotune_log(const ep_ctx *ctx, ep_tune_record *records, int32_t capacity, int32_t *count) {
+    if (ctx == nullptr || count == nullptr || capacity < 0 || (capacity > 0 && records == nullptr))
+        return EP_ERR_INVALID_ARG;
+    *count = ctx->tune_log_n;
+    for (int i = 0; i < ctx->tune_log_n && i < capacity; ++i) records[i] = ctx->tune_log[i];
     return EP_OK;
 }
 

@@ -66,10 +66,13 @@ struct DispatchParams {
     int32_t prestage;          // row kernel: tokens per CTA cast before waiting for the slots (>= 1;
                                // more than one pays when a layout kernel runs just before)
     // slot == nullptr: token g goes to row g (K must be 1): the send buffer of a split dispatch
+    int32_t row_bps;           // row kernel CTAs per SM, 0 = the built-in rule (from H)
 };
 
 cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks,
                             bool pdl, cudaStream_t stream);
+// The row dispatch kernel's CTAs per SM by the built-in rule (from H).
+int dispatch_row_ctas_rule(int H);
 // Resident blocks per SM of the warp-item dispatch kernel (for grid sizing).
 int dispatch_blocks_per_sm(bool fp8);
 // One-time kernel attribute set-up (call with the device current).
@@ -86,11 +89,17 @@ struct CombineParams {
     int32_t max_valid;         // most entries of one token that have rows (K, or min(K, R) by rank)
     int32_t token_major;       // 1: entry (g, k) with slot >= 0 reads row g*K + k of y (a staging
                                // buffer in token order) instead of row slot
+    int32_t cpi;               // 256-channel chunks per work item (1, 2, 4), 0 = the rule (from max_valid)
 };
 
 cudaError_t launch_combine(const CombineParams &p, int max_blocks, bool pdl,
                            cudaStream_t stream);
-int combine_blocks_per_sm(int max_valid);
+// The combine's chunks per work item by the built-in rule (from the most
+// entries a token can have rows for).
+int combine_cpi_rule(int max_valid);
+// Resident combine CTAs per SM for the chunks per item that max_valid (or a
+// nonzero cpi) selects.
+int combine_blocks_per_sm(int max_valid, int cpi = 0);
 
 // ------------------------------------------------------------------ row mover (copy engine)
 // Moves rows with bulk asynchronous copies only (global -> shared ->
@@ -121,6 +130,8 @@ struct MoveParams {
 cudaError_t launch_move(MoveParams p, int sms, bool pdl, cudaStream_t stream);
 // One-time set-up with the device current (shared memory limits).
 void move_init();
+// Read `bytes` (> L2) of `buf`: afterwards L2 holds only clean lines.
+cudaError_t launch_l2_evict(const void *buf, size_t bytes, int sms, cudaStream_t stream);
 
 // ------------------------------------------------------------------ identity expert
 struct IdentityParams {

@@ -163,6 +163,7 @@ extern "C" ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, 
     if (c.max_sms > 0 && c.max_sms < sms) sms = c.max_sms;
     dp.row_sms = sms;
     dp.prestage = 8;  // behind the layout kernel
+    dp.row_bps = 0;
     const int cap = sms * (use_fp8 ? s.bps_fp8 : s.bps_bf16);
     if (ep::launch_dispatch(dp, use_fp8 != 0, cap, /*pdl=*/true, st) != cudaSuccess) {
         cudaGetLastError();

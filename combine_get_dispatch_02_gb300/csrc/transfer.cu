@@ -159,7 +159,27 @@ __global__ void __launch_bounds__(32) move_rows_kernel(const MoveParams p) {
     if (lane < p.K) bulk_wait_all();
 }
 
+// Reads a buffer larger than L2 so that the next kernel starts with an L2
+// holding only clean lines of this buffer (the dirty lines of earlier kernels
+// are written back here).  The loaded words feed a comparison that is never
+// true in practice, so the loads are kept.
+__global__ void l2_evict_kernel(const uint4 *p, int64_t n, uint32_t *sink) {
+    uint32_t acc = 0;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 v = __ldcg(p + i);
+        acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+    if (acc == 0x9E3779B9u && sink != nullptr) *sink = acc;
+}
+
 }  // namespace
+
+cudaError_t launch_l2_evict(const void *buf, size_t bytes, int sms, cudaStream_t stream) {
+    const int64_t n = (int64_t)(bytes / 16);
+    if (n <= 0) return cudaSuccess;
+    l2_evict_kernel<<<sms * 4, 512, 0, stream>>>(static_cast<const uint4 *>(buf), n, nullptr);
+    return cudaGetLastError();
+}
 
 namespace {
 int g_smem_sm = 0, g_smem_blk = 0, g_reserved = 0;

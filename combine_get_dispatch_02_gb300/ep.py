@@ -38,7 +38,10 @@ ENTRY_POINTS = (
     "ep_get_device_status", "ep_dispatch_noalloc", "ep_get_rank_layout", "ep_rank_recv_rows",
     "ep_dispatch_range", "ep_combine_range", "ep_expert_identity", "ep_round_trip",
     "ep_round_trip_auto_chunk", "ep_dispatch_send", "ep_dispatch_recv", "ep_combine_send", "ep_combine_recv",
+    "ep_get_tuning", "ep_set_tuning", "ep_autotune", "ep_get_autotune_log",
 )
+
+TUNE_KNOBS = {0: "dispatch_ctas_per_sm", 1: "combine_chunks", 2: "round_trip_chunk"}
 
 EP_CHUNK_AUTO = -1
 
@@ -54,6 +57,18 @@ class ep_config(ctypes.Structure):
                 ("hidden", ctypes.c_int32), ("num_experts", ctypes.c_int32),
                 ("topk", ctypes.c_int32), ("layout", ctypes.c_int32),
                 ("max_sms", ctypes.c_int32)]
+
+
+class ep_tuning(ctypes.Structure):
+    _fields_ = [("dispatch_ctas_per_sm", ctypes.c_int32), ("combine_chunks", ctypes.c_int32),
+                ("round_trip_chunk", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class ep_tune_record(ctypes.Structure):
+    _fields_ = [("knob", ctypes.c_int32), ("value", ctypes.c_int32), ("median_us", ctypes.c_float)]
 
 
 class ep_handle_info(ctypes.Structure):
@@ -105,6 +120,10 @@ def lib() -> ctypes.CDLL:
             "ep_dispatch_recv": (I32, [P, P, I32, P, P, P, P, P, I32, P]),
             "ep_combine_send": (I32, [P, P, P, P, I32, P]),
             "ep_combine_recv": (I32, [P, P, P, P, P, P]),
+            "ep_get_tuning": (I32, [P, ctypes.POINTER(ep_tuning)]),
+            "ep_set_tuning": (I32, [P, ctypes.POINTER(ep_tuning)]),
+            "ep_autotune": (I32, [P, P, P, I32, P, I32, P, P, P, P, I32, ctypes.POINTER(ep_tuning), P]),
+            "ep_get_autotune_log": (I32, [P, ctypes.POINTER(ep_tune_record), I32, ctypes.POINTER(I32)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -307,6 +326,37 @@ def ep_combine_recv(ctx, handle, send_y: torch.Tensor, topk_weights: torch.Tenso
     _check(lib().ep_combine_recv(ctx, handle, _ptr(send_y, torch.bfloat16, "send_y"),
                                  _ptr(topk_weights, torch.float32, "topk_weights"),
                                  _ptr(out, torch.bfloat16, "out"), _stream(stream)), "ep_combine_recv")
+
+
+def ep_get_tuning(ctx) -> ep_tuning:
+    t = ep_tuning()
+    _check(lib().ep_get_tuning(ctx, ctypes.byref(t)), "ep_get_tuning")
+    return t
+
+
+def ep_set_tuning(ctx, tuning: ep_tuning) -> None:
+    _check(lib().ep_set_tuning(ctx, ctypes.byref(tuning)), "ep_set_tuning")
+
+
+def ep_autotune(ctx, x: torch.Tensor, topk_idx: torch.Tensor, tokens_per_rank: int,
+                topk_weights: torch.Tensor | None, use_fp8: bool, recv_x: torch.Tensor,
+                recv_scales: torch.Tensor | None, y: torch.Tensor, out: torch.Tensor, reps: int = 20,
+                stream=None) -> ep_tuning:
+    t = ep_tuning()
+    _check(lib().ep_autotune(
+        ctx, _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int64, "topk_idx"), int(tokens_per_rank),
+        _ptr(topk_weights, torch.float32, "topk_weights"), int(bool(use_fp8)), _ptr(recv_x, None, "recv_x"),
+        _ptr(recv_scales, torch.float32, "recv_scales"), _ptr(y, torch.bfloat16, "y"),
+        _ptr(out, torch.bfloat16, "out"), int(reps), ctypes.byref(t), _stream(stream)), "ep_autotune")
+    return t
+
+
+def ep_get_autotune_log(ctx) -> list[tuple[str, int, float]]:
+    """(knob, value, median µs) of each candidate the last ep_autotune timed."""
+    recs = (ep_tune_record * 16)()
+    n = ctypes.c_int32(0)
+    _check(lib().ep_get_autotune_log(ctx, recs, 16, ctypes.byref(n)), "ep_get_autotune_log")
+    return [(TUNE_KNOBS.get(r.knob, str(r.knob)), r.value, r.median_us) for r in recs[:min(n.value, 16)]]
 
 
 def ep_get_device_status(ctx, stream=None) -> int:

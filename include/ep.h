@@ -338,9 +338,68 @@ ep_status ep_round_trip(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
  * rows (payload, FP8 scales and the bf16 expert output: K rows per token,
  * min(K, R) for a rank-deduplicated layout when rank_layout != 0) take
  * about 70% of the device's L2, rounded down to a multiple of 64 tokens, at
- * least 64.  Host only. */
+ * least 64 — or the tuned size when ep_set_tuning / ep_autotune set one.
+ * Host only. */
 ep_status ep_round_trip_auto_chunk(const ep_ctx *ctx, int32_t use_fp8, int32_t rank_layout,
                                    int32_t *chunk_tokens);
+
+/* Launch shapes of a context ("run all tests and use the best auto-tuned
+ * setting", DeepTech announcement of DeepEP, 010bt.com; SM control of
+ * "如何突破MoE通信瓶颈：DeepEP跨节点优化技术终极指南", section 功能4).  None of
+ * them changes a result bit: they only decide how the work is spread.
+ *   dispatch_ctas_per_sm  CTAs per SM of the row dispatch kernel (1..16),
+ *                         0 = the built-in rule (from H)
+ *   combine_chunks        256-channel chunks per combine work item (1, 2 or 4),
+ *                         0 = the built-in rule (from the entries per token)
+ *   round_trip_chunk      tokens per chunk that EP_CHUNK_AUTO stands for in
+ *                         ep_round_trip; 0 = the L2 rule; >= R*T (INT32_MAX
+ *                         from ep_autotune) = one chunk */
+typedef struct ep_tuning {
+    int32_t dispatch_ctas_per_sm;
+    int32_t combine_chunks;
+    int32_t round_trip_chunk;
+} ep_tuning;
+
+/* One candidate ep_autotune timed: knob (EP_TUNE_*), its value, median µs. */
+typedef enum ep_tune_knob {
+    EP_TUNE_DISPATCH_CTAS_PER_SM = 0,  /* timed as layout + dispatch */
+    EP_TUNE_COMBINE_CHUNKS = 1,
+    EP_TUNE_ROUND_TRIP_CHUNK = 2       /* INT32_MAX: one chunk */
+} ep_tune_knob;
+typedef struct ep_tune_record {
+    int32_t knob;
+    int32_t value;
+    float median_us;
+} ep_tune_record;
+
+ep_status ep_get_tuning(const ep_ctx *ctx, ep_tuning *out);
+/* Values out of range: EP_ERR_INVALID_ARG and the tuning is unchanged. */
+ep_status ep_set_tuning(ep_ctx *ctx, const ep_tuning *tuning);
+
+/* Time each launch shape above on the caller's own inputs and keep the
+ * fastest in the context (also written to *out; the built-in rule's choice is
+ * timed first and kept unless another candidate is at least 3% faster):
+ * layout + dispatch with the
+ * row dispatch at 1..4 CTAs per SM (H % 512 == 0, H <= 16384), the combine
+ * with 1, 2 and 4 chunks per item, then the round trip in one chunk and in
+ * chunks of half, one and two times the L2 rule.  Each candidate: the median
+ * of `reps` (1..1000) runs, before each a write of twice the L2 size and a
+ * read of another twice the L2 size (as behind kernels that just wrote a lot).  Arguments as for ep_round_trip
+ * (d_topk_idx required, tokens_per_rank >= 1; d_y == d_recv_x tunes the BF16
+ * round trip in place); d_recv_x / d_recv_scales / d_y / d_out are
+ * overwritten.  Unlike the other calls it allocates (a handle and a 4x-L2
+ * buffer, freed before it returns) and synchronises `stream`; on error the
+ * previous tuning is kept. */
+ep_status ep_autotune(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
+                      int32_t tokens_per_rank, const float *d_topk_weights, int32_t use_fp8,
+                      void *d_recv_x, float *d_recv_scales, void *d_y, void *d_out, int32_t reps,
+                      ep_tuning *out, void *stream);
+
+/* The candidates the last ep_autotune on this context timed, in order (at
+ * most 16): *count gets their number, records[0 .. min(count, capacity))
+ * their values.  Host only. */
+ep_status ep_get_autotune_log(const ep_ctx *ctx, ep_tune_record *records, int32_t capacity,
+                              int32_t *count);
 
 /* Dispatch for callers that cannot allocate device memory (no counterpart on
  * the pages: it is this library's own addition).  Same operation and output as

@@ -1,0 +1,131 @@
+"""Launch-shape tuning: every shape gives the same bits (checked against the
+default shapes and the oracle), ep_set_tuning validates, and ep_autotune
+returns a valid tuning after which the results are unchanged."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_get_dispatch_02_gb300 import build as epbuild
+from combine_get_dispatch_02_gb300 import ep
+from combine_get_dispatch_02_gb300 import workloads as wl
+from helpers import ORACLE_LAYOUT, bf16_to_bits, bits_to_bf16, make_buffer, valid_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    epbuild.build()
+    oracle.build()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+
+
+def _run(buf, w, x, idx_d, wts_d, y, rank=False):
+    """(receive payload rows, scales, combined tokens) with the current tuning."""
+    if rank:
+        _, _, _, h = buf.get_rank_layout(idx_d)
+        recv, scales = buf.alloc_rank_recv(w.use_fp8)
+        ep.ep_dispatch(buf.ctx, x, None, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales, None)
+    else:
+        recv, scales = buf.alloc_recv(w.use_fp8)
+        _, _, h = buf.low_latency_dispatch(x, idx_d, w.max_tokens_per_rank, w.num_experts, use_fp8=w.use_fp8,
+                                           out=(recv, scales))
+    out = buf.low_latency_combine(y, None, None if rank else wts_d, h, w.num_experts)
+    assert buf.device_status() == ep.EP_OK
+    rows = torch.from_numpy(valid_rows(h.tensors()["slot"].cpu().numpy()).astype(np.int64)).cuda()
+    return (recv.view(torch.uint8)[rows].clone(), None if scales is None else scales[rows].clone(), out.clone())
+
+
+@pytest.mark.parametrize("name", ["ll", "skew_masked", "normal_rank", "tiny_bf16"])
+def test_every_launch_shape_gives_the_same_bits(name):
+    w = {"ll": wl.LL, "skew_masked": wl.SKEW.with_(tokens_per_rank=300), "tiny_bf16": wl.TINY,
+         "normal_rank": wl.NORMAL.with_(tokens_per_rank=256, max_tokens_per_rank=256, use_fp8=True)}[name]
+    rank = name == "normal_rank"
+    d = wl.generate(w)
+    idx = d["topk_idx"] if name != "skew_masked" else wl.inject_masks(d["topk_idx"], 0.1, 3)
+    buf = make_buffer(w)
+    x = bits_to_bf16(d["x_bits"].reshape(w.num_tokens, w.hidden))
+    idx_d = torch.from_numpy(idx).cuda()
+    wts_d = torch.from_numpy(d["topk_weights"].reshape(w.num_tokens, w.topk)).cuda()
+    rows = buf.rank_rows if rank else buf.rows
+    g = torch.Generator(device="cuda").manual_seed(5)
+    y = torch.randn(rows, w.hidden, device="cuda", generator=g).to(torch.bfloat16)
+    ref = _run(buf, w, x, idx_d, wts_d, y, rank)
+    if not rank:  # the default shapes against the oracle's combine
+        o = oracle.layout(idx, w.num_experts, w.max_tokens_per_rank, ORACLE_LAYOUT[w.layout])
+        sl = o["slot"]
+        m = sl.reshape(-1) >= 0
+        slot_c = np.full(sl.size, -1, np.int32)
+        slot_c[m] = np.arange(int(m.sum()), dtype=np.int32)
+        y_rows = bf16_to_bits(y[torch.from_numpy(sl.reshape(-1)[m].astype(np.int64)).cuda()])
+        assert np.array_equal(bf16_to_bits(ref[2]),
+                              oracle.combine(y_rows, slot_c.reshape(sl.shape),
+                                             d["topk_weights"].reshape(w.num_tokens, w.topk)))
+    for bps in (1, 2, 3, 4):
+        for cpi in (1, 2, 4):
+            ep.ep_set_tuning(buf.ctx, ep.ep_tuning(bps, cpi, 0))
+            got = _run(buf, w, x, idx_d, wts_d, y, rank)
+            assert torch.equal(got[0], ref[0]), (bps, cpi)
+            if ref[1] is not None:
+                assert torch.equal(got[1].view(torch.int32), ref[1].view(torch.int32)), (bps, cpi)
+            assert torch.equal(got[2].view(torch.int16), ref[2].view(torch.int16)), (bps, cpi)
+
+
+def test_set_tuning_validates():
+    buf = make_buffer(wl.TINY)
+    assert ep.ep_get_tuning(buf.ctx).as_dict() == {"dispatch_ctas_per_sm": 0, "combine_chunks": 0,
+                                                   "round_trip_chunk": 0}
+    for bad in (ep.ep_tuning(17, 0, 0), ep.ep_tuning(-1, 0, 0), ep.ep_tuning(0, 3, 0), ep.ep_tuning(0, 0, -5)):
+        with pytest.raises(ep.EPError) as e:
+            ep.ep_set_tuning(buf.ctx, bad)
+        assert e.value.status == ep.EP_ERR_INVALID_ARG
+    assert ep.ep_get_tuning(buf.ctx).as_dict()["combine_chunks"] == 0
+    ep.ep_set_tuning(buf.ctx, ep.ep_tuning(2, 4, 640))
+    assert ep.ep_get_tuning(buf.ctx).as_dict() == {"dispatch_ctas_per_sm": 2, "combine_chunks": 4,
+                                                   "round_trip_chunk": 640}
+    assert ep.ep_round_trip_auto_chunk(buf.ctx, True) == 640
+
+
+def test_autotune_then_round_trip_matches_the_oracle():
+    w = wl.LL
+    d = wl.generate(w)
+    N, K, H = w.num_tokens, w.topk, w.hidden
+    buf = make_buffer(w)
+    x_bits = d["x_bits"].reshape(N, H)
+    x = bits_to_bf16(x_bits)
+    idx_d = torch.from_numpy(d["topk_idx"]).cuda()
+    wts = d["topk_weights"].reshape(N, K).astype(np.float32)
+    wts_d = torch.from_numpy(wts).cuda()
+    recv, scales = buf.alloc_recv(True)
+    y = torch.empty(buf.rows, H, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(N, H, dtype=torch.bfloat16, device="cuda")
+    t = ep.ep_autotune(buf.ctx, x, idx_d, w.tokens_per_rank, wts_d, True, recv, scales, y, out, reps=5)
+    assert 1 <= t.dispatch_ctas_per_sm <= 4
+    assert t.combine_chunks in (1, 2, 4)
+    assert t.round_trip_chunk == 2 ** 31 - 1 or 64 <= t.round_trip_chunk <= N
+    assert ep.ep_get_tuning(buf.ctx).as_dict() == t.as_dict()
+    log = ep.ep_get_autotune_log(buf.ctx)
+    for knob in ("dispatch_ctas_per_sm", "combine_chunks", "round_trip_chunk"):
+        cands = [(v, us) for k, v, us in log if k == knob]
+        assert cands and all(us > 0 for _, us in cands)
+        # the first candidate is the built-in rule's; another is kept only when 3% faster than it
+        chosen = [us for v, us in cands if v == t.as_dict()[knob]][0]
+        assert chosen == cands[0][1] or chosen < 0.97 * cands[0][1]
+        assert chosen <= min(us for _, us in cands) / 0.97 + 1e-3
+    torch.cuda.synchronize()
+    o = oracle.layout(d["topk_idx"], w.num_experts, w.max_tokens_per_rank, ORACLE_LAYOUT[w.layout])
+    sl = o["slot"]
+    m = sl.reshape(-1) >= 0
+    slot_c = np.full(sl.size, -1, np.int32)
+    slot_c[m] = np.arange(int(m.sum()), dtype=np.int32)
+    slot_c = slot_c.reshape(N, K)
+    q, s = oracle.dispatch(x_bits, slot_c, int(m.sum()), True)
+    ref = oracle.combine(oracle.dequant_rows(q, s, slot_c), slot_c, wts)
+    res, _ = buf.round_trip(x, idx_d, wts_d, use_fp8=True, chunk_tokens=ep.EP_CHUNK_AUTO, recv=(recv, scales), y=y)
+    assert buf.device_status() == ep.EP_OK
+    assert np.array_equal(bf16_to_bits(res), ref)
