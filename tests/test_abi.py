@@ -89,3 +89,26 @@ def test_host_rejections_touch_no_device(lib):
     assert lib.ep_handle_destroy(None) == ep.EP_ERR_INVALID_ARG
     assert lib.ep_handle_create(None, ctypes.byref(out)) == ep.EP_ERR_INVALID_ARG
     assert lib.ep_handle_get_info(None, None) == ep.EP_ERR_INVALID_ARG
+
+
+def test_host_rejections_of_the_range_split_and_tuning_calls(lib):
+    """Every entry point added for the round trip, the split calls and the
+    launch-shape tuning rejects a NULL context before any CUDA call."""
+    P = ctypes.c_void_p
+    E = ep.EP_ERR_INVALID_ARG
+    assert lib.ep_dispatch_range(None, None, 0, None, 0, 0, None, None, None) == E
+    assert lib.ep_combine_range(None, None, None, None, 0, 0, None, None) == E
+    assert lib.ep_expert_identity(None, None, 0, None, None, None, 0, 0, None) == E
+    assert lib.ep_round_trip(None, None, None, 0, None, 0, None, None, None, None, None, 0, None) == E
+    n = ctypes.c_int32(0)
+    assert lib.ep_round_trip_auto_chunk(None, 0, 0, ctypes.byref(n)) == E
+    assert lib.ep_dispatch_send(None, None, None, 0, 0, None, None, None, None) == E
+    assert lib.ep_dispatch_recv(None, None, 0, None, None, None, None, None, 0, None) == E
+    assert lib.ep_combine_send(None, None, None, None, 0, None) == E
+    assert lib.ep_combine_recv(None, None, None, None, None, None) == E
+    t = ep.ep_tuning()
+    assert lib.ep_get_tuning(None, ctypes.byref(t)) == E
+    assert lib.ep_set_tuning(None, ctypes.byref(t)) == E
+    assert lib.ep_autotune(None, None, None, 1, None, 0, None, None, None, None, 1, ctypes.byref(t), None) == E
+    assert lib.ep_get_autotune_log(None, None, 0, ctypes.byref(n)) == E
+    assert lib.ep_status_str(ep.EP_ERR_TIMEOUT).decode() == "a bounded wait on the device gave up"
