@@ -126,8 +126,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const DispatchParams
 // whole row (and of its scale row) to its receive row.  Each destination row is
 // written as one contiguous transfer by the copy engine instead of 512-byte
 // pieces from many warps.  NB row buffers form a ring, so the casts of the
-// next tokens overlap the copies of earlier ones; the next token's row is
-// loaded while the current one is cast.  Launched behind the layout kernel
+// next tokens overlap the copies of earlier ones; the rows of the next two
+// tokens are being loaded while the current one is cast.  Launched behind the layout kernel
 // (programmatic dependent launch), a CTA first casts up to NB of its tokens
 // into the ring and only then waits for the slots, so most of the layout's
 // run time is spent loading and casting rows.  Needs H % 512 == 0 and
@@ -223,11 +223,16 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
     const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(p.x);
     const int64_t G = gridDim.x;
 
+    // x rows are loaded two tokens ahead: (a, b) = this token, (a2, b2) = the next
     int64_t g = blockIdx.x;
-    uint4 a = make_uint4(0, 0, 0, 0), b = a;
+    uint4 a = make_uint4(0, 0, 0, 0), b = a, a2 = a, b2 = a;
     if (g < p.N) {
         a = ld_nc_na_v4(x + g * H + t * 16);
         b = ld_nc_na_v4(x + g * H + t * 16 + 8);
+    }
+    if (g + G < p.N) {
+        a2 = ld_nc_na_v4(x + (g + G) * H + t * 16);
+        b2 = ld_nc_na_v4(x + (g + G) * H + t * 16 + 8);
     }
 
     // 1. Before the slots exist: cast up to `pre_max` tokens into the ring.
@@ -236,9 +241,11 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
     for (; pre < pre_max && g < p.N; ++pre) {
         const uint4 ca = a, cb = b;
         const int64_t gn = g + G;
-        if (gn < p.N) {
-            a = ld_nc_na_v4(x + gn * H + t * 16);
-            b = ld_nc_na_v4(x + gn * H + t * 16 + 8);
+        a = a2;
+        b = b2;
+        if (gn + G < p.N) {
+            a2 = ld_nc_na_v4(x + (gn + G) * H + t * 16);
+            b2 = ld_nc_na_v4(x + (gn + G) * H + t * 16 + 8);
         }
         uint4 q = make_uint4(0, 0, 0, 0);
         float scale = 0.0f;
@@ -268,9 +275,11 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
         uint8_t *row = row_smem + (it % NB) * rowb;
         const uint4 ca = a, cb = b;
         const int64_t gn = g + G;
-        if (gn < p.N) {
-            a = ld_nc_na_v4(x + gn * H + t * 16);
-            b = ld_nc_na_v4(x + gn * H + t * 16 + 8);
+        a = a2;
+        b = b2;
+        if (gn + G < p.N) {
+            a2 = ld_nc_na_v4(x + (gn + G) * H + t * 16);
+            b2 = ld_nc_na_v4(x + (gn + G) * H + t * 16 + 8);
         }
         const int32_t my_slot = slot_next;
         if (gn < p.N) slot_next = slot_of(p, gn, t);
