@@ -595,10 +595,20 @@ def _e2e(args, w, d, x, idx, wts, out, enqueue, stream):
 
     h2d_gbs = link_gbs(lambda: xs[0].copy_(xh, non_blocking=True), xh.numel() * 2)
     d2h_gbs = link_gbs(lambda: outh[0].copy_(outs[0], non_blocking=True), d2h)
+
+    # both directions at once (the pipelined steps need this): one copy each way
+    # per rep, on two streams
+    def both():
+        with torch.cuda.stream(s_in):
+            xs[1].copy_(xh, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            outh[1].copy_(outs[1], non_blocking=True)
+    bidir_gbs = link_gbs(both, xh.numel() * 2 + d2h)
     return {"value": N / (res[True] / 1e3) * ws, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": res[True], "ms_per_step_serial": res[False],
             "pipelining": "H2D / compute / D2H on three streams, two buffer sets",
-            "host_link_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs}}
+            "host_link_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs, "both_directions_at_once": bidir_gbs},
+            "host_link_bound_ms_per_step": (h2d + d2h) / bidir_gbs / 1e6}
 
 
 def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
