@@ -24,6 +24,8 @@ struct ep_ctx {
     uint32_t *d_status;
     int layout_cluster;
     int layout_threads;
+    int layout_cluster_many;  // shape for layouts of kLayoutManyEntries entries or more
+    int layout_threads_many;
     int dispatch_bps_bf16;
     int dispatch_bps_fp8;
     int combine_bps;       // resident combine CTAs per SM, expert layout
@@ -129,7 +131,9 @@ ep_status enqueue_layout(ep_ctx *ctx, const int64_t *topk_idx, int32_t T, int32_
     p.tokens_per_rank = tokens_per_rank;
     p.is_token_in_rank = is_token_in_rank;
     p.status = ctx->d_status;
-    const cudaError_t err = ep::launch_layout(p, ctx->layout_cluster, ctx->layout_threads, stream);
+    const bool many = p.N * p.K >= ep::kLayoutManyEntries;
+    const cudaError_t err = ep::launch_layout(p, many ? ctx->layout_cluster_many : ctx->layout_cluster,
+                                              many ? ctx->layout_threads_many : ctx->layout_threads, stream);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return err == cudaErrorInvalidConfiguration ? EP_ERR_UNSUPPORTED : EP_ERR_CUDA;
@@ -378,7 +382,9 @@ ep_status ep_create(const ep_config *cfg, ep_ctx **out) {
         free(ctx);
         return EP_ERR_CUDA;
     }
-    if (!ep::layout_pick_shape(cfg->num_experts, cfg->num_ranks, &ctx->layout_cluster, &ctx->layout_threads)) {
+    if (!ep::layout_pick_shape(cfg->num_experts, cfg->num_ranks, &ctx->layout_cluster, &ctx->layout_threads) ||
+        !ep::layout_pick_shape(cfg->num_experts, cfg->num_ranks, &ctx->layout_cluster_many,
+                               &ctx->layout_threads_many, true)) {
         free(ctx);
         return EP_ERR_UNSUPPORTED;
     }
@@ -533,7 +539,10 @@ ep_status ep_get_rank_layout(ep_ctx *ctx, const int64_t *d_topk_idx, const float
     p.tokens_per_rank = nullptr;
     p.is_token_in_rank = nullptr;
     p.status = ctx->d_status;
-    const cudaError_t err = ep::launch_layout(p, ctx->layout_cluster, ctx->layout_threads, (cudaStream_t)stream);
+    const bool many = p.N * p.K >= ep::kLayoutManyEntries;
+    const cudaError_t err = ep::launch_layout(p, many ? ctx->layout_cluster_many : ctx->layout_cluster,
+                                              many ? ctx->layout_threads_many : ctx->layout_threads,
+                                              (cudaStream_t)stream);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return err == cudaErrorInvalidConfiguration ? EP_ERR_UNSUPPORTED : EP_ERR_CUDA;

@@ -48,8 +48,10 @@ cudaError_t launch_layout(const LayoutParams &p, int cluster_size, int threads,
 // Dynamic shared memory the layout kernel needs for these sizes.
 size_t layout_smem_bytes(int E, int R, int threads, int cluster_size);
 // Largest cluster size (16, 8, 4, 2 or 1) and thread count the device can run
-// for these sizes; false if none fits.
-bool layout_pick_shape(int E, int R, int *cluster_size, int *threads);
+// for these sizes (1024 threads first when many_entries); false if none fits.
+bool layout_pick_shape(int E, int R, int *cluster_size, int *threads, bool many_entries = false);
+// Entries (R*T*K) from which the many-entries shape is used.
+constexpr int64_t kLayoutManyEntries = 65536;
 
 // ------------------------------------------------------------------ dispatch
 struct DispatchParams {

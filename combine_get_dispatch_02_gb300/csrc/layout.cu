@@ -432,9 +432,13 @@ size_t layout_smem_bytes(int E, int R, int threads, int cluster_size) {
     return smem_words(E, R, threads, cluster_size) * sizeof(int32_t);
 }
 
-bool layout_pick_shape(int E, int R, int *cluster_size, int *threads) {
+bool layout_pick_shape(int E, int R, int *cluster_size, int *threads, bool many_entries) {
     static const int cls[] = {16, 8, 4, 2, 1};
-    for (int cl : cls) {  // 512 threads measured fastest at the low-latency sizes
+    for (int cl : cls) {
+        // 512 threads measured fastest at the low-latency sizes (32K entries);
+        // from ~64K entries on, 1024 threads hide more of each warp's latency
+        // (262K entries: 27 vs 31 µs, 524K: 50 vs 60 µs)
+        if (many_entries && fits<1024>(E, R, cl)) { *cluster_size = cl; *threads = 1024; return true; }
         if (fits<512>(E, R, cl)) { *cluster_size = cl; *threads = 512; return true; }
         if (fits<1024>(E, R, cl)) { *cluster_size = cl; *threads = 1024; return true; }
         if (fits<256>(E, R, cl)) { *cluster_size = cl; *threads = 256; return true; }
