@@ -378,7 +378,11 @@ def run_ours(args):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    # the timed region: K steps, events at the step boundaries only
+    # the timed region: K steps, events at the step boundaries only.  The GPU
+    # first sleeps ~50 ms (outside the events) so that the host queues the
+    # steps well ahead of it: a host-side stall cannot then leave the GPU
+    # idle inside a timed step.
+    torch.cuda._sleep(100_000_000)
     evs = []
     for _ in range(args.steps):
         flush_l2()
@@ -397,6 +401,7 @@ def run_ours(args):
     ms_per_step, value = replica_throughput(sum(step_ms), args.steps, N, ws, device="cuda")
     # the same K steps again with an event between the dispatch and the
     # combine: each kernel's share of a step (for the rooflines)
+    torch.cuda._sleep(100_000_000)
     evs = []
     for _ in range(args.steps):
         flush_l2()

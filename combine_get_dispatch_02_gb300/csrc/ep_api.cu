@@ -51,6 +51,7 @@ struct ep_handle {
     int32_t has_rank_ranges;  // cnt_er / off_er hold the current layout's ranges
     int32_t rank_mode;        // the layout is rank-deduplicated (keys are ranks)
     int32_t num_keys;         // experts, or ranks in rank mode
+    int32_t *cta_hist;        // grid-form layout: [num_sms][max(E, R)] per-CTA key totals
 };
 
 namespace {
@@ -101,6 +102,24 @@ int grid_cap(const ep_ctx *ctx, int blocks_per_sm) {
     return sms * blocks_per_sm;
 }
 
+// The layout kernel(s) for p: one cluster (512 threads per CTA, or 1024 from
+// kLayoutManyEntries entries on), or the grid form over all SMs from
+// kLayoutGridEntries (rank layout: kLayoutGridEntriesRank) entries on.
+cudaError_t launch_layout_any(const ep_ctx *ctx, ep::LayoutParams &p, const ep_handle *h, cudaStream_t stream) {
+    const int64_t entries = p.N * p.K;
+    p.cta_hist = h->cta_hist;
+    if (entries >= (p.rank_mode ? ep::kLayoutGridEntriesRank : ep::kLayoutGridEntries)) {
+        int sms = ctx->num_sms;
+        if (ctx->cfg.max_sms > 0 && ctx->cfg.max_sms < sms) sms = ctx->cfg.max_sms;
+        const cudaError_t e = ep::launch_layout_grid(p, sms, stream);
+        if (e != cudaErrorInvalidConfiguration) return e;
+        cudaGetLastError();  // beyond the grid form's limits: the cluster form decides
+    }
+    const bool many = entries >= ep::kLayoutManyEntries;
+    return ep::launch_layout(p, many ? ctx->layout_cluster_many : ctx->layout_cluster,
+                             many ? ctx->layout_threads_many : ctx->layout_threads, stream);
+}
+
 ep_status enqueue_layout(ep_ctx *ctx, const int64_t *topk_idx, int32_t T, int32_t *tokens_per_rank,
                          int32_t *user_tokens_per_expert, uint8_t *is_token_in_rank, bool want_ranges,
                          ep_handle *h, cudaStream_t stream) {
@@ -131,9 +150,7 @@ ep_status enqueue_layout(ep_ctx *ctx, const int64_t *topk_idx, int32_t T, int32_
     p.tokens_per_rank = tokens_per_rank;
     p.is_token_in_rank = is_token_in_rank;
     p.status = ctx->d_status;
-    const bool many = p.N * p.K >= ep::kLayoutManyEntries;
-    const cudaError_t err = ep::launch_layout(p, many ? ctx->layout_cluster_many : ctx->layout_cluster,
-                                              many ? ctx->layout_threads_many : ctx->layout_threads, stream);
+    const cudaError_t err = launch_layout_any(ctx, p, h, stream);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return err == cudaErrorInvalidConfiguration ? EP_ERR_UNSUPPORTED : EP_ERR_CUDA;
@@ -441,7 +458,9 @@ ep_status ep_handle_create(ep_ctx *ctx, ep_handle **out) {
               cudaMalloc(&h->cnt_er, er * sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&h->off_er, er * sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&h->base, (size_t)c.num_experts * sizeof(int64_t)) == cudaSuccess &&
-              cudaMalloc(&h->tokens_per_expert, (size_t)c.num_experts * sizeof(int32_t)) == cudaSuccess;
+              cudaMalloc(&h->tokens_per_expert, (size_t)c.num_experts * sizeof(int32_t)) == cudaSuccess &&
+              cudaMalloc(&h->cta_hist, (size_t)ctx->num_sms * (c.num_experts > c.num_ranks ? c.num_experts : c.num_ranks) *
+                                           sizeof(int32_t)) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
         ep_handle_destroy(h);
@@ -459,6 +478,7 @@ ep_status ep_handle_destroy(ep_handle *h) {
     cudaFree(h->off_er);
     cudaFree(h->base);
     cudaFree(h->tokens_per_expert);
+    cudaFree(h->cta_hist);
     free(h);
     return EP_OK;
 }
@@ -539,10 +559,7 @@ ep_status ep_get_rank_layout(ep_ctx *ctx, const int64_t *d_topk_idx, const float
     p.tokens_per_rank = nullptr;
     p.is_token_in_rank = nullptr;
     p.status = ctx->d_status;
-    const bool many = p.N * p.K >= ep::kLayoutManyEntries;
-    const cudaError_t err = ep::launch_layout(p, many ? ctx->layout_cluster_many : ctx->layout_cluster,
-                                              many ? ctx->layout_threads_many : ctx->layout_threads,
-                                              (cudaStream_t)stream);
+    const cudaError_t err = launch_layout_any(ctx, p, handle, (cudaStream_t)stream);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return err == cudaErrorInvalidConfiguration ? EP_ERR_UNSUPPORTED : EP_ERR_CUDA;

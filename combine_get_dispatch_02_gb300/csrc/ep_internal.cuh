@@ -39,6 +39,9 @@ struct LayoutParams {
     uint32_t *status;
     int32_t staged;            // set by launch_layout: entries staged in shared memory
     int32_t er_span;           // set by launch_layout: ranks per CTA for the (e, r) counts
+    // grid form (launch_layout_grid): per-CTA key totals -> prefixes [grid_ctas][E]
+    int32_t *cta_hist;
+    int32_t grid_ctas, grid_tpc;  // set by launch_layout_grid: CTAs, tokens per CTA
 };
 
 // Launch the single-cluster layout kernel.  cluster_size / threads come from
@@ -52,6 +55,16 @@ size_t layout_smem_bytes(int E, int R, int threads, int cluster_size);
 bool layout_pick_shape(int E, int R, int *cluster_size, int *threads, bool many_entries = false);
 // Entries (R*T*K) from which the many-entries shape is used.
 constexpr int64_t kLayoutManyEntries = 65536;
+// The same layout from three kernels spread over `ctas` CTAs (count, scan,
+// write), for many entries: the single cluster leaves most SMs idle.  Needs
+// p.cta_hist with ctas * E ints.  Zeroes tokens_per_rank / cnt_er itself.
+cudaError_t launch_layout_grid(LayoutParams p, int ctas, cudaStream_t stream);
+// Entries from which the grid form is used (measured crossovers, layout +
+// dispatch: below them the single cluster wins because the dispatch casts
+// rows on the SMs the cluster leaves free; the rank-deduplicated keys cost
+// more per entry, so that layout switches earlier).
+constexpr int64_t kLayoutGridEntries = 524288;
+constexpr int64_t kLayoutGridEntriesRank = 262144;
 
 // ------------------------------------------------------------------ dispatch
 struct DispatchParams {

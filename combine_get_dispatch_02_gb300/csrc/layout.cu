@@ -426,6 +426,205 @@ bool fits(int E, int R, int cl) {
     return n >= 1;
 }
 
+// ---------------------------------------------------------------- grid form
+// The same layout for many entries, from three kernels over the whole GPU
+// (the single cluster above uses 16 SMs):
+//   count  (C CTAs)  pass 1 over the CTA's token range, as in the cluster
+//                    kernel; each entry's (position among the CTA's entries of
+//                    its key, key) is staged in its slot cell; the CTA's key
+//                    totals go to cta_hist[c][key]
+//   scan   (1 CTA)   cta_hist[c][e] -> entries of e in CTAs below c; totals,
+//                    bases and counts; per-(expert, rank) offsets
+//   write  (C CTAs)  slot = base + prefix + position, src_info, rank-mode rows
+// Chained with programmatic dependent launch; the write kernel lets the
+// dispatch queued behind it start casting rows at once.
+constexpr int kGridThreads = 512;
+
+__global__ void __launch_bounds__(kGridThreads) layout_count_kernel(const LayoutParams p) {
+    constexpr int NT = kGridThreads, NW = NT / 32;
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int E = p.E, R = p.R, K = p.K, T = p.T;
+    const int N = (int)p.N;
+    const int c = blockIdx.x;
+    const int ebits = bits_for(E + 1);
+    extern __shared__ int32_t sm[];
+    int32_t *hist_w = sm;                 // [NW][E] warp counts -> warp start positions in the CTA
+    int32_t *tok_rank = hist_w + NW * E;  // [R]
+    const int span = p.er_span;
+    int32_t *hist_er = tok_rank + R;      // [E][span]
+    const int cta_t0 = min(N, c * p.grid_tpc), cta_t1 = min(N, cta_t0 + p.grid_tpc);
+    const int tpw = (p.grid_tpc + NW - 1) / NW;
+    const int t0 = min(cta_t1, cta_t0 + w * tpw), t1 = min(cta_t1, t0 + tpw);
+    const int i0 = t0 * K, i1 = t1 * K;
+    int32_t *stage = p.slot;  // (position, key) of each entry until the write kernel
+    const bool want_er = p.cnt_er != nullptr;
+    const int r0 = T > 0 ? cta_t0 / T : 0;
+
+    int64_t raw[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) raw[u] = load_raw(p.topk_idx, i0 + u * 32 + lane, i1);
+    for (int i = tid; i < NW * E + R; i += NT) sm[i] = 0;
+    for (int i = tid; i < E * span; i += NT) hist_er[i] = 0;
+    if (p.is_token_in_rank) {
+        for (int b = cta_t0 * R + tid; b < cta_t1 * R; b += NT) p.is_token_in_rank[b] = 0;
+    }
+    __syncthreads();
+
+    const int erbits = bits_for(E * span + 1);
+    for (int ib = i0; ib < i1; ib += 32 * kU) {
+        if (ib != i0) {
+#pragma unroll
+            for (int u = 0; u < kU; ++u) raw[u] = load_raw(p.topk_idx, ib + u * 32 + lane, i1);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (ib + u * 32 >= i1) break;  // warp-uniform
+            const int i = ib + u * 32 + lane;
+            const int e = to_key(p, raw[u], i);
+            const uint32_t peers = warp_match(e < 0 ? E : e, ebits);
+            int local = 0;
+            if (e >= 0) local = hist_w[w * E + e] + __popc(peers & lanemask_lt());
+            __syncwarp();
+            if (e >= 0 && lane == __ffs(peers) - 1) hist_w[w * E + e] += __popc(peers);
+            __syncwarp();
+            if (i < i1) stage[i] = (local << 11) | (e + 1);
+            if (want_er) {
+                const int key = e >= 0 ? e * span + (i / K) / T - r0 : E * span;
+                const uint32_t pk = warp_match(key, erbits);
+                if (e >= 0 && lane == __ffs(pk) - 1) atomicAdd(&hist_er[key], __popc(pk));
+            }
+        }
+    }
+    if (p.tokens_per_rank || p.is_token_in_rank) {
+        for (int g = t0 + lane; g < t1; g += 32) {
+            const int64_t *row = p.topk_idx + (int64_t)g * K;
+            for (int k = 0; k < K; ++k) {
+                const int64_t e = row[k];
+                if (e < 0 || e >= p.num_experts) continue;
+                const int d = (int)e / p.L;
+                bool seen = false;
+                for (int k2 = 0; k2 < k && !seen; ++k2) {
+                    const int64_t e2 = row[k2];
+                    seen = e2 >= 0 && e2 < p.num_experts && (int)e2 / p.L == d;
+                }
+                if (seen) continue;
+                atomicAdd(&tok_rank[d], 1);
+                if (p.is_token_in_rank) p.is_token_in_rank[(int64_t)g * R + d] = 1;
+            }
+        }
+    }
+    __syncthreads();
+    // per key: exclusive prefix over the CTA's warps; the CTA total to global
+    for (int e = tid; e < E; e += NT) {
+        int s = 0;
+        for (int ww = 0; ww < NW; ++ww) {
+            const int v = hist_w[ww * E + e];
+            hist_w[ww * E + e] = s;
+            s += v;
+        }
+        p.cta_hist[(int64_t)c * E + e] = s;
+    }
+    if (p.tokens_per_rank)  // zeroed before this kernel
+        for (int d = tid; d < R; d += NT)
+            if (tok_rank[d] != 0) atomicAdd(&p.tokens_per_rank[d], tok_rank[d]);
+    if (want_er)  // zeroed before this kernel
+        for (int j = tid; j < E * span; j += NT)
+            if (hist_er[j] != 0) atomicAdd(&p.cnt_er[(j / span) * R + r0 + j % span], hist_er[j]);
+    __syncthreads();
+    // positions relative to the CTA (the lane that staged an entry rewrites it)
+    for (int i = i0 + lane; i < i1; i += 32) {
+        const int v = stage[i];
+        const int e = (v & 2047) - 1;
+        if (e >= 0) stage[i] = ((hist_w[w * E + e] + (v >> 11)) << 11) | (e + 1);
+    }
+}
+
+__global__ void __launch_bounds__(1024) layout_scan_kernel(const LayoutParams p) {
+    __shared__ int32_t tot[1024];
+    __shared__ int32_t scan[1024 / 32 + 1];
+    pdl_wait();
+    const int E = p.E, C = p.grid_ctas, R = p.R;
+    const int e = threadIdx.x;  // E <= 1024
+    if (e < E) {
+        int run = 0;
+#pragma unroll 8
+        for (int c = 0; c < C; ++c) {
+            const int v = p.cta_hist[(int64_t)c * E + e];
+            p.cta_hist[(int64_t)c * E + e] = run;
+            run += v;
+        }
+        tot[e] = run;
+    }
+    __syncthreads();
+    int total;
+    const int excl = block_exclusive_scan<1024>(e < E ? tot[e] : 0, scan, &total);
+    if (e < E) {
+        const int64_t b = p.layout == kLayoutPadded ? (int64_t)e * p.cap : (int64_t)excl;
+        const int n = (int)min((int64_t)tot[e], p.cap);
+        p.tokens_per_expert[e] = n;
+        if (p.user_tokens_per_expert) p.user_tokens_per_expert[e] = n;
+        p.base[e] = b;
+        if (p.cnt_er != nullptr) {  // offsets over the source ranks
+            int run = 0;
+            for (int r = 0; r < R; ++r) {
+                const int v = p.cnt_er[e * R + r];
+                p.off_er[e * R + r] = run;
+                run += v;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kGridThreads) layout_write_kernel(const LayoutParams p) {
+    // the dispatch queued behind may start loading and casting rows now; it
+    // waits for this kernel's results before it reads a slot
+    pdl_launch_dependents();
+    pdl_wait();
+    const int E = p.E, K = p.K, N = (int)p.N;
+    const int c = blockIdx.x;
+    const int cta_t0 = min(N, c * p.grid_tpc), cta_t1 = min(N, cta_t0 + p.grid_tpc);
+    const int i0 = cta_t0 * K, i1 = cta_t1 * K;
+    const int cap = (int)min(p.cap, (int64_t)0x7FFFFFFF);
+    for (int i = i0 + threadIdx.x; i < i1; i += kGridThreads) {
+        const int v = p.slot[i];
+        const int e = (v & 2047) - 1;
+        int32_t s = -1;
+        if (e >= 0) {
+            const int pos = p.cta_hist[(int64_t)c * E + e] + (v >> 11);
+            if (pos < cap) {
+                s = (int32_t)(p.base[e] + pos);
+                p.src_info[s] = i;
+                if (p.recv_topk_idx != nullptr) {  // rank mode: the token's experts on rank e
+                    const int g0 = (i / K) * K;
+                    for (int k2 = 0; k2 < K; ++k2) {
+                        const int64_t e2 = __ldg(p.topk_idx + g0 + k2);
+                        const bool on = e2 >= 0 && e2 < p.num_experts && (int)e2 / p.L == e;
+                        p.recv_topk_idx[(int64_t)s * K + k2] = on ? (int)e2 - e * p.L : -1;
+                        if (p.recv_topk_weights != nullptr)
+                            p.recv_topk_weights[(int64_t)s * K + k2] =
+                                on ? (p.topk_weights != nullptr ? __ldg(p.topk_weights + g0 + k2) : 1.0f) : 0.0f;
+                    }
+                }
+            } else {
+                atomicOr(p.status, kStatusCapacity);
+            }
+        }
+        p.slot[i] = s;
+    }
+}
+
+size_t grid_count_smem(int E, int R, int span) {
+    return ((size_t)(kGridThreads / 32) * E + R + (size_t)E * span) * sizeof(int32_t);
+}
+
+void grid_init() {
+    int dev = 0, optin = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    cudaGetLastError();
+}
+
 }  // namespace
 
 size_t layout_smem_bytes(int E, int R, int threads, int cluster_size) {
@@ -434,6 +633,7 @@ size_t layout_smem_bytes(int E, int R, int threads, int cluster_size) {
 
 bool layout_pick_shape(int E, int R, int *cluster_size, int *threads, bool many_entries) {
     static const int cls[] = {16, 8, 4, 2, 1};
+    grid_init();
     for (int cl : cls) {
         // 512 threads measured fastest at the low-latency sizes (32K entries);
         // from ~64K entries on, 1024 threads hide more of each warp's latency
@@ -444,6 +644,52 @@ bool layout_pick_shape(int E, int R, int *cluster_size, int *threads, bool many_
         if (fits<256>(E, R, cl)) { *cluster_size = cl; *threads = 256; return true; }
     }
     return false;
+}
+
+cudaError_t launch_layout_grid(LayoutParams p, int ctas, cudaStream_t stream) {
+    const int64_t N = p.N;
+    if (N <= 0 || ctas < 1) return cudaErrorInvalidValue;
+    // tokens per CTA; a CTA's entries are packed into 20 bits between the kernels
+    int64_t tpc = (N + ctas - 1) / ctas;
+    if (tpc * p.K >= (int64_t(1) << 20)) return cudaErrorInvalidConfiguration;
+    const int C = (int)((N + tpc - 1) / tpc);
+    p.grid_ctas = C;
+    p.grid_tpc = (int)tpc;
+    p.staged = 0;
+    p.er_span = 0;
+    if (p.cnt_er != nullptr) {
+        const int64_t span = p.T > 0 ? (tpc + p.T - 1) / p.T + 1 : 1;
+        p.er_span = (int)(span < p.R ? span : p.R);
+    }
+    const size_t smem = grid_count_smem(p.E, p.R, p.er_span);
+    if (smem > kMaxSmem) return cudaErrorInvalidConfiguration;
+    cudaError_t e = cudaSuccess;
+    if (p.tokens_per_rank != nullptr) e = cudaMemsetAsync(p.tokens_per_rank, 0, (size_t)p.R * sizeof(int32_t), stream);
+    if (e == cudaSuccess && p.cnt_er != nullptr)
+        e = cudaMemsetAsync(p.cnt_er, 0, (size_t)p.E * p.R * sizeof(int32_t), stream);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = stream;
+    // count: after the previous work in full (it rewrites the slot array)
+    cfg.gridDim = dim3((unsigned)C, 1, 1);
+    cfg.blockDim = dim3(kGridThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, layout_count_kernel, p);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(1024, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, layout_scan_kernel, p);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3((unsigned)C, 1, 1);
+    cfg.blockDim = dim3(kGridThreads, 1, 1);
+    return cudaLaunchKernelEx(&cfg, layout_write_kernel, p);
 }
 
 cudaError_t launch_layout(const LayoutParams &p, int cluster_size, int threads,

@@ -142,6 +142,7 @@ extern "C" ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, 
     lp.tokens_per_rank = nullptr;
     lp.is_token_in_rank = nullptr;
     lp.status = status;
+    lp.cta_hist = nullptr;  // at most 65536 entries here: always the cluster form
     if (ep::launch_layout(lp, s.cluster, s.threads, st) != cudaSuccess) {
         cudaGetLastError();
         return EP_ERR_CUDA;

@@ -75,6 +75,11 @@ LAYOUT_CASES = {
     # 1M entries: too many to keep a shared-memory copy per CTA, so the
     # second pass re-reads topk_idx
     "unstaged_packed": wl.LL.with_(tokens_per_rank=4096, max_tokens_per_rank=4096, layout=wl.PACKED),
+    # 512K+ entries: the grid form (count / scan / write kernels over all SMs)
+    "grid_ll_padded": wl.LL.with_(tokens_per_rank=2048, max_tokens_per_rank=2048),
+    "grid_skew_packed": wl.SKEW.with_(tokens_per_rank=6000, max_tokens_per_rank=6000, layout=wl.PACKED),
+    "grid_ragged_e1024": wl.TINY.with_(num_ranks=8, num_experts=1024, topk=8, tokens_per_rank=8193,
+                                       max_tokens_per_rank=8200),
 }
 
 
@@ -85,29 +90,31 @@ def test_layout_parity(name):
     _check_layout(w, idx)
 
 
-@pytest.mark.parametrize("name", ["tiny", "skew"])
+@pytest.mark.parametrize("name", ["tiny", "skew", "grid_ll_padded"])
 def test_layout_masked_entries(name):
     w = LAYOUT_CASES[name]
     idx = wl.inject_masks(wl.generate(w, with_x=False)["topk_idx"], 0.1, 5)
     _check_layout(w, idx)
 
 
-def test_layout_bad_expert_ids_flagged_and_skipped():
-    w = wl.TINY
+@pytest.mark.parametrize("name", ["tiny", "grid_ll_padded"])
+def test_layout_bad_expert_ids_flagged_and_skipped(name):
+    w = LAYOUT_CASES[name]
     idx = wl.generate(w, with_x=False)["topk_idx"].copy()
-    idx.reshape(-1)[[3, 50, 400]] = [w.num_experts, -7, 10 ** 9]
+    idx.reshape(-1)[[3, 50, 400, idx.size - 1]] = [w.num_experts, -7, 10 ** 9, -2]
     o, _, buf = _check_layout(w, idx, expect_status=ep.EP_ERR_BAD_EXPERT)
-    assert o["n_bad"] == 3
+    assert o["n_bad"] == 4
     assert buf.device_status() == ep.EP_OK  # the status word was cleared
 
 
-def test_layout_capacity_overflow_flagged():
+@pytest.mark.parametrize("T", [8, 65536])  # the cluster form, and the grid form (524288 entries)
+def test_layout_capacity_overflow_flagged(T):
     # repeated experts in a row can offer an expert more than R*Tmax entries
-    w = wl.TINY.with_(num_ranks=2, num_experts=4, topk=4, tokens_per_rank=8, max_tokens_per_rank=8)
-    idx = np.zeros((2, 8, 4), np.int64)
+    w = wl.TINY.with_(num_ranks=2, num_experts=4, topk=4, tokens_per_rank=T, max_tokens_per_rank=T)
+    idx = np.zeros((2, T, 4), np.int64)
     idx[:, :, 3] = 3
     o, _, _ = _check_layout(w, idx, expect_status=ep.EP_ERR_CAPACITY)
-    assert o["n_overflow"] == 2 * 8 * 3 - 16
+    assert o["n_overflow"] == 2 * T * 3 - 2 * T
 
 
 def test_layout_deterministic():
