@@ -544,18 +544,34 @@ __global__ void __launch_bounds__(1024) layout_scan_kernel(const LayoutParams p)
     __shared__ int32_t scan[1024 / 32 + 1];
     pdl_wait();
     const int E = p.E, C = p.grid_ctas, R = p.R;
-    const int e = threadIdx.x;  // E <= 1024
-    if (e < E) {
-        int run = 0;
-#pragma unroll 8
-        for (int c = 0; c < C; ++c) {
-            const int v = p.cta_hist[(int64_t)c * E + e];
-            p.cta_hist[(int64_t)c * E + e] = run;
+    // Q lanes per key (a power of two <= 32, so a key's lanes share a warp),
+    // each summing a contiguous slice of the CTAs with independent loads;
+    // a shuffle scan inside the group gives each slice its start
+    int Q = 1;
+    while (Q < 32 && Q * 2 * E <= 1024) Q *= 2;
+    const int ke = threadIdx.x / Q, q = threadIdx.x % Q;
+    const int per = (C + Q - 1) / Q;
+    const int c0 = min(C, q * per), c1 = min(C, c0 + per);
+    int local = 0;
+    if (ke < E)
+        for (int c = c0; c < c1; ++c) local += p.cta_hist[(int64_t)c * E + ke];
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d, Q);  // within groups of Q lanes
+        if (q >= d) incl += y;
+    }
+    if (ke < E) {
+        int run = incl - local;
+        for (int c = c0; c < c1; ++c) {
+            const int v = p.cta_hist[(int64_t)c * E + ke];
+            p.cta_hist[(int64_t)c * E + ke] = run;
             run += v;
         }
-        tot[e] = run;
+        if (q == Q - 1) tot[ke] = incl;
     }
     __syncthreads();
+    const int e = threadIdx.x;  // E <= 1024
     int total;
     const int excl = block_exclusive_scan<1024>(e < E ? tot[e] : 0, scan, &total);
     if (e < E) {
