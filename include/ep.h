@@ -51,8 +51,9 @@
  *   - Errors a host can see (bad sizes, NULL pointers, misalignment) return at
  *     once and enqueue nothing.  Errors only the GPU can see (an expert id
  *     outside [-1, E), a padded expert buffer offered more than R*Tmax
- *     entries) set bits in a per-context device status word, read and
- *     cleared by ep_get_device_status; the offending entries get no row.
+ *     entries, a copy kernel's bounded wait giving up) set bits in a per-context
+ *     device status word, read and cleared by ep_get_device_status; the
+ *     offending entries get no row.
  *   - A context and its handles belong to the device current at ep_create;
  *     calls must be made with that device current.  A context is not
  *     thread-safe; calls on one context must not overlap on the GPU unless
@@ -92,9 +93,9 @@ typedef enum ep_layout {
  *   num_experts % num_ranks == 0, 1 <= num_experts <= 1024,
  *   num_experts * num_ranks <= 16384,
  *   8 <= hidden <= 65536, hidden % 8 == 0 (FP8 dispatch: hidden % 128 == 0),
- *   receive rows and R*Tmax*K below 2^31, and fewer than 2^20 entries per
- *   warp of the layout kernel (R*T*K < 2^28 when the device runs 16-CTA
- *   clusters of 512 threads; larger calls return EP_ERR_UNSUPPORTED).
+ *   receive rows and R*Tmax*K below 2^31, and a layout of fewer than
+ *   (SM count) * 2^20 entries R*T*K (about 1.6e8 on 152 SMs; larger calls
+ *   return EP_ERR_UNSUPPORTED).
  * max_sms caps the SMs the dispatch and combine kernels spread over (0 = all),
  * the SM-count control of the normal kernels. */
 typedef struct ep_config {
@@ -170,7 +171,9 @@ ep_status ep_handle_get_info(const ep_handle *handle, ep_handle_info *out);
  *   d_is_token_in_rank    device uint8 [R*T, R] or NULL: 1 if token g has an
  *                         entry on rank d, else 0
  *   handle                receives slot / src_info / counts / bases
- * One kernel (a thread-block cluster; no host synchronisation). */
+ * One kernel (a thread-block cluster), or from 512K entries (rank layout:
+ * 256K) three kernels over all SMs plus zeroing copies of the counts they
+ * accumulate; no host synchronisation. */
 ep_status ep_get_dispatch_layout(ep_ctx *ctx, const int64_t *d_topk_idx,
                                  int32_t tokens_per_rank,
                                  int32_t *d_num_tokens_per_rank,
@@ -379,12 +382,12 @@ ep_status ep_set_tuning(ep_ctx *ctx, const ep_tuning *tuning);
 /* Time each launch shape above on the caller's own inputs and keep the
  * fastest in the context (also written to *out; the built-in rule's choice is
  * timed first and kept unless another candidate is at least 3% faster):
- * layout + dispatch with the
- * row dispatch at 1..4 CTAs per SM (H % 512 == 0, H <= 16384), the combine
- * with 1, 2 and 4 chunks per item, then the round trip in one chunk and in
- * chunks of half, one and two times the L2 rule.  Each candidate: the median
- * of `reps` (1..1000) runs, before each a write of twice the L2 size and a
- * read of another twice the L2 size (as behind kernels that just wrote a lot).  Arguments as for ep_round_trip
+ * layout + dispatch with the row dispatch at 1..4 CTAs per SM
+ * (H % 512 == 0, H <= 16384), the combine with 1, 2 and 4 chunks per item,
+ * then the round trip in one chunk and in chunks of half, one and two times
+ * the L2 rule.  Each candidate: the median of `reps` (1..1000) runs, before
+ * each a write of twice the L2 size and a read of another twice the L2 size
+ * (as behind kernels that just wrote a lot).  Arguments as for ep_round_trip
  * (d_topk_idx required, tokens_per_rank >= 1; d_y == d_recv_x tunes the BF16
  * round trip in place); d_recv_x / d_recv_scales / d_y / d_out are
  * overwritten.  Unlike the other calls it allocates (a handle and a 4x-L2
