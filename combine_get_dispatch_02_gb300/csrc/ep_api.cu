@@ -185,6 +185,13 @@ ep_status enqueue_dispatch(ep_ctx *ctx, const ep_handle *h, const void *x, int64
     p.count_dst = count_dst;
     p.E = h->num_keys;
     p.row_sms = (c.max_sms > 0 && c.max_sms < ctx->num_sms) ? c.max_sms : ctx->num_sms;
+    // the warp-item kernel when tuned so, and by the rule for FP8 rows of at
+    // most 2048 channels sent to at most 2 rows each (a 2 KB row and a
+    // 64-byte scale row per bulk copy pair, and only two pairs to amortise
+    // the row's staging: sweep medians 0.88 vs 0.75 of peak at top-2; the
+    // row kernel wins from top-6 on, 0.92 vs 0.87)
+    const int kern = ctx->tune.dispatch_kernel;
+    if (kern == 2 || (kern == 0 && fp8 && c.hidden <= 2048 && c.topk <= 2)) p.row_sms = 0;
     p.prestage = behind_layout ? 8 : 1;
     p.row_bps = ctx->tune.dispatch_ctas_per_sm;
     const int cap = grid_cap(ctx, fp8 ? ctx->dispatch_bps_fp8 : ctx->dispatch_bps_bf16);
@@ -837,6 +844,7 @@ ep_status ep_set_tuning(ep_ctx *ctx, const ep_tuning *t) {
     if (t->combine_chunks != 0 && t->combine_chunks != 1 && t->combine_chunks != 2 && t->combine_chunks != 4)
         return EP_ERR_INVALID_ARG;
     if (t->round_trip_chunk < 0) return EP_ERR_INVALID_ARG;
+    if (t->dispatch_kernel < 0 || t->dispatch_kernel > 2) return EP_ERR_INVALID_ARG;
     if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
     ctx->tune = *t;
     ctx->combine_bps_tuned = t->combine_chunks > 0 ? ep::combine_blocks_per_sm(0, t->combine_chunks) : 0;
@@ -886,17 +894,18 @@ ep_status ep_autotune(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, i
     // start behind a large write differ by a few per cent from run to run).
     constexpr float kMargin = 0.97f;
 
-    // dispatch: row-kernel CTAs per SM, timed as the common call runs it
-    // (layout kernel, then the dispatch behind it)
-    if (s == EP_OK && c.hidden % 512 == 0 && c.hidden <= 16384) {
-        const int rule = ep::dispatch_row_ctas_rule(c.hidden);
-        std::vector<int> cands = {rule};
-        for (int b = 1; b <= 4; ++b)
-            if (b != rule) cands.push_back(b);
+    // dispatch: (kernel, row-kernel CTAs per SM), timed as the common call
+    // runs it (layout kernel, then the dispatch behind it); the rule first
+    if (s == EP_OK) {
+        std::vector<std::pair<int, int>> cands = {{0, 0}};
+        if (c.hidden % 512 == 0 && c.hidden <= 16384)
+            for (int b = 1; b <= 4; ++b) cands.push_back({1, b});
+        cands.push_back({2, 0});
         float best_us = 0.0f;
         for (size_t j = 0; s == EP_OK && j < cands.size(); ++j) {
             ep_tuning t = best;
-            t.dispatch_ctas_per_sm = cands[j];
+            t.dispatch_kernel = cands[j].first;
+            t.dispatch_ctas_per_sm = cands[j].second;
             s = ep_set_tuning(ctx, &t);
             float us = 0.0f;
             if (s == EP_OK)
@@ -909,10 +918,11 @@ ep_status ep_autotune(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, i
                                                              nullptr, true, st);
                     },
                     reps, flush, flush_bytes, sms, st, &us);
-            if (s == EP_OK) log_candidate(ctx, EP_TUNE_DISPATCH_CTAS_PER_SM, cands[j], us);
+            if (s == EP_OK) log_candidate(ctx, EP_TUNE_DISPATCH, 100 * cands[j].first + cands[j].second, us);
             if (s == EP_OK && (j == 0 || us < kMargin * best_us)) {
                 best_us = us;
-                best.dispatch_ctas_per_sm = cands[j];
+                best.dispatch_kernel = cands[j].first;
+                best.dispatch_ctas_per_sm = cands[j].second;
             }
         }
     }

@@ -41,7 +41,7 @@ ENTRY_POINTS = (
     "ep_get_tuning", "ep_set_tuning", "ep_autotune", "ep_get_autotune_log",
 )
 
-TUNE_KNOBS = {0: "dispatch_ctas_per_sm", 1: "combine_chunks", 2: "round_trip_chunk"}
+TUNE_KNOBS = {0: "dispatch", 1: "combine_chunks", 2: "round_trip_chunk"}  # dispatch: 100 * kernel + CTAs/SM
 
 EP_CHUNK_AUTO = -1
 
@@ -61,7 +61,7 @@ class ep_config(ctypes.Structure):
 
 class ep_tuning(ctypes.Structure):
     _fields_ = [("dispatch_ctas_per_sm", ctypes.c_int32), ("combine_chunks", ctypes.c_int32),
-                ("round_trip_chunk", ctypes.c_int32)]
+                ("round_trip_chunk", ctypes.c_int32), ("dispatch_kernel", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -356,16 +356,24 @@ ep_status ep_round_trip_auto_chunk(const ep_ctx *ctx, int32_t use_fp8, int32_t r
  *                         0 = the built-in rule (from the entries per token)
  *   round_trip_chunk      tokens per chunk that EP_CHUNK_AUTO stands for in
  *                         ep_round_trip; 0 = the L2 rule; >= R*T (INT32_MAX
- *                         from ep_autotune) = one chunk */
+ *                         from ep_autotune) = one chunk
+ *   dispatch_kernel       0 = the built-in rule (the warp-item kernel for FP8
+ *                         rows of H <= 2048 with topk <= 2, else the row
+ *                         kernel where it applies), 1 = the row kernel (bulk copies of whole
+ *                         rows; only where H % 512 == 0 and H <= 16384, the
+ *                         warp-item kernel elsewhere), 2 = the warp-item kernel
+ *                         (16-byte stores by every lane) */
 typedef struct ep_tuning {
     int32_t dispatch_ctas_per_sm;
     int32_t combine_chunks;
     int32_t round_trip_chunk;
+    int32_t dispatch_kernel;
 } ep_tuning;
 
 /* One candidate ep_autotune timed: knob (EP_TUNE_*), its value, median µs. */
 typedef enum ep_tune_knob {
-    EP_TUNE_DISPATCH_CTAS_PER_SM = 0,  /* timed as layout + dispatch */
+    EP_TUNE_DISPATCH = 0,              /* value 100 * dispatch_kernel + dispatch_ctas_per_sm;
+                                          timed as layout + dispatch */
     EP_TUNE_COMBINE_CHUNKS = 1,
     EP_TUNE_ROUND_TRIP_CHUNK = 2       /* INT32_MAX: one chunk */
 } ep_tune_knob;
@@ -382,8 +390,9 @@ ep_status ep_set_tuning(ep_ctx *ctx, const ep_tuning *tuning);
 /* Time each launch shape above on the caller's own inputs and keep the
  * fastest in the context (also written to *out; the built-in rule's choice is
  * timed first and kept unless another candidate is at least 3% faster):
- * layout + dispatch with the row dispatch at 1..4 CTAs per SM
- * (H % 512 == 0, H <= 16384), the combine with 1, 2 and 4 chunks per item,
+ * layout + dispatch with the rule's kernel, the row kernel at 1..4 CTAs per
+ * SM (H % 512 == 0, H <= 16384) and the warp-item kernel, the combine with
+ * 1, 2 and 4 chunks per item,
  * then the round trip in one chunk and in chunks of half, one and two times
  * the L2 rule.  Each candidate: the median of `reps` (1..1000) runs, before
  * each a write of twice the L2 size and a read of another twice the L2 size
