@@ -57,6 +57,10 @@ def _args():
                     help="time the sweep grid (one JSON line per point) instead of the bench step")
     ap.add_argument("--sweep-filter", default="", help="only sweep points whose name contains this")
     ap.add_argument("--sweep-reps", type=int, default=10)
+    ap.add_argument("--dtype", choices=["fp8", "bf16"], default=None,
+                    help="override the workload's dispatch payload")
+    ap.add_argument("--backward-reps", type=int, default=20,
+                    help="reps of the backward pair (BF16 expert-major workloads; 0: skip)")
     ap.add_argument("--autotune", action="store_true",
                     help="time the launch-shape candidates on the workload first (ep_autotune) and use the best")
     ap.add_argument("--split-reps", type=int, default=50,
@@ -291,6 +295,8 @@ def run_ours(args):
     w = wl.WORKLOADS[args.workload]
     if args.layout is not None:
         w = w.with_(layout=args.layout)
+    if args.dtype is not None:
+        w = w.with_(use_fp8=(args.dtype == "fp8"))
     d = wl.generate(w)
     N, K, H = w.num_tokens, w.topk, w.hidden
 
@@ -458,6 +464,19 @@ def run_ours(args):
     except Exception as exc:  # report, do not hide, a capture failure
         graph_us = (f"capture failed: {exc}", None)
 
+    # the backward pair on the cached layout: grad of combine = BF16 dispatch
+    # of the output gradient, grad of dispatch = unweighted combine of the
+    # received-row gradients
+    backward = None
+    if args.backward_reps > 0 and not args.rank and not w.use_fp8:
+        gx = torch.empty(N, H, dtype=torch.bfloat16, device="cuda")
+        bd = timed(lambda: ep.ep_dispatch(ctx, out, None, w.tokens_per_rank, False, h.raw, recv, None, None,
+                                          stream), args.backward_reps)
+        bc = timed(lambda: ep.ep_combine(ctx, y, None, h.raw, gx, stream), args.backward_reps)
+        backward = {"grad_combine_dispatch_median_us": bd[0], "grad_dispatch_combine_median_us": bc[0],
+                    "tokens_per_s": N / ((bd[0] + bc[0]) / 1e6)}
+        del gx
+
     # the round trip with the identity expert between dispatch and combine,
     # pipelined over token chunks (layout included), and the identity
     # expert alone
@@ -545,7 +564,7 @@ def run_ours(args):
             torch.distributed.destroy_process_group()
         return
     _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
-            e2e, clk, graph_us, copy_gbs, round_trip, split, tuning, split_step_ms)
+            e2e, clk, graph_us, copy_gbs, round_trip, split, tuning, split_step_ms, backward)
     if ws > 1:
         torch.distributed.destroy_process_group()
 
@@ -647,7 +666,7 @@ def _e2e(args, w, d, x, idx, wts, out, enqueue, stream):
 
 def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
             e2e, clk, graph_us=None, copy_gbs=None, round_trip=None, split=None, tuning=None,
-            split_step_ms=None):
+            split_step_ms=None, backward=None):
     peak, peak_kind = _peaks()
     disp_bytes, disp_kernel_bytes, comb_bytes = _algorithmic_bytes(w, M)
     comb_avg_s = statistics.mean(comb_ms) / 1e3
@@ -691,6 +710,7 @@ def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, la
         "e2e": e2e,
         "round_trip": round_trip,
         "split": split,
+        "backward": backward,
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
         "host_cores": os.cpu_count(),
