@@ -185,13 +185,15 @@ ep_status enqueue_dispatch(ep_ctx *ctx, const ep_handle *h, const void *x, int64
     p.count_dst = count_dst;
     p.E = h->num_keys;
     p.row_sms = (c.max_sms > 0 && c.max_sms < ctx->num_sms) ? c.max_sms : ctx->num_sms;
-    // the warp-item kernel when tuned so, and by the rule for FP8 rows of at
-    // most 2048 channels sent to at most 2 rows each (a 2 KB row and a
-    // 64-byte scale row per bulk copy pair, and only two pairs to amortise
-    // the row's staging: sweep medians 0.88 vs 0.75 of peak at top-2; the
-    // row kernel wins from top-6 on, 0.92 vs 0.87)
+    // the warp-item kernel when tuned so, and by the rule for short FP8 rows
+    // (a <= 2 KB row and a 64-byte scale row per bulk copy pair, too few
+    // pairs to amortise the row's staging): H <= 1024 at any top-k, and
+    // H <= 2048 up to top-4 (sweep medians at H = 2048: 0.88 vs 0.75 of peak
+    // at top-2, 0.89 vs 0.83 at top-3; the row kernel wins from top-6 on,
+    // 0.92 vs 0.87)
     const int kern = ctx->tune.dispatch_kernel;
-    if (kern == 2 || (kern == 0 && fp8 && c.hidden <= 2048 && c.topk <= 2)) p.row_sms = 0;
+    const bool short_fp8 = fp8 && (c.hidden <= 1024 || (c.hidden <= 2048 && c.topk <= 4));
+    if (kern == 2 || (kern == 0 && short_fp8)) p.row_sms = 0;
     p.prestage = behind_layout ? 8 : 1;
     p.row_bps = ctx->tune.dispatch_ctas_per_sm;
     const int cap = grid_cap(ctx, fp8 ? ctx->dispatch_bps_fp8 : ctx->dispatch_bps_bf16);

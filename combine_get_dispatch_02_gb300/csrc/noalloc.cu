@@ -162,7 +162,9 @@ extern "C" ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, 
     dp.E = c.num_experts;
     int sms = s.num_sms;
     if (c.max_sms > 0 && c.max_sms < sms) sms = c.max_sms;
-    dp.row_sms = (use_fp8 && c.hidden <= 2048 && c.topk <= 2) ? 0 : sms;  // small FP8 rows, top-1/2: warp-item
+    // short FP8 rows go to the warp-item kernel (the rule of ep_dispatch)
+    const bool short_fp8 = use_fp8 && (c.hidden <= 1024 || (c.hidden <= 2048 && c.topk <= 4));
+    dp.row_sms = short_fp8 ? 0 : sms;
     dp.prestage = 8;  // behind the layout kernel
     dp.row_bps = 0;
     const int cap = sms * (use_fp8 ? s.bps_fp8 : s.bps_bf16);

@@ -358,8 +358,8 @@ ep_status ep_round_trip_auto_chunk(const ep_ctx *ctx, int32_t use_fp8, int32_t r
  *                         ep_round_trip; 0 = the L2 rule; >= R*T (INT32_MAX
  *                         from ep_autotune) = one chunk
  *   dispatch_kernel       0 = the built-in rule (the warp-item kernel for FP8
- *                         rows of H <= 2048 with topk <= 2, else the row
- *                         kernel where it applies), 1 = the row kernel (bulk copies of whole
+ *                         rows of H <= 1024, or H <= 2048 with topk <= 4, else
+ *                         the row kernel where it applies), 1 = the row kernel (bulk copies of whole
  *                         rows; only where H % 512 == 0 and H <= 16384, the
  *                         warp-item kernel elsewhere), 2 = the warp-item kernel
  *                         (16-byte stores by every lane) */
