@@ -697,6 +697,13 @@ def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, la
             "combine_alone_median": comb_us[0],
             "step_cuda_graph_replay_median": graph_us[0] if graph_us else None,
         },
+        "tokens_per_s": {  # N / t per op (in-step means) and for the step
+            "step": value,
+            "dispatch_with_layout": ws * N / (statistics.mean(disp_ms) / 1e3),
+            "combine": ws * N / (statistics.mean(comb_ms) / 1e3),
+            "dispatch_cached_layout": N / (disp_us[0] / 1e6) if disp_us[0] else None,
+            "step_cuda_graph_replay": N / (graph_us[0] / 1e6) if graph_us and isinstance(graph_us[0], float) else None,
+        },
         "hbm_copy_gbs_torch_here": copy_gbs,
         "roofline": {"bound": "hbm", "kernel": "combine", "achieved": comb_gbs, "peak": peak,
                      "unit": "GB/s", "frac": comb_gbs / peak, "traffic": traffic,
