@@ -3,7 +3,7 @@
 Each ``csrc/*.cu`` is compiled in parallel with
 ``nvcc -gencode arch=compute_103a,code=sm_103a -O3 -lineinfo`` and the objects
 are linked into ``combine_get_dispatch_02_gb300/libep.so`` (CUDA runtime
-linked statically, so the library needs only the driver at run time).
+linked statically, so the library needs only libcuda at run time).
 
 Usage: ``python -m combine_get_dispatch_02_gb300.build [--verbose-ptxas]``.
 """

@@ -74,7 +74,7 @@ extern "C" {
 typedef enum ep_status {
     EP_OK = 0,
     EP_ERR_INVALID_ARG = 1,  /* a host-checkable argument is wrong; nothing enqueued */
-    EP_ERR_UNSUPPORTED = 2,  /* valid but beyond this build's limits (see ep_config) */
+    EP_ERR_UNSUPPORTED = 2,  /* valid but beyond the library's limits (see ep_config) */
     EP_ERR_OOM = 3,          /* a device allocation in ep_create / ep_handle_create failed */
     EP_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
     EP_ERR_BAD_EXPERT = 5,   /* device: a topk_idx entry was outside [-1, E) */
@@ -88,7 +88,7 @@ typedef enum ep_layout {
     EP_LAYOUT_PACKED = 1     /* normal mode: experts back to back (prefix sums) */
 } ep_layout;
 
-/* Sizes of one expert-parallel group.  Limits of this build:
+/* Sizes of one expert-parallel group.  Limits of the library:
  *   1 <= num_ranks <= 1024, 1 <= max_tokens_per_rank, 1 <= topk <= 32,
  *   num_experts % num_ranks == 0, 1 <= num_experts <= 1024,
  *   num_experts * num_ranks <= 16384,
