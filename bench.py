@@ -162,38 +162,78 @@ class Clocks:
 
 # ------------------------------------------------------------------ CPU oracle
 
-def _oracle_sample_step(w, d, ye, tokens):
+def _oracle_sample_step(w, topk_idx, topk_weights, x_rows, ye, tokens):
     """One oracle step on a token sample: the full layout, then FP8 dispatch
-    and combine of the sampled tokens."""
+    and combine of the sampled tokens (x_rows, ye: their rows)."""
     import oracle
-    o = oracle.layout(d["topk_idx"], w.num_experts, w.max_tokens_per_rank, oracle.LAYOUT_PADDED)
-    x2 = d["x_bits"].reshape(w.num_tokens, w.hidden)
+    o = oracle.layout(topk_idx, w.num_experts, w.max_tokens_per_rank, oracle.LAYOUT_PADDED)
     sl = o["slot"][tokens]
     # dispatch rows of the sample into a compact buffer (row j*K + k)
     compact = np.arange(len(tokens) * w.topk, dtype=np.int32).reshape(len(tokens), w.topk)
     compact = np.where(sl >= 0, compact, -1).astype(np.int32)
-    oracle.dispatch(x2[tokens], compact, len(tokens) * w.topk, True)
-    oracle.combine(ye.reshape(-1, w.hidden), compact, d["topk_weights"].reshape(w.num_tokens, -1)[tokens])
+    oracle.dispatch(x_rows, compact, len(tokens) * w.topk, True)
+    oracle.combine(ye.reshape(-1, w.hidden), compact, topk_weights.reshape(w.num_tokens, -1)[tokens])
+
+
+def _oracle_timed(w, topk_idx, topk_weights, x_rows, ye, tokens, seconds):
+    """Oracle steps on one token sample for about `seconds`: (tokens done, s)."""
+    n, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_sample_step(w, topk_idx, topk_weights, x_rows, ye, tokens)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return n * len(tokens), el
+
+
+def _oracle_worker(job):
+    """Process-pool entry (spawned): one core's share of the CPU baseline."""
+    return _oracle_timed(*job)
 
 
 def cpu_baseline(w, seconds: float, sample_tokens: int):
+    """The C oracle as it stands on the host's cores: one process per core,
+    each timing full steps (layout + FP8 dispatch + combine) on its own token
+    sample; and the same on one core."""
+    import multiprocessing
     import oracle
     oracle.build()
     from combine_get_dispatch_02_gb300 import workloads as wl
     d = wl.generate(w)
-    tokens = np.arange(min(sample_tokens, w.num_tokens))
-    ye = wl.expert_outputs(w, tokens)
-    n, t0 = 0, time.perf_counter()
-    while True:
-        _oracle_sample_step(w, d, ye, tokens)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": n * len(tokens) / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} oracle steps of {len(tokens)} of the {w.num_tokens} tokens "
-                      f"(full layout each step, FP8 dispatch + combine of the sample), "
-                      f"{el:.1f} s single-threaded"}
+    x2 = d["x_bits"].reshape(w.num_tokens, w.hidden)
+    wts = d["topk_weights"].reshape(w.num_tokens, -1)
+    ns = min(sample_tokens, w.num_tokens)
+
+    def job(i):
+        tokens = (np.arange(ns) + i * ns) % w.num_tokens
+        return (w, d["topk_idx"], wts, np.ascontiguousarray(x2[tokens]), wl.expert_outputs(w, tokens), tokens,
+                seconds)
+
+    done1, el1 = _oracle_timed(*job(0))
+    one = done1 / el1
+    cores = os.cpu_count() or 1
+    value, used = one, 1
+    if cores > 1:
+        # spawned, not forked (this process has already used CUDA); an
+        # executor, not a Pool, so that a worker that dies raises instead of
+        # being replaced for ever; bounded in time
+        from concurrent.futures import ProcessPoolExecutor
+        ex = ProcessPoolExecutor(max_workers=cores, mp_context=multiprocessing.get_context("spawn"))
+        try:
+            res = list(ex.map(_oracle_worker, [job(i) for i in range(cores)], timeout=4 * seconds + 120))
+            value, used = sum(r[0] for r in res) / max(r[1] for r in res), cores
+        except Exception as exc:  # report the one-core number and why
+            for proc in list(getattr(ex, "_processes", {}).values()):
+                proc.terminate()
+            ex.shutdown(wait=False, cancel_futures=True)
+            return {"value": one, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                    "sample": f"{ns} of the {w.num_tokens} tokens per step, full layout each step, one core "
+                              f"(the all-cores run failed: {type(exc).__name__})"}
+        ex.shutdown(wait=True)
+    return {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"each process: steps on {ns} of the {w.num_tokens} tokens (full layout each step, FP8 "
+                      f"dispatch + combine of the sample) for ~{seconds:.0f} s; {used} processes, one per core",
+            "one_core": {"value": one, "cores": 1}}
 
 
 def run_reference(args):
@@ -206,20 +246,23 @@ def run_reference(args):
     # bounded sample per step so that warmup + steps finish in about two minutes
     import oracle
     oracle.build()
+    x2 = d["x_bits"].reshape(w.num_tokens, w.hidden)
+    wts = d["topk_weights"].reshape(w.num_tokens, -1)
     probe_tokens = np.arange(16)
     ye16 = wl.expert_outputs(w, probe_tokens)
     t0 = time.perf_counter()
-    _oracle_sample_step(w, d, ye16, probe_tokens)
+    _oracle_sample_step(w, d["topk_idx"], wts, x2[probe_tokens], ye16, probe_tokens)
     per_token = max((time.perf_counter() - t0) / 16, 1e-6)
     budget = 120.0 / max(args.steps + args.warmup, 1)
     ntok = int(max(1, min(w.num_tokens, budget / per_token)))
     tokens = np.arange(ntok)
     ye = wl.expert_outputs(w, tokens)
+    x_rows = np.ascontiguousarray(x2[tokens])
     for _ in range(args.warmup):
-        _oracle_sample_step(w, d, ye, tokens)
+        _oracle_sample_step(w, d["topk_idx"], wts, x_rows, ye, tokens)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_sample_step(w, d, ye, tokens)
+        _oracle_sample_step(w, d["topk_idx"], wts, x_rows, ye, tokens)
     el = time.perf_counter() - t0
     value = args.steps * ntok / el
     line = {
