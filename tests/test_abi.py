@@ -112,3 +112,22 @@ def test_host_rejections_of_the_range_split_and_tuning_calls(lib):
     assert lib.ep_autotune(None, None, None, 1, None, 0, None, None, None, None, 1, ctypes.byref(t), None) == E
     assert lib.ep_get_autotune_log(None, None, 0, ctypes.byref(n)) == E
     assert lib.ep_status_str(ep.EP_ERR_TIMEOUT).decode() == "a bounded wait on the device gave up"
+
+
+def test_receive_row_counts_match_the_definitions_and_the_oracle(lib):
+    """Host-only size queries: padded E·R·Tmax / packed R·Tmax·K rows, and for
+    the rank-deduplicated layout R·R·Tmax / R·Tmax·min(K, R) — the same
+    numbers the oracle's own (independent) definitions give."""
+    import oracle
+    for R, Tmax, E, K in [(32, 128, 256, 8), (8, 4096, 256, 8), (4, 32, 32, 4), (16, 512, 64, 6), (2, 8, 4, 4),
+                          (8, 100, 16, 12)]:
+        for layout in (ep.EP_LAYOUT_PADDED, ep.EP_LAYOUT_PACKED):
+            cfg = ep.make_config(R, Tmax, 1024, E, K, layout=layout)
+            rows = ep.ep_recv_rows(cfg)
+            rank_rows = ep.ep_rank_recv_rows(cfg)
+            if layout == ep.EP_LAYOUT_PADDED:
+                assert rows == E * R * Tmax and rank_rows == R * R * Tmax
+            else:
+                assert rows == R * Tmax * K and rank_rows == R * Tmax * min(K, R)
+            assert rows == oracle.recv_rows(R, Tmax, E, K, layout)
+            assert rank_rows == oracle.rank_recv_rows(R, Tmax, K, layout)
