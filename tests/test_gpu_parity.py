@@ -71,6 +71,9 @@ LAYOUT_CASES = {
     "tiny_k32": wl.TINY.with_(num_experts=64, topk=32),
     "r16_e1024": wl.TINY.with_(num_ranks=16, num_experts=1024, topk=8, tokens_per_rank=40,
                                max_tokens_per_rank=64),
+    # the most ranks the limits allow (E % R == 0 and E*R <= 16384): one expert per rank
+    "r128_e128": wl.TINY.with_(num_ranks=128, num_experts=128, topk=8, tokens_per_rank=16,
+                               max_tokens_per_rank=16),
     "empty": wl.TINY.with_(tokens_per_rank=0),
     # 1M entries: too many to keep a shared-memory copy per CTA, so the
     # second pass re-reads topk_idx
@@ -162,6 +165,9 @@ DISPATCH_CASES = {
     "h32768_fp8": wl.TINY.with_(hidden=32768, use_fp8=True, tokens_per_rank=8,
                                 max_tokens_per_rank=8),                          # warp-item kernel
     "packed_fp8": wl.SKEW.with_(layout=wl.PACKED),
+    # the largest hidden size (the warp-item kernel)
+    "h65536_bf16": wl.TINY.with_(hidden=65536, tokens_per_rank=2, max_tokens_per_rank=2),
+    "h65536_fp8": wl.TINY.with_(hidden=65536, tokens_per_rank=2, max_tokens_per_rank=2, use_fp8=True),
 }
 
 
@@ -277,6 +283,9 @@ COMBINE_CASES = {
     "h32768_k2": (wl.TINY.with_(hidden=32768, topk=2, tokens_per_rank=8, max_tokens_per_rank=8), True),
     "k3": (wl.TINY.with_(topk=3), True),
     "skew_packed": (wl.SKEW.with_(layout=wl.PACKED), True),
+    "h65536": (wl.TINY.with_(hidden=65536, tokens_per_rank=2, max_tokens_per_rank=2), True),
+    "r128_e128": (wl.TINY.with_(num_ranks=128, num_experts=128, topk=8, tokens_per_rank=16,
+                                max_tokens_per_rank=16), True),
 }
 
 
