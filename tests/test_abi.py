@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(8):
+    for s in range(9):
         assert ep.status_str(s) and ep.status_str(s) != "unknown status"
     assert ep.status_str(99) == "unknown status"
 
@@ -58,6 +58,45 @@ def test_config_limits(lib):
     for cfg, want in bad:
         assert ep.ep_config_check(cfg) == want, (cfg.num_ranks, cfg.hidden, cfg.num_experts)
     assert lib.ep_config_check(None) == ep.EP_ERR_INVALID_ARG
+
+
+def _limits_of_header(R, Tmax, H, E, K, layout, max_sms):
+    """The status ep_config_check must give, read off the limits the header
+    states for ep_config: a malformed size is INVALID_ARG, a well-formed one
+    past the library's limits UNSUPPORTED."""
+    if min(R, Tmax, H, E, K) < 1 or max_sms < 0 or layout not in (0, 1):
+        return ep.EP_ERR_INVALID_ARG
+    if E % R or H % 8:
+        return ep.EP_ERR_INVALID_ARG
+    if R > 1024 or K > 32 or E > 1024 or H > 65536 or E * R > 16384:
+        return ep.EP_ERR_UNSUPPORTED
+    rows = E * R * Tmax if layout == 0 else R * Tmax * K
+    if rows >= 2**31 or R * Tmax * K >= 2**31:
+        return ep.EP_ERR_UNSUPPORTED
+    return ep.EP_OK
+
+
+def test_config_limits_search(lib):
+    """Hypothesis walks the edges of every limit (and the 2^31 row bound)."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    def near(*edges):
+        return st.one_of([st.integers(e - 2, e + 2) for e in edges] + [st.integers(-3, 2**31 - 1)])
+
+    @hyp.settings(max_examples=600, deadline=None, derandomize=True, database=None)
+    @hyp.given(R=near(1, 32, 1024), Tmax=near(1, 128, 1 << 16, 1 << 21), H=near(8, 7168, 65536),
+               E=near(1, 256, 1024, 16384), K=near(1, 8, 32), layout=st.integers(-1, 2),
+               max_sms=st.integers(-2, 200))
+    def check(R, Tmax, H, E, K, layout, max_sms):
+        cfg = ep.make_config(R, Tmax, H, E, K, layout=layout, max_sms=max_sms)
+        want = _limits_of_header(R, Tmax, H, E, K, layout, max_sms)
+        assert ep.ep_config_check(cfg) == want, (R, Tmax, H, E, K, layout, max_sms)
+        if want == ep.EP_OK:
+            rows = E * R * Tmax if layout == 0 else R * Tmax * K
+            assert ep.ep_recv_rows(cfg) == rows
+
+    check()
 
 
 def test_size_queries(lib):
