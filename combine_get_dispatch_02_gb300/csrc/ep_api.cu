@@ -1,8 +1,8 @@
 // Host side of libep.so: the C ABI declared in include/ep.h — argument checks,
 // context / handle management and kernel launches.  No call here synchronises
-// the host except ep_get_device_status, and none allocates except
-// ep_create / ep_handle_create, so a dispatch + combine sequence can be
-// captured in a CUDA graph.
+// the host except ep_get_device_status and ep_autotune, and none allocates
+// except ep_create / ep_handle_create / ep_autotune, so a dispatch + combine
+// sequence can be captured in a CUDA graph.
 #include <limits.h>
 #include <stdlib.h>
 #include <string.h>
@@ -150,6 +150,7 @@ ep_status enqueue_layout(ep_ctx *ctx, const int64_t *topk_idx, int32_t T, int32_
     p.tokens_per_rank = tokens_per_rank;
     p.is_token_in_rank = is_token_in_rank;
     p.status = ctx->d_status;
+    h->tokens_per_rank = -1;  // until the launches are in: a failed one may have overwritten part of the layout
     const cudaError_t err = launch_layout_any(ctx, p, h, stream);
     if (err != cudaSuccess) {
         cudaGetLastError();
@@ -568,6 +569,7 @@ ep_status ep_get_rank_layout(ep_ctx *ctx, const int64_t *d_topk_idx, const float
     p.tokens_per_rank = nullptr;
     p.is_token_in_rank = nullptr;
     p.status = ctx->d_status;
+    handle->tokens_per_rank = -1;  // as in enqueue_layout
     const cudaError_t err = launch_layout_any(ctx, p, handle, (cudaStream_t)stream);
     if (err != cudaSuccess) {
         cudaGetLastError();

@@ -47,7 +47,7 @@
  *     host memory.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
  *     enqueue work: none of them synchronises the host, except
- *     ep_get_device_status.
+ *     ep_get_device_status and ep_autotune (which times candidates).
  *   - Errors a host can see (bad sizes, NULL pointers, misalignment) return at
  *     once and enqueue nothing.  Errors only the GPU can see (an expert id
  *     outside [-1, E), a padded expert buffer offered more than R*Tmax
@@ -173,7 +173,10 @@ ep_status ep_handle_get_info(const ep_handle *handle, ep_handle_info *out);
  *   handle                receives slot / src_info / counts / bases
  * One kernel (a thread-block cluster), or from 512K entries (rank layout:
  * 256K) three kernels over all SMs plus zeroing copies of the counts they
- * accumulate; no host synchronisation. */
+ * accumulate; no host synchronisation.  If a launch fails (EP_ERR_CUDA /
+ * EP_ERR_UNSUPPORTED) the handle holds no layout afterwards (the calls that
+ * need one return EP_ERR_NO_LAYOUT); host-side argument errors leave it as
+ * it was. */
 ep_status ep_get_dispatch_layout(ep_ctx *ctx, const int64_t *d_topk_idx,
                                  int32_t tokens_per_rank,
                                  int32_t *d_num_tokens_per_rank,
