@@ -166,6 +166,9 @@ SEARCH_MUTANTS = {
     "layout: padded buffers sized by T instead of Tmax": "layout",
     "layout: invalid ids not reported": "layout",
     "layout: padded overflow not dropped": "layout",
+    "layout: padded counts not capped": "layout",
+    "layout: source rank taken as g mod R": "layout",
+    "layout: tokens per rank counts entries": "layout",
     "rank layout: every entry carries its token": "rank_layout",
     "rank layout: weights of other ranks' experts kept": "rank_layout",
     "rank layout: rank buffers sized by T instead of Tmax": "rank_layout",

@@ -79,6 +79,27 @@ MUTANTS = {
     "layout: padded overflow not dropped": (
         "            if (layout == ORC_LAYOUT_PADDED && pos >= cap) {",
         "            if (0) {"),
+    "layout: padded counts not capped": (
+        "tokens_per_expert[e] = (int32_t)cap;",
+        "tokens_per_expert[e] = tokens_per_expert[e];"),
+    "layout: source rank taken as g mod R": (
+        "int r = (int)(g / T);",
+        "int r = (int)(g % R);"),
+    "layout: tokens per rank counts entries": (
+        "hit = 1;",
+        "hit += 1;"),
+    "fp8: scale from a rounded 1/448": (
+        "float s = amax_c / 448.0f;",
+        "float s = amax_c * (1.0f / 448.0f);"),
+    "fp8: amax of signed values": (
+        "float a = fabsf(orc_bf16_to_f32(x[i]));",
+        "float a = orc_bf16_to_f32(x[i]);"),
+    "fp8 dispatch: scales written to the source token's row": (
+        "orc_quant_token(xg, H, (uint8_t *)recv + s * H, scales + s * (H / 128));",
+        "orc_quant_token(xg, H, (uint8_t *)recv + s * H, scales + g * (H / 128));"),
+    "combine: NULL weights read as 0": (
+        "float wk = w ? w[g * K + k] : 1.0f;",
+        "float wk = w ? w[g * K + k] : 0.0f;"),
 }
 
 
@@ -102,6 +123,8 @@ def _pins():
     yield "e4m3_torch", lambda: pins.test_e4m3_encode_matches_torch(oracle)
     for seed in range(4):
         yield f"exact_rational[{seed}]", (lambda seed=seed: pins.test_combine_exact_rational(oracle, seed))
+    yield "round_trip_bf16", lambda: pins.test_round_trip_bf16(oracle)
+    yield "round_trip_fp8", lambda: pins.test_round_trip_fp8(oracle)
 
 
 @pytest.fixture(scope="module")

@@ -344,7 +344,7 @@ def test_fp8_golden_blocks(orc):
         assert s[0, 0] == sc
         i += 3
         n += 1
-    assert n == 2
+    assert n == 3
 
 
 def test_dequant_rows_golden_and_bound(orc):
