@@ -127,3 +127,111 @@ def test_random_shape_parity(i):
     sl = np.where(o["slot"] >= 0, np.arange(N * K).reshape(N, K), -1).astype(np.int32)
     ref = oracle.combine(ye.reshape(-1, H), sl, wts if weighted else None)
     assert np.array_equal(bf16_to_bits(out), ref)
+
+
+def _compact(slot: np.ndarray):
+    """slot with the received rows renumbered 0..M-1 in slot order."""
+    flat = slot.reshape(-1)
+    m = flat >= 0
+    sc = np.full(flat.shape, -1, np.int32)
+    sc[m] = np.arange(int(m.sum()), dtype=np.int32)
+    return sc.reshape(slot.shape)
+
+
+EXTRA = 16
+
+
+@pytest.mark.parametrize("i", range(EXTRA))
+def test_random_shape_rank_round_trip_split(i):
+    """The other calls at the same kind of shapes: the rank-deduplicated
+    layout with its dispatch and combine, the chunked round trip
+    (dispatch -> identity expert -> combine) and the split send / receive-hook
+    dispatch and combine."""
+    rng, idx, E, Tmax, H, fp8, packed, weighted = _case(CASES + i)
+    R, T, K = idx.shape
+    N = R * T
+    lay = 1 if packed else 0
+    o = oracle.layout(idx, E, Tmax, lay)
+    want_status = ep.EP_ERR_CAPACITY if o["n_overflow"] > 0 else ep.EP_OK
+    scale = np.exp(rng.uniform(np.log(1e-2), np.log(1e2), size=(N, 1)))
+    xb = _bf16_bits(rng.standard_normal((N, H)) * scale)
+    wts = rng.random((N, K)).astype(np.float32)
+    ye = _bf16_bits(rng.standard_normal((N, K, H)))
+    hook_sms = int(rng.choice([0, 3]))
+    buf = Buffer(R, Tmax, H, E, K, low_latency_mode=not packed, num_hook_sms=hook_sms)
+    x = bits_to_bf16(xb.reshape(R, T, H))
+    idx_d = torch.from_numpy(idx).cuda()
+    wts_d = torch.from_numpy(wts).cuda()
+    wd = wts_d if weighted else None
+    wref = wts if weighted else None
+    tokens = np.arange(N)
+
+    # rank-deduplicated layout, its dispatch and its (unweighted) combine
+    ro = oracle.rank_layout(idx, wts, E, Tmax, lay)
+    ntr, ridx, rw, hr = buf.get_rank_layout(idx_d, wts_d)
+    assert buf.device_status() == ep.EP_OK
+    rslot = ro["rank_slot"]
+    rrows = rslot[rslot >= 0]
+    assert np.array_equal(hr.tensors()["slot"].cpu().numpy(), rslot)
+    assert np.array_equal(ntr.cpu().numpy(), ro["tokens_per_rank"])
+    assert np.array_equal(hr.tensors()["src_info"].cpu().numpy()[rrows], ro["src_info"][rrows])
+    assert np.array_equal(ridx.cpu().numpy()[rrows], ro["recv_topk_idx"][rrows])
+    assert np.array_equal(rw.cpu().numpy()[rrows].view(np.uint32), ro["recv_topk_weights"][rrows].view(np.uint32))
+    recv, sc = buf.alloc_rank_recv(fp8)
+    buf.low_latency_dispatch(x, None, Tmax, E, use_fp8=fp8, handle=hr, out=(recv, sc))
+    assert buf.device_status() == ep.EP_OK
+    g_of = np.nonzero(rslot.reshape(-1) >= 0)[0] // K
+    rrows_d = torch.from_numpy(rrows.astype(np.int64)).cuda()
+    if fp8:
+        q, s = oracle.quant_token(xb)
+        assert np.array_equal(e4m3_to_bits(recv.view(torch.uint8)[rrows_d]), q[g_of])
+        assert np.array_equal(sc[rrows_d].cpu().numpy().view(np.uint32), s[g_of].view(np.uint32))
+    else:
+        assert np.array_equal(bf16_to_bits(recv[rrows_d]), xb[g_of])
+    if N > 0:
+        yr = place_rows(buf.rank_rows, H, rslot, ye, tokens)
+        out = buf.low_latency_combine(yr, None, None, hr, E)
+        assert buf.device_status() == ep.EP_OK
+        sl = np.where(rslot >= 0, np.arange(N * K).reshape(N, K), -1).astype(np.int32)
+        assert np.array_equal(bf16_to_bits(out), oracle.combine(ye.reshape(-1, H), sl, None))
+    del recv, sc
+
+    # round trip over chunks (identity expert), against the oracle's
+    # dispatch -> dequant_rows -> combine on the received rows
+    chunk = int(rng.choice([0, -1, int(rng.integers(1, max(N, 1) + 1))]))
+    out, h = buf.round_trip(x, idx_d, wd, use_fp8=fp8, chunk_tokens=chunk)
+    assert buf.device_status() == want_status
+    assert tuple(out.shape) == (N, H)
+    csl = _compact(o["slot"])
+    m = int((csl >= 0).sum())
+    if fp8:
+        q, s = oracle.dispatch(xb, csl, m, True)
+        y = oracle.dequant_rows(q, s, csl)
+    else:
+        y = oracle.dispatch(xb, csl, m, False)
+    assert np.array_equal(bf16_to_bits(out), oracle.combine(y, csl, wref))
+
+    # split dispatch and combine (FP8 rows of a multiple of 512 channels)
+    if fp8 and H % 512 != 0:
+        return
+    (res, cnt, hs, hook) = buf.low_latency_dispatch(x, idx_d, Tmax, E, use_fp8=fp8, return_recv_hook=True)
+    hook()
+    assert buf.device_status() == want_status
+    assert np.array_equal(cnt.cpu().numpy(), o["tokens_per_expert"])
+    rows = valid_rows(o["slot"])
+    rows_d = torch.from_numpy(rows.astype(np.int64)).cuda()
+    g_of = np.nonzero(o["slot"].reshape(-1) >= 0)[0] // K
+    if fp8:
+        recv, sc = res
+        q, s = oracle.quant_token(xb)
+        assert np.array_equal(e4m3_to_bits(recv.view(torch.uint8)[rows_d]), q[g_of])
+        assert np.array_equal(sc[rows_d].cpu().numpy().view(np.uint32), s[g_of].view(np.uint32))
+    else:
+        assert np.array_equal(bf16_to_bits(res[rows_d]), xb[g_of])
+    if N > 0:
+        ys = place_rows(o["rows"], H, o["slot"], ye, tokens)
+        out, hook = buf.low_latency_combine(ys, None, wd, hs, E, return_recv_hook=True)
+        hook()
+        assert buf.device_status() == ep.EP_OK
+        sl = np.where(o["slot"] >= 0, np.arange(N * K).reshape(N, K), -1).astype(np.int32)
+        assert np.array_equal(bf16_to_bits(out), oracle.combine(ye.reshape(-1, H), sl, wref))
