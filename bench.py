@@ -82,15 +82,22 @@ def _sha(path):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def _peaks():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def _peaks(path=None):
+    """(HBM copy bandwidth in GB/s, "measured" | "fallback").  The measured
+    file may hold the number directly or in an object (its burst figure:
+    these kernels are timed alone or inside sub-millisecond steps)."""
+    p = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         try:
-            d = json.load(open(p))
+            with open(p) as f:
+                d = json.load(f)
             for k in ("hbm_gbs", "hbm_GBps", "hbm"):
-                if k in d:
-                    return float(d[k]), "measured"
-        except Exception:
+                v = d.get(k)
+                if isinstance(v, dict):
+                    v = next((v[j] for j in ("burst", "value", "gbs") if j in v), None)
+                if v is not None and float(v) > 0:
+                    return float(v), "measured"
+        except (OSError, ValueError, TypeError, AttributeError):
             pass
     return FALLBACK_HBM_GBS, "fallback"
 

@@ -39,3 +39,18 @@ def test_skew_and_identity_bytes():
     assert (_mb(disp), _mb(comb)) == (275.5, 470.2)
     # identity expert at ll: read codes + scales, write bf16 rows, read slots
     assert bench._identity_bytes(wl.LL, 32768) == 32768 * (7168 + 56 * 4) + 32768 * 7168 * 2 + 4096 * 8 * 4
+
+
+def test_peak_lookup(tmp_path):
+    """The roofline denominator: the measured copy bandwidth when the file
+    holds one (as a number or an object with a burst figure), else the
+    fallback, which is said."""
+    p = tmp_path / "peaks.json"
+    assert bench._peaks(str(p)) == (bench.FALLBACK_HBM_GBS, "fallback")
+    p.write_text('{"hbm_gbs": 7012.5, "bf16_tflops": 1900}')
+    assert bench._peaks(str(p)) == (7012.5, "measured")
+    p.write_text('{"hbm_gbs": {"burst": 7100, "sustained": 6900}}')
+    assert bench._peaks(str(p)) == (7100.0, "measured")
+    for bad in ('{"hbm_gbs": null}', '{"hbm_gbs": "n/a"}', "not json", "[1, 2]", '{"hbm_gbs": 0}'):
+        p.write_text(bad)
+        assert bench._peaks(str(p)) == (bench.FALLBACK_HBM_GBS, "fallback")
