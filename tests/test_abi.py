@@ -28,6 +28,52 @@ def test_header_declares_entry_points():
     assert _declared() == sorted(ep.ENTRY_POINTS)
 
 
+def _prototypes():
+    """{name: (return type, [(parameter type, parameter name)])} of every
+    entry point, parsed from the header (comments removed)."""
+    text = re.sub(r"/\*.*?\*/", " ", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"^\s*(const\s+char\s*\*|ep_status)\s*(ep_\w+)\s*\(([^)]*)\)\s*;", text, re.M):
+        params = []
+        for a in " ".join(m.group(3).split()).split(","):
+            a = a.strip()
+            name = re.findall(r"(\w+)$", a)[0]
+            params.append((a[: -len(name)].replace(" ", ""), name))
+        out[m.group(2)] = (m.group(1).replace(" ", ""), params)
+    return out
+
+
+def _ctype_of(ctype: str, name: str):
+    """The ctypes type a C parameter must be bound with: device pointers
+    (d_*), streams and opaque context / handle pointers pass as void*, host
+    out-parameters and structs as typed pointers."""
+    base = ctype.replace("const", "")
+    stars = base.count("*")
+    base = base.replace("*", "")
+    scalars = {"int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64, "uint64_t": ctypes.c_uint64}
+    structs = {"ep_config": ep.ep_config, "ep_handle_info": ep.ep_handle_info, "ep_tuning": ep.ep_tuning,
+               "ep_tune_record": ep.ep_tune_record}
+    if stars == 0:
+        return scalars[base]
+    if stars == 2:  # ep_ctx ** / ep_handle **: an opaque pointer written back
+        return ctypes.POINTER(ctypes.c_void_p)
+    if name.startswith("d_") or base in ("void", "ep_ctx", "ep_handle"):
+        return ctypes.c_void_p
+    if base in structs:
+        return ctypes.POINTER(structs[base])
+    return ctypes.POINTER(scalars[base])
+
+
+def test_binding_signatures_match_header(lib):
+    protos = _prototypes()
+    assert sorted(protos) == sorted(ep.ENTRY_POINTS)
+    for name, (ret, params) in protos.items():
+        fn = getattr(lib, name)
+        assert fn.restype == (ctypes.c_char_p if ret.startswith("const") else ctypes.c_int32), name
+        want = [_ctype_of(t, n) for t, n in params]
+        assert list(fn.argtypes) == want, (name, [n for _, n in params])
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared():
         assert hasattr(lib, name), name
