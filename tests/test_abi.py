@@ -216,3 +216,32 @@ def test_receive_row_counts_match_the_definitions_and_the_oracle(lib):
                 assert rows == R * Tmax * K and rank_rows == R * Tmax * min(K, R)
             assert rows == oracle.recv_rows(R, Tmax, E, K, layout)
             assert rank_rows == oracle.rank_recv_rows(R, Tmax, K, layout)
+
+
+def test_struct_layouts_match_header(tmp_path):
+    """The binding's ctypes structures have the sizes and field offsets the C
+    compiler gives the header's structs."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("needs gcc")
+    structs = {"ep_config": ep.ep_config, "ep_tuning": ep.ep_tuning,
+               "ep_tune_record": ep.ep_tune_record, "ep_handle_info": ep.ep_handle_info}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "ep.h"', "int main(void) {"]
+    for s, cls in structs.items():
+        lines.append(f'    printf("{s} size %zu\\n", sizeof({s}));')
+        for f, _ in cls._fields_:
+            lines.append(f'    printf("{s} {f} %zu\\n", offsetof({s}, {f}));')
+    lines += ["    return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines():
+        s, f, v = line.split()
+        got[(s, f)] = int(v)
+    for s, cls in structs.items():
+        assert got[(s, "size")] == ctypes.sizeof(cls), s
+        for f, _ in cls._fields_:
+            assert got[(s, f)] == getattr(cls, f).offset, (s, f)
