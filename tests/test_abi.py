@@ -245,3 +245,19 @@ def test_struct_layouts_match_header(tmp_path):
         assert got[(s, "size")] == ctypes.sizeof(cls), s
         for f, _ in cls._fields_:
             assert got[(s, f)] == getattr(cls, f).offset, (s, f)
+
+
+def test_c_program_uses_the_abi(lib, tmp_path):
+    """A plain C11 program compiled against include/ep.h and linked with
+    libep.so makes the calls that need no GPU (tests/c/abi_host.c)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("needs gcc")
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "c", "abi_host.c")
+    libdir = os.path.dirname(ep._LIB_PATH)
+    exe = tmp_path / "abi_host"
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.dirname(HEADER), src,
+                    "-L", libdir, "-l:libep.so", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
