@@ -14,7 +14,11 @@ What each function computes follows the DeepEP pages:
 "如何突破MoE通信瓶颈：DeepEP跨节点优化技术终极指南" (section 技术解析) says is
 computed once and reused; ``dispatch``/``quant_token`` — low_latency_dispatch
 with the optional FP8 cast (section 核心API示例 and 核心优势 of the same page);
-``combine`` — low_latency_combine's top-k weighted reduce to BF16 (same sections).
+``combine`` — low_latency_combine's top-k weighted reduce to BF16 (same sections);
+``rank_layout`` / ``rank_runs`` — the rank-deduplicated transport of the normal
+kernels (DeepTech announcement of DeepEP, 010bt.com) and its per-(source rank,
+destination rank) runs, which a receive that occupies no SM copies whole
+(section 技术解析, 通信-计算重叠技术, of the first page).
 """
 from __future__ import annotations
 
@@ -74,6 +78,8 @@ def use_library(path: str | None):
                                P, P, P, P, P, P, P, P, I64, P]
     lib.orc_rank_layout.restype = None
     lib.orc_rank_layout.argtypes = [I32, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, I64]
+    lib.orc_rank_runs.restype = ctypes.c_int64
+    lib.orc_rank_runs.argtypes = [I32, I32, I32, I32, P, P, P, P, P, P]
     lib.orc_quant_block.argtypes = [P, P, P]
     lib.orc_quant_token.argtypes = [P, I32, P, P]
     lib.orc_dispatch.argtypes = [I64, I32, I32, I32, P, P, P, P]
@@ -191,6 +197,23 @@ def rank_layout(topk_idx: np.ndarray, topk_weights: np.ndarray | None, num_exper
                             _p(out["tokens_per_rank"]), _p(out["rbase"]), _p(out["src_info"]),
                             _p(out["recv_topk_idx"]), _p(out["recv_topk_weights"]), rows)
     out["rows"] = rows
+    return out
+
+
+def rank_runs(topk_idx: np.ndarray, num_experts: int, rbase: np.ndarray) -> dict:
+    """Runs of the rank-deduplicated transport (topk_idx [R, T, K], rbase [R]
+    from rank_layout): send_slot [N, K] (row of the carrying entry in the send
+    buffer ordered by source rank, destination rank, token; else -1),
+    run_cnt [R, R] (tokens source r carries to rank d), send_off [R, R],
+    recv_off [R, R] (first send / receive row of each run), send_rows."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    R, T, K = idx.shape
+    rb = np.ascontiguousarray(rbase, dtype=np.int64)
+    assert rb.shape == (R,)
+    out = dict(send_slot=np.zeros((R * T, K), np.int32), run_cnt=np.zeros((R, R), np.int32),
+               send_off=np.zeros((R, R), np.int64), recv_off=np.zeros((R, R), np.int64))
+    out["send_rows"] = int(_load().orc_rank_runs(R, T, K, int(num_experts), _p(idx), _p(rb), _p(out["send_slot"]),
+                                                _p(out["run_cnt"]), _p(out["send_off"]), _p(out["recv_off"])))
     return out
 
 

@@ -352,6 +352,88 @@ void orc_rank_layout(int R, int T, int Tmax, int K, int E, int layout,
 }
 
 /* ------------------------------------------------------------------ */
+/* Per-(source rank, destination rank) runs of the rank-deduplicated      */
+/* transport  [API] section 技术解析 (hook-based overlap that occupies no   */
+/* SM; CPU and GPU cooperating on the layout); [ANN] normal kernels:      */
+/* tokens forwarded per destination domain                               */
+/* ------------------------------------------------------------------ */
+
+/*
+ * A source rank r sends its tokens carried to rank d as one contiguous run.
+ * Send buffer order: source rank r ascending, then destination d ascending,
+ * then token t ascending (the token's carrying entry is its first k whose
+ * expert lives on d, as in orc_rank_layout).  In the receive layout of
+ * orc_rank_layout the rows of rank d hold its tokens in ascending g = r*T + t,
+ * so the tokens rank d gets from source r are one contiguous run there too.
+ *   run_cnt[r*R + d]   tokens of source rank r carried to rank d
+ *   send_off[r*R + d]  first send row of the run: sum of run_cnt over the
+ *                      (r', d') before (r, d) in r-major order
+ *   recv_off[r*R + d]  first receive row of the run: rbase[d] plus the sum of
+ *                      run_cnt[r'*R + d] over r' < r
+ *   send_slot[g*K + k] send row of the carrying entry (g, k), else -1
+ * Copying run_cnt rows from send_off to recv_off for every (r, d) puts every
+ * token's row where orc_rank_layout's rank_slot says.  Ids outside [0, E)
+ * carry nothing.  Returns the number of send rows (the sum of run_cnt).
+ */
+int64_t orc_rank_runs(int R, int T, int K, int E, const int64_t *topk_idx, const int64_t *rbase,
+                      int32_t *send_slot, int32_t *run_cnt, int64_t *send_off, int64_t *recv_off)
+{
+    int64_t N = (int64_t)R * T;
+    int L = E / R;
+    for (int64_t i = 0; i < N * K; i++)
+        send_slot[i] = -1;
+    for (int i = 0; i < R * R; i++)
+        run_cnt[i] = 0;
+    /* carrying entry of token g for rank d: its first k with an expert on d */
+    for (int64_t g = 0; g < N; g++) {
+        int src = (int)(g / T); /* source rank of token g */
+        for (int k = 0; k < K; k++) {
+            int64_t e = topk_idx[g * K + k];
+            if (e < 0 || e >= E)
+                continue;
+            int d = (int)(e / L), first = 1;
+            for (int k2 = 0; k2 < k; k2++) {
+                int64_t e2 = topk_idx[g * K + k2];
+                if (e2 >= 0 && e2 < E && e2 / L == d)
+                    first = 0;
+            }
+            if (first)
+                run_cnt[src * R + d]++;
+        }
+    }
+    int64_t acc = 0;
+    for (int r = 0; r < R; r++)
+        for (int d = 0; d < R; d++) {
+            send_off[r * R + d] = acc;
+            acc += run_cnt[r * R + d];
+        }
+    for (int d = 0; d < R; d++) {
+        int64_t run = rbase[d];
+        for (int r = 0; r < R; r++) {
+            recv_off[r * R + d] = run;
+            run += run_cnt[r * R + d];
+        }
+    }
+    /* send rows: r, then d, then t ascending */
+    for (int r = 0; r < R; r++)
+        for (int d = 0; d < R; d++) {
+            int64_t row = send_off[r * R + d];
+            for (int t = 0; t < T; t++) {
+                int64_t g = (int64_t)r * T + t;
+                for (int k = 0; k < K; k++) {
+                    int64_t e = topk_idx[g * K + k];
+                    if (e >= 0 && e < E && (int)(e / L) == d) {
+                        send_slot[g * K + k] = (int32_t)row;
+                        row++;
+                        break; /* later k on d are not carrying entries */
+                    }
+                }
+            }
+        }
+    return acc;
+}
+
+/* ------------------------------------------------------------------ */
 /* FP8 cast  [ANN] native FP8 dispatch; [LL] FP8 dispatch               */
 /* ------------------------------------------------------------------ */
 

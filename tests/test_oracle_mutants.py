@@ -100,6 +100,18 @@ MUTANTS = {
     "combine: NULL weights read as 0": (
         "float wk = w ? w[g * K + k] : 1.0f;",
         "float wk = w ? w[g * K + k] : 0.0f;"),
+    "rank runs: send offsets in destination-major order": (
+        "    for (int r = 0; r < R; r++)\n        for (int d = 0; d < R; d++) {\n            send_off[r * R + d] = acc;",
+        "    for (int d = 0; d < R; d++)\n        for (int r = 0; r < R; r++) {\n            send_off[r * R + d] = acc;"),
+    "rank runs: receive offsets without the rank's base": (
+        "int64_t run = rbase[d];",
+        "int64_t run = 0;"),
+    "rank runs: every entry on a rank gets a send row": (
+        "                        break; /* later k on d are not carrying entries */\n",
+        ""),
+    "rank runs: tokens in descending order within a run": (
+        "            for (int t = 0; t < T; t++) {\n                int64_t g = (int64_t)r * T + t;",
+        "            for (int t = T - 1; t >= 0; t--) {\n                int64_t g = (int64_t)r * T + t;"),
 }
 
 
@@ -111,6 +123,9 @@ def _pins():
     for f in cheap:
         yield f.__name__, (lambda f=f: f(oracle))
     yield "rank_golden", lambda: pins.test_rank_layout_golden(oracle)
+    yield "rank_runs_golden", lambda: pins.test_rank_runs_golden(oracle)
+    for seed in range(10):
+        yield f"rank_runs_brute_force[{seed}]", (lambda seed=seed: pins.test_rank_runs_brute_force(oracle, seed))
     for seed in range(30):
         yield f"brute_force[{seed}]", (lambda seed=seed: pins.test_layout_brute_force(oracle, seed))
     for seed in range(20):

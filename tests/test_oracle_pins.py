@@ -266,6 +266,94 @@ def test_rank_layout_brute_force(orc, seed):
         assert np.array_equal(o["tokens_per_rank"], orc.layout(idx, E, Tmax, lay)["tokens_per_rank"])
 
 
+def test_rank_runs_golden(orc):
+    g, _ = _read_golden("layout_small.txt")
+    iv = lambda k: np.array([int(v) for v in g[k][0]])
+    R, T, Tmax, K, E = (int(g[k][0][0]) for k in ("R", "T", "Tmax", "K", "E"))
+    idx = iv("topk_idx").reshape(R, T, K)
+    for lay, pfx in ((orc.LAYOUT_PACKED, "rank_packed"), (orc.LAYOUT_PADDED, "rank_padded")):
+        o = orc.rank_layout(idx, None, E, Tmax, lay)
+        r = orc.rank_runs(idx, E, o["rbase"])
+        assert np.array_equal(r["run_cnt"].ravel(), iv("rank_run_cnt"))
+        assert np.array_equal(r["send_off"].ravel(), iv("rank_send_off"))
+        assert np.array_equal(r["send_slot"].ravel(), iv("rank_send_slot"))
+        assert np.array_equal(r["recv_off"].ravel(), iv(pfx + "_recv_off"))
+        assert r["send_rows"] == int(iv("rank_run_cnt").sum())
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_rank_runs_brute_force(orc, seed):
+    """Send rows by enumeration (carried (token, rank) pairs sorted by source
+    rank, destination rank, token), and the run copies checked end to end:
+    copying every run from the send buffer to its receive rows puts each
+    token where the rank layout says."""
+    rng = np.random.default_rng(900 + seed)
+    R = int(rng.integers(1, 5))
+    L = int(rng.integers(1, 4))
+    E = R * L
+    Tmax = int(rng.integers(1, 6))
+    T = int(rng.integers(0, Tmax + 1))
+    K = int(rng.integers(1, 6))
+    idx = rng.integers(-1, E, size=(R, T, K))
+    N = R * T
+    flat = idx.reshape(N, K)
+    carry = {}
+    for gg in range(N):
+        for k in range(K):
+            e = flat[gg, k]
+            if 0 <= e < E and (gg, e // L) not in carry:
+                carry[(gg, e // L)] = k
+    pairs = sorted(carry, key=lambda p: (p[0] // max(T, 1), p[1], p[0]))  # (r, d, t)
+    cnt = np.zeros((R, R), np.int64)
+    for gg, d in pairs:
+        cnt[gg // T, d] += 1
+    send_off = np.concatenate([[0], np.cumsum(cnt.ravel())[:-1]]).reshape(R, R)
+    slot = np.full((N, K), -1)
+    for row, (gg, d) in enumerate(pairs):
+        slot[gg, carry[(gg, d)]] = row
+    for lay in (orc.LAYOUT_PACKED, orc.LAYOUT_PADDED):
+        o = orc.rank_layout(idx, None, E, Tmax, lay)
+        r = orc.rank_runs(idx, E, o["rbase"])
+        recv_off = o["rbase"][None, :] + np.concatenate([np.zeros((1, R), np.int64), np.cumsum(cnt, 0)[:-1]], 0)
+        assert np.array_equal(r["run_cnt"], cnt)
+        assert np.array_equal(r["send_off"], send_off)
+        assert np.array_equal(r["recv_off"], recv_off)
+        assert np.array_equal(r["send_slot"], slot)
+        assert r["send_rows"] == len(pairs)
+        # the copies: a token id per send row, moved run by run
+        send = np.full(max(len(pairs), 1), -1)
+        m = slot >= 0
+        send[slot[m]] = np.nonzero(m)[0]
+        recv = np.full(o["rows"], -1)
+        for a in range(R):
+            for d in range(R):
+                n = cnt[a, d]
+                recv[recv_off[a, d]:recv_off[a, d] + n] = send[send_off[a, d]:send_off[a, d] + n]
+        rs = o["rank_slot"]
+        assert np.array_equal(m, rs >= 0)
+        assert np.array_equal(recv[rs[m]], np.nonzero(m)[0])
+
+
+def test_rank_runs_carry_bytes(orc):
+    """BF16 rows dispatched into the send order and copied run by run equal
+    the rank layout's own dispatch, bit for bit (ragged T, masked entries)."""
+    w = wl.NORMAL.with_(tokens_per_rank=37, max_tokens_per_rank=40, hidden=256)
+    d = wl.generate(w)
+    idx = wl.inject_masks(d["topk_idx"], 0.1, 4)
+    x = d["x_bits"].reshape(w.num_tokens, w.hidden)
+    o = orc.rank_layout(idx, None, w.num_experts, w.max_tokens_per_rank)
+    r = orc.rank_runs(idx, w.num_experts, o["rbase"])
+    send = orc.dispatch(x, r["send_slot"], r["send_rows"], use_fp8=False)
+    recv = np.zeros((o["rows"], w.hidden), np.uint16)
+    R = w.num_ranks
+    for a in range(R):
+        for dd in range(R):
+            n = r["run_cnt"][a, dd]
+            so, ro = r["send_off"][a, dd], r["recv_off"][a, dd]
+            recv[ro:ro + n] = send[so:so + n]
+    assert np.array_equal(recv, orc.dispatch(x, o["rank_slot"], o["rows"], use_fp8=False))
+
+
 def test_rank_round_trip_bf16(orc):
     """Rank dispatch, an identity expert per rank that returns the token times
     the sum of its local weights, rank combine: weights summing to one give x
