@@ -9,7 +9,8 @@
 //
 // Two kernels.  For hidden sizes that are a multiple of 512 (all the
 // workloads) the row kernel below stages a whole token row in shared memory
-// and writes it with bulk asynchronous copies.  Otherwise the warp-item
+// and writes it with bulk asynchronous copies (producer warps and an issuer
+// warp handing buffers over through mbarriers).  Otherwise the warp-item
 // kernel does:
 // the work item is (token, 512-channel chunk) for one warp, 16
 // channels (two 16-byte loads) per lane.  The token row is read once from
@@ -18,7 +19,7 @@
 // nothing else.  A 128-channel FP8 block is 8 lanes: its amax is three xor
 // shuffles.  The kernel is launched with programmatic dependent launch behind
 // the layout kernel: each warp loads and casts its first chunk before
-// waiting for the slots.
+// waiting for the slots (x was written before the layout kernel started).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -59,6 +60,10 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const DispatchParams
         for (int e = threadIdx.x; e < p.E; e += kThreads) p.count_dst[e] = p.count_src[e];
     }
 
+    if (!p.early_x && !waited) {  // x may be the output of the kernel just before
+        pdl_wait();
+        waited = true;
+    }
     const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(p.x);
     for (int64_t it = warp; it < items; it += nwarp) {
         const int64_t g = it / nch;
@@ -120,23 +125,36 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const DispatchParams
 }
 
 // ---------------------------------------------------------------- row kernel
-// One CTA per token at a time (H/16 threads, 16 channels each): the row is
-// loaded once, cast once (FP8) and laid out in shared memory, then one
-// lane per top-k entry issues a bulk asynchronous copy (cp.async.bulk) of the
-// whole row (and of its scale row) to its receive row.  Each destination row is
-// written as one contiguous transfer by the copy engine instead of 512-byte
-// pieces from many warps.  NB row buffers form a ring, so the casts of the
-// next tokens overlap the copies of earlier ones; the rows of the next two
-// tokens are being loaded while the current one is cast.  Launched behind the layout kernel
-// (programmatic dependent launch), a CTA first casts up to NB of its tokens
-// into the ring and only then waits for the slots, so most of the layout's
-// run time is spent loading and casting rows.  Needs H % 512 == 0 and
-// H <= 16384.
+// One CTA per token at a time.  H/16 producer threads (16 channels each) and
+// one issuer warp.  The producers load the token row once (two tokens
+// ahead), cast it once (FP8) and lay it out in a shared-memory row buffer;
+// the issuer warp then has lane k < K copy the whole row (and its scale row)
+// to the receive row of entry k with one bulk asynchronous copy
+// (cp.async.bulk), so each destination row is one contiguous transfer by the
+// copy engine.  NB row buffers form a ring with two mbarriers each:
+//   full[b]   completes when every producer warp has written its part of the
+//             buffer (one arrival per warp, after a proxy fence that makes
+//             the writes visible to the copy engine);
+//   empty[b]  completes when the copies of the buffer's row have read it
+//             (the issuer's cp.async.bulk.wait_group.read, kLag tokens
+//             later), so the producers may refill it.
+// No CTA-wide barrier per token: the producer warps run up to NB - kLag
+// tokens ahead of the issuer and independently of one another.  Only the
+// issuer waits for the layout kernel before it (programmatic dependent
+// launch: it reads the slots); behind the library's own layout kernel the
+// producers fill the ring meanwhile (x was written before that kernel
+// started).  Every
+// mbarrier wait is bounded (about one second); if one gives up the kernel
+// sets kStatusTimeout, stops issuing, lets its copies finish and returns.
+// Needs H % 512 == 0 and H/16 + 32 <= 1024 threads.
 // CTAs per SM: about 1024 threads, at least 2 (measured best at H = 7168)
 int row_blocks_per_sm(int H) {
     const int b = 16384 / H;
     return b < 2 ? 2 : (b > 16 ? 16 : b);
 }
+
+constexpr int kLag = 2;                            // tokens the issuer lets its copies run before a release
+constexpr uint64_t kRowWaitNs = 1000000000ull;     // bound of one mbarrier wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -154,6 +172,34 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t now_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait for the phase with this parity; false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = now_ns();
+    while (!mbar_try(bar, parity))
+        if (now_ns() - t0 > kRowWaitNs) return false;
+    return true;
 }
 
 // FP8 cast of this thread's 16 channels (two 16-byte bf16 loads): codes and
@@ -197,33 +243,64 @@ __device__ __forceinline__ void put_row(uint8_t *row, int t, int H, uint4 ca, ui
     }
 }
 
-// Warp 0: the K copies of one row buffer.  Lane k < K holds slot k and
-// issues that copy (and its scale row) itself, as its own bulk group, so
-// the K copies are issued in parallel; every lane k < K commits one group
-// per row (empty for a masked entry) and waits for its own groups.
-template <bool FP8>
-__device__ __forceinline__ void send_row(const DispatchParams &p, int32_t my_slot, const uint8_t *row, int lane) {
-    const int H = p.H;
-    const int payload = FP8 ? H : 2 * H;
-    if (lane < p.K) {
-        if (my_slot >= 0) {
-            bulk_store(static_cast<uint8_t *>(p.recv) + (int64_t)my_slot * payload, smem_addr(row), payload);
-            if constexpr (FP8) bulk_store(p.recv_scales + (int64_t)my_slot * (H / 128), smem_addr(row + H), H / 32);
-        }
-        bulk_commit();
-    }
-}
-
 template <bool FP8, int NB>
 __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchParams p) {
     extern __shared__ __align__(128) uint8_t row_smem[];
+    __shared__ __align__(8) uint64_t full[NB], empty[NB];
     const int H = p.H, K = p.K;
     const int t = threadIdx.x, lane = t & 31;
+    const int np = H / 16;                      // producer threads; the issuer warp follows them
     const int rowb = FP8 ? H + H / 32 : 2 * H;  // bytes of one buffer
-    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(p.x);
     const int64_t G = gridDim.x;
+    if (t == 0) {
+        for (int b = 0; b < NB; ++b) {
+            mbar_init(smem_addr(&full[b]), (uint32_t)(np / 32));
+            mbar_init(smem_addr(&empty[b]), 1);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
 
-    // x rows are loaded two tokens ahead: (a, b) = this token, (a2, b2) = the next
+    if (t >= np) {
+        // ------------------------------------------------ issuer warp
+        pdl_wait();  // slots (and counts) of the layout kernel
+        if (p.count_dst != nullptr && blockIdx.x == 0)
+            for (int e = lane; e < p.E; e += 32) p.count_dst[e] = p.count_src[e];
+        const int payload = FP8 ? H : 2 * H;
+        int64_t g = blockIdx.x;
+        int32_t s0 = g < p.N ? slot_of(p, g, lane) : -1;          // this token's slots,
+        int32_t s1 = g + G < p.N ? slot_of(p, g + G, lane) : -1;  // and the next one's
+        bool ok = true;
+        for (int it = 0; g < p.N; ++it, g += G) {
+            const int b = it % NB;
+            const int32_t my_slot = s0;
+            s0 = s1;
+            s1 = g + 2 * G < p.N ? slot_of(p, g + 2 * G, lane) : -1;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&full[b]), (uint32_t)((it / NB) & 1)))) {
+                ok = false;
+                break;
+            }
+            const uint8_t *row = row_smem + b * rowb;
+            if (lane < K) {
+                if (my_slot >= 0) {
+                    bulk_store(static_cast<uint8_t *>(p.recv) + (int64_t)my_slot * payload, smem_addr(row), payload);
+                    if constexpr (FP8)
+                        bulk_store(p.recv_scales + (int64_t)my_slot * (H / 128), smem_addr(row + H), H / 32);
+                }
+                bulk_commit();
+                bulk_wait_read<kLag>();  // the copies of token it - kLag have read their buffer
+            }
+            __syncwarp();
+            if (lane == 0 && it >= kLag) mbar_arrive(smem_addr(&empty[(it - kLag) % NB]));
+        }
+        if (!ok && lane == 0 && p.status != nullptr) atomicOr(p.status, kStatusTimeout);
+        if (lane < K) bulk_wait_all();  // copies read shared memory until they finish
+        return;
+    }
+
+    // ---------------------------------------------------- producer warps
+    if (!p.early_x) pdl_wait();  // x may be the output of the kernel just before
+    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(p.x);
     int64_t g = blockIdx.x;
     uint4 a = make_uint4(0, 0, 0, 0), b = a, a2 = a, b2 = a;
     if (g < p.N) {
@@ -234,72 +311,31 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
         a2 = ld_nc_na_v4(x + (g + G) * H + t * 16);
         b2 = ld_nc_na_v4(x + (g + G) * H + t * 16 + 8);
     }
-
-    // 1. Before the slots exist: cast up to `pre_max` tokens into the ring.
-    const int pre_max = p.prestage < NB ? p.prestage : NB;
-    int pre = 0;
-    for (; pre < pre_max && g < p.N; ++pre) {
+    for (int it = 0; g < p.N; ++it, g += G) {
         const uint4 ca = a, cb = b;
-        const int64_t gn = g + G;
         a = a2;
         b = b2;
-        if (gn + G < p.N) {
-            a2 = ld_nc_na_v4(x + (gn + G) * H + t * 16);
-            b2 = ld_nc_na_v4(x + (gn + G) * H + t * 16 + 8);
+        if (g + 2 * G < p.N) {
+            a2 = ld_nc_na_v4(x + (g + 2 * G) * H + t * 16);
+            b2 = ld_nc_na_v4(x + (g + 2 * G) * H + t * 16 + 8);
         }
         uint4 q = make_uint4(0, 0, 0, 0);
         float scale = 0.0f;
         if constexpr (FP8) cast16(ca, cb, q, scale);
-        put_row<FP8>(row_smem + pre * rowb, t, H, ca, cb, q, scale);
-        g = gn;
-    }
-    fence_proxy_async_smem();  // make the rows visible to the copy engine
-    pdl_wait();                // slots (and counts) of the layout kernel
-    if (p.count_dst != nullptr && blockIdx.x == 0)
-        for (int e = t; e < p.E; e += blockDim.x) p.count_dst[e] = p.count_src[e];
-    __syncthreads();
-    if (t < 32) {
-        int32_t my_slot[NB];  // all staged tokens' slots in flight at once
-#pragma unroll
-        for (int j = 0; j < NB; ++j)
-            my_slot[j] = j < pre ? slot_of(p, (int64_t)blockIdx.x + (int64_t)j * G, lane) : -1;
-#pragma unroll
-        for (int j = 0; j < NB; ++j)
-            if (j < pre) send_row<FP8>(p, my_slot[j], row_smem + j * rowb, lane);
-    }
-
-    // 2. The remaining tokens through the ring (one bulk group per token);
-    // each token's slots are loaded one token ahead.
-    int32_t slot_next = g < p.N ? slot_of(p, g, t) : -1;
-    for (int it = pre; g < p.N; ++it) {
-        uint8_t *row = row_smem + (it % NB) * rowb;
-        const uint4 ca = a, cb = b;
-        const int64_t gn = g + G;
-        a = a2;
-        b = b2;
-        if (gn + G < p.N) {
-            a2 = ld_nc_na_v4(x + (gn + G) * H + t * 16);
-            b2 = ld_nc_na_v4(x + (gn + G) * H + t * 16 + 8);
+        const int buf = it % NB;
+        // the buffer's previous row (NB tokens ago) must have been read
+        if (it >= NB && !__all_sync(0xFFFFFFFFu, mbar_wait(smem_addr(&empty[buf]), (uint32_t)((it / NB - 1) & 1)))) {
+            if (lane == 0 && p.status != nullptr) atomicOr(p.status, kStatusTimeout);
+            return;
         }
-        const int32_t my_slot = slot_next;
-        if (gn < p.N) slot_next = slot_of(p, gn, t);
-        uint4 q = make_uint4(0, 0, 0, 0);
-        float scale = 0.0f;
-        if constexpr (FP8) cast16(ca, cb, q, scale);
-        // this buffer was last filled NB tokens ago: its copies (one group
-        // per lane k < K and token) must have read it
-        if (t < K) bulk_wait_read<NB - 1>();
-        __syncthreads();
-        put_row<FP8>(row, t, H, ca, cb, q, scale);
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (t < 32) send_row<FP8>(p, my_slot, row, lane);
-        g = gn;
+        put_row<FP8>(row_smem + buf * rowb, t, H, ca, cb, q, scale);
+        fence_proxy_async_smem();  // make the writes visible to the copy engine
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&full[buf]));
     }
-    if (t < K) bulk_wait_all();  // copies read shared memory until they finish
 }
 
-bool row_kernel_fits(int H) { return H % 512 == 0 && H / 16 <= 1024; }
+bool row_kernel_fits(int H) { return H % 512 == 0 && H / 16 + 32 <= 1024; }
 
 size_t row_smem_bytes(bool fp8, int H) { return 2 * (size_t)(fp8 ? H + H / 32 : 2 * H); }
 
@@ -333,10 +369,21 @@ int g_smem_per_block = 0;     // largest dynamic shared memory of one CTA
 size_t row_smem_for_occupancy(bool fp8, int H, int blocks) {
     const size_t need = row_smem_bytes(fp8, H);
     if (g_smem_per_sm <= 0) return need;
-    const int64_t cap = (int64_t)g_smem_per_sm / (blocks + 1) - g_smem_reserved + 16;
+    const int64_t cap = (int64_t)g_smem_per_sm / (blocks + 1) - g_smem_reserved + 16;  // (static: 16 * NB bytes)
     size_t s = cap > (int64_t)need ? (size_t)cap : need;
     s = (s + 15) / 16 * 16;
     return s > (size_t)g_smem_per_block ? need : s;
+}
+}  // namespace
+
+namespace {
+// The most dynamic shared memory a kernel may ask for: the opt-in limit less
+// its static shared memory (the row kernel's mbarriers).
+template <typename F>
+void allow_smem(F kernel) {
+    cudaFuncAttributes fa;
+    const int st = cudaFuncGetAttributes(&fa, kernel) == cudaSuccess ? (int)fa.sharedSizeBytes : 1024;
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block - st);
 }
 }  // namespace
 
@@ -347,12 +394,12 @@ void dispatch_init() {
     cudaDeviceGetAttribute(&g_smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     cudaDeviceGetAttribute(&g_smem_per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     // the row kernel asks for more than the 48 KB default (see above)
-    cudaFuncSetAttribute(dispatch_row_kernel<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
-    cudaFuncSetAttribute(dispatch_row_kernel<false, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
-    cudaFuncSetAttribute(dispatch_row_kernel<false, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
-    cudaFuncSetAttribute(dispatch_row_kernel<true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
-    cudaFuncSetAttribute(dispatch_row_kernel<true, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
-    cudaFuncSetAttribute(dispatch_row_kernel<true, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_per_block);
+    allow_smem(dispatch_row_kernel<false, 2>);
+    allow_smem(dispatch_row_kernel<false, 4>);
+    allow_smem(dispatch_row_kernel<false, 8>);
+    allow_smem(dispatch_row_kernel<true, 2>);
+    allow_smem(dispatch_row_kernel<true, 4>);
+    allow_smem(dispatch_row_kernel<true, 8>);
     cudaGetLastError();
 }
 
@@ -386,16 +433,14 @@ cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks, b
         if (blocks < 1) blocks = 1;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)blocks, 1, 1);
-        cfg.blockDim = dim3(p.H / 16, 1, 1);
+        cfg.blockDim = dim3(p.H / 16 + 32, 1, 1);
         const size_t smem = row_smem_for_occupancy(fp8, p.H, bps);
         const int nb = ring_buffers(fp8, p.H, smem);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = pdl ? 1 : 0;
-        DispatchParams q = p;
-        if (q.prestage < 1) q.prestage = 1;
-        return fp8 ? launch_row<true>(cfg, nb, q) : launch_row<false>(cfg, nb, q);
+        return fp8 ? launch_row<true>(cfg, nb, p) : launch_row<false>(cfg, nb, p);
     }
     const int nch = (p.H + kChunk - 1) / kChunk;
     const int64_t warps = p.N * nch;

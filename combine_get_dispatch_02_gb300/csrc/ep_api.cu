@@ -1,8 +1,11 @@
 // Host side of libep.so: the C ABI declared in include/ep.h — argument checks,
-// context / handle management and kernel launches.  No call here synchronises
-// the host except ep_get_device_status and ep_autotune, and none allocates
-// except ep_create / ep_handle_create / ep_autotune, so a dispatch + combine
-// sequence can be captured in a CUDA graph.
+// context / handle management, kernel launches and the copy-engine copies of
+// the rank transport.  No call here synchronises the host except
+// ep_get_device_status, ep_autotune and the first use of a new rank
+// layout's run sizes (ep_rank_dispatch_recv / ep_rank_combine_send /
+// ep_rank_runs), and none allocates except ep_create / ep_handle_create /
+// ep_autotune, so a dispatch + combine sequence can be captured in a CUDA
+// graph.
 #include <limits.h>
 #include <stdlib.h>
 #include <string.h>
@@ -15,6 +18,11 @@
 
 #include "ep.h"
 #include "ep_internal.cuh"
+
+namespace {
+constexpr int kCeStreams = 2;  // device wire: copies spread over two streams (measured: 1 stream 2.5,
+                               // 2 streams 3.4 TB/s of 29 MB copies)
+}
 
 struct ep_ctx {
     ep_config cfg;
@@ -37,6 +45,13 @@ struct ep_ctx {
     int combine_bps_tuned; // resident combine CTAs per SM for tune.combine_chunks
     ep_tune_record tune_log[16];  // the candidates the last ep_autotune timed
     int tune_log_n;
+    ep_test_hooks hooks;   // test-only switches (ep_set_test_hooks)
+    // copy-engine streams of the rank transport, forked from and joined back
+    // into the caller's stream around each call's copies
+    cudaStream_t ce_stream[kCeStreams];
+    cudaEvent_t ce_fork;
+    cudaEvent_t ce_join[kCeStreams];
+    cudaEvent_t ce_rank[ep::kRankRunsMaxRanks];  // host wire: source rank r's first leg has landed
 };
 
 struct ep_handle {
@@ -52,11 +67,29 @@ struct ep_handle {
     int32_t rank_mode;        // the layout is rank-deduplicated (keys are ranks)
     int32_t num_keys;         // experts, or ranks in rank mode
     int32_t *cta_hist;        // grid-form layout: [num_sms][max(E, R)] per-CTA key totals
+    // rank transport (ep_rank_dispatch_send): send row of each carrying entry,
+    // and the per-(destination, source) run sizes copied to the host
+    int32_t *send_slot;       // [R*Tmax*K]
+    int32_t *h_runs;          // pinned host [R*R] (R <= kRankRunsMaxRanks), h_runs[d*R + r]
+    cudaEvent_t runs_ev;      // recorded after the copy of the run sizes to h_runs
+    int32_t runs_state;       // 0: none, 1: copy queued (wait on runs_ev), 2: on the host
+    int32_t has_send;         // send_slot / runs belong to the layout held
 };
 
 namespace {
 
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// A new layout in the handle: the rank transport's send rows and runs no
+// longer belong to it.
+void forget_send(ep_handle *h) {
+    h->has_send = 0;
+    if (h->runs_state == 1) {  // a copy into h_runs may still be queued: let it land first
+        cudaEventSynchronize(h->runs_ev);
+        cudaGetLastError();
+    }
+    h->runs_state = 0;
+}
 
 // NVTX range around each enqueueing call (free unless a profiler is attached)
 struct NvtxRange {
@@ -85,6 +118,13 @@ ep_status check_config(const ep_config *c) {
 int64_t rows_of(const ep_config *c) {
     const int64_t n = (int64_t)c->num_ranks * c->max_tokens_per_rank;
     return c->layout == EP_LAYOUT_PADDED ? n * c->num_experts : n * c->topk;
+}
+
+// Ints of a handle's per-CTA key totals of the grid-form layout (the grid
+// barrier's counter follows them).
+size_t grid_hist_ints(const ep_ctx *ctx) {
+    const ep_config &c = ctx->cfg;
+    return (size_t)ctx->num_sms * (c.num_experts > c.num_ranks ? c.num_experts : c.num_ranks);
 }
 
 bool on_ctx_device(const ep_ctx *ctx) {
@@ -150,6 +190,7 @@ ep_status enqueue_layout(ep_ctx *ctx, const int64_t *topk_idx, int32_t T, int32_
     p.tokens_per_rank = tokens_per_rank;
     p.is_token_in_rank = is_token_in_rank;
     p.status = ctx->d_status;
+    forget_send(h);
     h->tokens_per_rank = -1;  // until the launches are in: a failed one may have overwritten part of the layout
     const cudaError_t err = launch_layout_any(ctx, p, h, stream);
     if (err != cudaSuccess) {
@@ -172,11 +213,11 @@ int64_t rank_rows_of(const ep_config *c) {
 // The dispatch kernel over tokens [g0, g1) of the handle's layout (g1 > g0).
 ep_status enqueue_dispatch(ep_ctx *ctx, const ep_handle *h, const void *x, int64_t g0, int64_t g1, bool fp8,
                            void *recv, float *recv_scales, int32_t *count_dst, bool behind_layout,
-                           cudaStream_t st, bool identity_rows = false) {
+                           cudaStream_t st, bool identity_rows = false, const int32_t *slots = nullptr) {
     const ep_config &c = ctx->cfg;
     ep::DispatchParams p;
     p.x = static_cast<const uint16_t *>(x) + g0 * c.hidden;
-    p.slot = identity_rows ? nullptr : h->slot + g0 * c.topk;
+    p.slot = identity_rows ? nullptr : (slots != nullptr ? slots : h->slot) + g0 * c.topk;
     p.recv = recv;
     p.recv_scales = recv_scales;
     p.N = g1 - g0;
@@ -195,8 +236,9 @@ ep_status enqueue_dispatch(ep_ctx *ctx, const ep_handle *h, const void *x, int64
     const int kern = ctx->tune.dispatch_kernel;
     const bool short_fp8 = fp8 && (c.hidden <= 1024 || (c.hidden <= 2048 && c.topk <= 4));
     if (kern == 2 || (kern == 0 && short_fp8)) p.row_sms = 0;
-    p.prestage = behind_layout ? 8 : 1;
     p.row_bps = ctx->tune.dispatch_ctas_per_sm;
+    p.status = ctx->d_status;
+    p.early_x = behind_layout ? 1 : 0;
     const int cap = grid_cap(ctx, fp8 ? ctx->dispatch_bps_fp8 : ctx->dispatch_bps_bf16);
     if (ep::launch_dispatch(p, fp8, cap, /*pdl=*/true, st) != cudaSuccess) {
         cudaGetLastError();
@@ -226,12 +268,12 @@ ep_status enqueue_identity(ep_ctx *ctx, const ep_handle *h, bool fp8, const void
 
 // The combine kernel over tokens [g0, g1) (g1 > g0).
 ep_status enqueue_combine(ep_ctx *ctx, const ep_handle *h, const void *y, const float *w, int64_t g0, int64_t g1,
-                          void *out, cudaStream_t st, bool token_major = false) {
+                          void *out, cudaStream_t st, bool token_major = false, const int32_t *slots = nullptr) {
     const ep_config &c = ctx->cfg;
     ep::CombineParams p;
     p.y = y;
     p.weights = w != nullptr ? w + g0 * c.topk : nullptr;
-    p.slot = h->slot + g0 * c.topk;
+    p.slot = (slots != nullptr ? slots : h->slot) + g0 * c.topk;
     p.out = static_cast<uint16_t *>(out) + g0 * c.hidden;
     p.N = g1 - g0;
     p.K = c.topk;
@@ -270,7 +312,9 @@ int mover_sms(const ep_ctx *ctx, int32_t num_sms) {
     return sms;
 }
 
-ep_status enqueue_move(ep::MoveParams &p, int sms, cudaStream_t st) {
+ep_status enqueue_move(const ep_ctx *ctx, ep::MoveParams &p, int sms, cudaStream_t st) {
+    p.withhold = ctx->hooks.move_withhold_item;
+    p.wait_ns = ctx->hooks.move_wait_ns;
     const cudaError_t e = ep::launch_move(p, sms, /*pdl=*/true, st);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -287,7 +331,7 @@ ep_status enqueue_round_trip(ep_ctx *ctx, const ep_handle *h, const void *x, con
     if (chunk <= 0 || chunk > N) chunk = N;
     for (int64_t g0 = 0; g0 < N; g0 += chunk) {
         const int64_t g1 = g0 + chunk < N ? g0 + chunk : N;
-        ep_status s = enqueue_dispatch(ctx, h, x, g0, g1, fp8, recv, recv_scales, nullptr, fresh && g0 == 0, st);
+        ep_status s = enqueue_dispatch(ctx, h, x, g0, g1, fp8, recv, recv_scales, nullptr, fresh || g0 > 0, st);
         if (s == EP_OK && (fp8 || y != recv)) s = enqueue_identity(ctx, h, fp8, recv, recv_scales, y, g0, g1, st);
         if (s == EP_OK) s = enqueue_combine(ctx, h, y, w, g0, g1, out, st);
         if (s != EP_OK) return s;
@@ -304,6 +348,206 @@ ep_status check_range(const ep_ctx *ctx, const ep_handle *h, int64_t g0, int64_t
     if (g0 < 0 || g1 < g0 || g1 > N) return EP_ERR_INVALID_ARG;
     if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
     return EP_OK;
+}
+
+// The rank-deduplicated layout (keys are destination ranks); with
+// want_ranges also the per-(destination, source rank) counts and offsets
+// that the rank transport's runs come from.
+ep_status enqueue_rank_layout(ep_ctx *ctx, const int64_t *topk_idx, const float *topk_weights, int32_t T,
+                              int32_t *num_tokens_per_rank, int32_t *recv_topk_idx, float *recv_topk_weights,
+                              bool want_ranges, ep_handle *h, cudaStream_t stream) {
+    const ep_config &c = ctx->cfg;
+    ep::LayoutParams p;
+    p.topk_idx = topk_idx;
+    p.R = c.num_ranks;
+    p.T = T;
+    p.K = c.topk;
+    p.E = c.num_ranks;  // keys are destination ranks
+    p.L = c.num_experts / c.num_ranks;
+    p.num_experts = c.num_experts;
+    p.rank_mode = 1;
+    p.topk_weights = topk_weights;
+    p.recv_topk_idx = recv_topk_idx;
+    p.recv_topk_weights = recv_topk_weights;
+    p.layout = c.layout;
+    p.N = (int64_t)c.num_ranks * T;
+    p.cap = c.layout == EP_LAYOUT_PADDED ? (int64_t)c.num_ranks * c.max_tokens_per_rank : rank_rows_of(&c);
+    p.slot = h->slot;
+    p.src_info = h->src_info;
+    p.cnt_er = want_ranges ? h->cnt_er : nullptr;
+    p.off_er = want_ranges ? h->off_er : nullptr;
+    p.base = h->base;
+    p.tokens_per_expert = h->tokens_per_expert;
+    p.user_tokens_per_expert = num_tokens_per_rank;
+    p.tokens_per_rank = nullptr;
+    p.is_token_in_rank = nullptr;
+    p.status = ctx->d_status;
+    forget_send(h);
+    h->tokens_per_rank = -1;  // as in enqueue_layout
+    const cudaError_t err = launch_layout_any(ctx, p, h, stream);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return err == cudaErrorInvalidConfiguration ? EP_ERR_UNSUPPORTED : EP_ERR_CUDA;
+    }
+    h->tokens_per_rank = T;
+    h->has_rank_ranges = want_ranges ? 1 : 0;
+    h->rank_mode = 1;
+    h->num_keys = c.num_ranks;
+    return EP_OK;
+}
+
+// Runs of the rank transport, [r*R + d]: tokens source r carries to rank d,
+// and the first send / receive row of each run.
+struct RankRuns {
+    std::vector<int64_t> cnt, send_off, recv_off;
+    int64_t send_rows = 0;
+};
+
+// The run sizes on the host: the first use after a new layout waits for the
+// copy of the counts that ep_rank_dispatch_send queued (a host
+// synchronisation on the end of that send), later uses read them directly.
+ep_status rank_runs(const ep_ctx *ctx, ep_handle *h, RankRuns *o) {
+    if (!h->has_send || h->runs_state == 0 || h->tokens_per_rank < 0) return EP_ERR_NO_LAYOUT;
+    if (h->runs_state == 1) {
+        if (cudaEventSynchronize(h->runs_ev) != cudaSuccess) {
+            cudaGetLastError();
+            return EP_ERR_CUDA;
+        }
+        h->runs_state = 2;
+    }
+    const ep_config &c = ctx->cfg;
+    const int R = c.num_ranks;
+    o->cnt.assign((size_t)R * R, 0);
+    o->send_off.assign((size_t)R * R, 0);
+    o->recv_off.assign((size_t)R * R, 0);
+    for (int r = 0; r < R; ++r)
+        for (int d = 0; d < R; ++d) o->cnt[(size_t)r * R + d] = h->h_runs[(size_t)d * R + r];
+    int64_t acc = 0;
+    for (size_t i = 0; i < (size_t)R * R; ++i) {
+        o->send_off[i] = acc;
+        acc += o->cnt[i];
+    }
+    o->send_rows = acc;
+    int64_t packed = 0;  // packed layout: rank d's rows start after every lower rank's
+    for (int d = 0; d < R; ++d) {
+        const int64_t base = c.layout == EP_LAYOUT_PADDED ? (int64_t)d * R * c.max_tokens_per_rank : packed;
+        int64_t run = base;
+        for (int r = 0; r < R; ++r) {
+            o->recv_off[(size_t)r * R + d] = run;
+            run += o->cnt[(size_t)r * R + d];
+        }
+        packed += run - base;
+    }
+    return EP_OK;
+}
+
+// One row block that a wire moves: rows of `row` bytes (and of `row2` bytes
+// in a second array, e.g. FP8 scales, when row2 > 0).
+struct RowArrays {
+    const uint8_t *src, *src2;
+    uint8_t *dst, *dst2;
+    size_t row, row2;
+};
+
+cudaError_t copy_rows(const RowArrays &a, int64_t src_row, int64_t dst_row, int64_t n, cudaMemcpyKind kind,
+                      cudaStream_t s) {
+    cudaError_t e = cudaMemcpyAsync(a.dst + dst_row * a.row, a.src + src_row * a.row, n * a.row, kind, s);
+    if (e == cudaSuccess && a.row2 > 0)
+        e = cudaMemcpyAsync(a.dst2 + dst_row * a.row2, a.src2 + src_row * a.row2, n * a.row2, kind, s);
+    return e;
+}
+
+// Device wire: one device-to-device copy per non-empty run (send -> receive
+// rows when to_recv, else receive -> send rows), spread over the context's
+// copy streams, forked from and joined back into st.  (The CUDA driver
+// carries out same-device copies with its own copy kernels on the SMs.)
+ep_status wire_device(ep_ctx *ctx, const RankRuns &t, const RowArrays &a, bool to_recv, cudaStream_t st) {
+    const int R = ctx->cfg.num_ranks;
+    cudaError_t e = cudaEventRecord(ctx->ce_fork, st);
+    for (int i = 0; e == cudaSuccess && i < kCeStreams; ++i) e = cudaStreamWaitEvent(ctx->ce_stream[i], ctx->ce_fork, 0);
+    int j = 0;
+    for (size_t i = 0; e == cudaSuccess && i < (size_t)R * R; ++i) {
+        if (t.cnt[i] == 0) continue;
+        const int64_t from = to_recv ? t.send_off[i] : t.recv_off[i], to = to_recv ? t.recv_off[i] : t.send_off[i];
+        e = copy_rows(a, from, to, t.cnt[i], cudaMemcpyDeviceToDevice, ctx->ce_stream[j++ % kCeStreams]);
+    }
+    for (int i = 0; e == cudaSuccess && i < kCeStreams; ++i) {
+        e = cudaEventRecord(ctx->ce_join[i], ctx->ce_stream[i]);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ctx->ce_join[i], 0);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    return EP_OK;
+}
+
+// Host wire: the rows cross through the pinned host buffer `stage` (laid out
+// like the send buffer: payload rows, then the second array's rows after
+// send_rows_max payload rows) on the copy engines only, one leg per
+// direction, pipelined per source rank r: stream 0 carries the first leg
+// (device -> host), stream 1 the second (host -> device) of rank r once its
+// first leg has landed.
+//   to_recv (dispatch):  send rows of r (one copy) -> stage, then each run
+//                        stage -> receive rows
+//   !to_recv (combine):  each run receive rows -> stage, then the send rows
+//                        of r (one copy) stage -> send buffer
+ep_status wire_host(ep_ctx *ctx, const RankRuns &t, const RowArrays &a, bool to_recv, uint8_t *stage,
+                    int64_t send_rows_max, cudaStream_t st) {
+    const int R = ctx->cfg.num_ranks;
+    RowArrays leg1 = a, leg2 = a;
+    uint8_t *stage2 = stage + send_rows_max * (int64_t)a.row;
+    leg1.dst = stage;
+    leg1.dst2 = stage2;
+    leg2.src = stage;
+    leg2.src2 = stage2;
+    cudaStream_t s1 = ctx->ce_stream[0], s2 = ctx->ce_stream[1 % kCeStreams];
+    cudaError_t e = cudaEventRecord(ctx->ce_fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s1, ctx->ce_fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s2, ctx->ce_fork, 0);
+    for (int r = 0; e == cudaSuccess && r < R; ++r) {
+        const size_t r0 = (size_t)r * R;
+        int64_t n_r = 0;
+        for (int d = 0; d < R; ++d) n_r += t.cnt[r0 + d];
+        if (n_r == 0) continue;
+        const int64_t first = t.send_off[r0];  // the send rows of r are contiguous
+        if (to_recv) {
+            e = copy_rows(leg1, first, first, n_r, cudaMemcpyDeviceToHost, s1);
+        } else {
+            for (int d = 0; e == cudaSuccess && d < R; ++d)
+                if (t.cnt[r0 + d] > 0)
+                    e = copy_rows(leg1, t.recv_off[r0 + d], t.send_off[r0 + d], t.cnt[r0 + d], cudaMemcpyDeviceToHost, s1);
+        }
+        if (e == cudaSuccess) e = cudaEventRecord(ctx->ce_rank[r], s1);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s2, ctx->ce_rank[r], 0);
+        if (to_recv) {
+            for (int d = 0; e == cudaSuccess && d < R; ++d)
+                if (t.cnt[r0 + d] > 0)
+                    e = copy_rows(leg2, t.send_off[r0 + d], t.recv_off[r0 + d], t.cnt[r0 + d], cudaMemcpyHostToDevice, s2);
+        } else if (e == cudaSuccess) {
+            e = copy_rows(leg2, first, first, n_r, cudaMemcpyHostToDevice, s2);
+        }
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(ctx->ce_join[0], s1);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ctx->ce_join[0], 0);
+    if (e == cudaSuccess) e = cudaEventRecord(ctx->ce_join[1 % kCeStreams], s2);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ctx->ce_join[1 % kCeStreams], 0);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    return EP_OK;
+}
+
+// Pinned (page-locked) host memory: what the copy engines read and write
+// without a staging copy of the driver's.
+bool pinned_host(const void *p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost;
 }
 
 }  // namespace
@@ -368,6 +612,7 @@ const char *ep_status_str(int32_t s) {
         case EP_ERR_CAPACITY: return "padded expert buffer overflow";
         case EP_ERR_NO_LAYOUT: return "handle holds no layout for these sizes";
         case EP_ERR_TIMEOUT: return "a bounded wait on the device gave up";
+        case EP_ERR_TIMEOUT_IN_FLIGHT: return "a bounded wait on the device gave up with copies still in flight";
         default: return "unknown status";
     }
 }
@@ -440,6 +685,19 @@ ep_status ep_create(const ep_config *cfg, ep_ctx **out) {
         free(ctx);
         return EP_ERR_CUDA;
     }
+    ctx->hooks.move_withhold_item = -1;
+    ctx->hooks.move_wait_ns = 0;
+    bool ok = cudaEventCreateWithFlags(&ctx->ce_fork, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < kCeStreams; ++i)
+        ok = cudaStreamCreateWithFlags(&ctx->ce_stream[i], cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&ctx->ce_join[i], cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < ep::kRankRunsMaxRanks; ++i)
+        ok = cudaEventCreateWithFlags(&ctx->ce_rank[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        ep_destroy(ctx);
+        return EP_ERR_CUDA;
+    }
     *out = ctx;
     return EP_OK;
 }
@@ -447,6 +705,13 @@ ep_status ep_create(const ep_config *cfg, ep_ctx **out) {
 ep_status ep_destroy(ep_ctx *ctx) {
     if (ctx == nullptr) return EP_ERR_INVALID_ARG;
     cudaFree(ctx->d_status);
+    if (ctx->ce_fork) cudaEventDestroy(ctx->ce_fork);
+    for (int i = 0; i < kCeStreams; ++i) {
+        if (ctx->ce_stream[i]) cudaStreamDestroy(ctx->ce_stream[i]);
+        if (ctx->ce_join[i]) cudaEventDestroy(ctx->ce_join[i]);
+    }
+    for (int i = 0; i < ep::kRankRunsMaxRanks; ++i)
+        if (ctx->ce_rank[i]) cudaEventDestroy(ctx->ce_rank[i]);
     free(ctx);
     return EP_OK;
 }
@@ -469,8 +734,11 @@ ep_status ep_handle_create(ep_ctx *ctx, ep_handle **out) {
               cudaMalloc(&h->off_er, er * sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&h->base, (size_t)c.num_experts * sizeof(int64_t)) == cudaSuccess &&
               cudaMalloc(&h->tokens_per_expert, (size_t)c.num_experts * sizeof(int32_t)) == cudaSuccess &&
-              cudaMalloc(&h->cta_hist, (size_t)ctx->num_sms * (c.num_experts > c.num_ranks ? c.num_experts : c.num_ranks) *
-                                           sizeof(int32_t)) == cudaSuccess;
+              cudaMalloc(&h->cta_hist, (grid_hist_ints(ctx) + 16) * sizeof(int32_t)) == cudaSuccess &&
+              cudaMalloc(&h->send_slot, nk * sizeof(int32_t)) == cudaSuccess;
+    if (ok && c.num_ranks <= ep::kRankRunsMaxRanks)
+        ok = cudaMallocHost(&h->h_runs, (size_t)c.num_ranks * c.num_ranks * sizeof(int32_t)) == cudaSuccess &&
+             cudaEventCreateWithFlags(&h->runs_ev, cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
         ep_handle_destroy(h);
@@ -489,6 +757,11 @@ ep_status ep_handle_destroy(ep_handle *h) {
     cudaFree(h->base);
     cudaFree(h->tokens_per_expert);
     cudaFree(h->cta_hist);
+    if (h->runs_state == 1 && h->runs_ev) cudaEventSynchronize(h->runs_ev);  // the copy into h_runs lands first
+    cudaFree(h->send_slot);
+    if (h->h_runs) cudaFreeHost(h->h_runs);
+    if (h->runs_ev) cudaEventDestroy(h->runs_ev);
+    cudaGetLastError();
     free(h);
     return EP_OK;
 }
@@ -544,42 +817,9 @@ ep_status ep_get_rank_layout(ep_ctx *ctx, const int64_t *d_topk_idx, const float
         !aligned(d_recv_topk_idx, 4) || !aligned(d_recv_topk_weights, 4))
         return EP_ERR_INVALID_ARG;
     if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
-    ep::LayoutParams p;
-    p.topk_idx = d_topk_idx;
-    p.R = c.num_ranks;
-    p.T = tokens_per_rank;
-    p.K = c.topk;
-    p.E = c.num_ranks;  // keys are destination ranks
-    p.L = c.num_experts / c.num_ranks;
-    p.num_experts = c.num_experts;
-    p.rank_mode = 1;
-    p.topk_weights = d_topk_weights;
-    p.recv_topk_idx = d_recv_topk_idx;
-    p.recv_topk_weights = d_recv_topk_weights;
-    p.layout = c.layout;
-    p.N = (int64_t)c.num_ranks * tokens_per_rank;
-    p.cap = c.layout == EP_LAYOUT_PADDED ? (int64_t)c.num_ranks * c.max_tokens_per_rank : rank_rows_of(&c);
-    p.slot = handle->slot;
-    p.src_info = handle->src_info;
-    p.cnt_er = nullptr;
-    p.off_er = nullptr;
-    p.base = handle->base;
-    p.tokens_per_expert = handle->tokens_per_expert;
-    p.user_tokens_per_expert = d_num_tokens_per_rank;
-    p.tokens_per_rank = nullptr;
-    p.is_token_in_rank = nullptr;
-    p.status = ctx->d_status;
-    handle->tokens_per_rank = -1;  // as in enqueue_layout
-    const cudaError_t err = launch_layout_any(ctx, p, handle, (cudaStream_t)stream);
-    if (err != cudaSuccess) {
-        cudaGetLastError();
-        return err == cudaErrorInvalidConfiguration ? EP_ERR_UNSUPPORTED : EP_ERR_CUDA;
-    }
-    handle->tokens_per_rank = tokens_per_rank;
-    handle->has_rank_ranges = 0;
-    handle->rank_mode = 1;
-    handle->num_keys = c.num_ranks;
-    return EP_OK;
+    return enqueue_rank_layout(ctx, d_topk_idx, d_topk_weights, tokens_per_rank, d_num_tokens_per_rank,
+                               d_recv_topk_idx, d_recv_topk_weights, /*want_ranges=*/false, handle,
+                               (cudaStream_t)stream);
 }
 
 ep_status ep_dispatch(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, int32_t tokens_per_rank,
@@ -782,7 +1022,7 @@ ep_status ep_dispatch_recv(ep_ctx *ctx, const ep_handle *handle, int32_t use_fp8
     p.count_dst = d_recv_count;
     p.E = handle->num_keys;
     p.status = ctx->d_status;
-    return enqueue_move(p, mover_sms(ctx, num_sms), st);
+    return enqueue_move(ctx, p, mover_sms(ctx, num_sms), st);
 }
 
 ep_status ep_combine_send(ep_ctx *ctx, const ep_handle *handle, const void *d_y, void *d_send_y, int32_t num_sms,
@@ -812,7 +1052,7 @@ ep_status ep_combine_send(ep_ctx *ctx, const ep_handle *handle, const void *d_y,
     p.count_dst = nullptr;
     p.E = 0;
     p.status = ctx->d_status;
-    return enqueue_move(p, mover_sms(ctx, num_sms), (cudaStream_t)stream);
+    return enqueue_move(ctx, p, mover_sms(ctx, num_sms), (cudaStream_t)stream);
 }
 
 ep_status ep_combine_recv(ep_ctx *ctx, const ep_handle *handle, const void *d_send_y, const float *d_topk_weights,
@@ -827,6 +1067,184 @@ ep_status ep_combine_recv(ep_ctx *ctx, const ep_handle *handle, const void *d_se
     if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
     return enqueue_combine(ctx, handle, d_send_y, d_topk_weights, 0, N, d_out, (cudaStream_t)stream,
                            /*token_major=*/true);
+}
+
+ep_status ep_rank_send_rows(const ep_config *cfg, int64_t *rows) {
+    const ep_status s = check_config(cfg);
+    if (s != EP_OK) return s;
+    if (rows == nullptr) return EP_ERR_INVALID_ARG;
+    const int64_t n = (int64_t)cfg->num_ranks * cfg->max_tokens_per_rank;
+    *rows = n * (cfg->topk < cfg->num_ranks ? cfg->topk : cfg->num_ranks);
+    return EP_OK;
+}
+
+ep_status ep_rank_dispatch_send(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, const float *d_topk_weights,
+                                int32_t tokens_per_rank, int32_t use_fp8, int32_t *d_recv_topk_idx,
+                                float *d_recv_topk_weights, ep_handle *handle, void *d_send_x, float *d_send_scales,
+                                void *stream) {
+    NvtxRange nvtx("ep_rank_dispatch_send");
+    if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
+    const ep_config &c = ctx->cfg;
+    if (c.num_ranks > ep::kRankRunsMaxRanks) return EP_ERR_UNSUPPORTED;
+    if (tokens_per_rank < 0 || tokens_per_rank > c.max_tokens_per_rank) return EP_ERR_INVALID_ARG;
+    if (use_fp8 != 0 && use_fp8 != 1) return EP_ERR_INVALID_ARG;
+    if (use_fp8 && c.hidden % 128 != 0) return EP_ERR_UNSUPPORTED;
+    if (d_recv_topk_weights != nullptr && d_recv_topk_idx == nullptr) return EP_ERR_INVALID_ARG;
+    const int64_t N = (int64_t)c.num_ranks * tokens_per_rank;
+    if (N > 0 && (d_x == nullptr || d_send_x == nullptr || (use_fp8 && d_send_scales == nullptr)))
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(d_x, 16) || !aligned(d_send_x, 16) || !aligned(d_send_scales, 16) || !aligned(d_topk_idx, 8) ||
+        !aligned(d_topk_weights, 4) || !aligned(d_recv_topk_idx, 4) || !aligned(d_recv_topk_weights, 4))
+        return EP_ERR_INVALID_ARG;
+    const bool fresh = d_topk_idx != nullptr || tokens_per_rank == 0;
+    if (!fresh && (!handle->has_send || handle->tokens_per_rank != tokens_per_rank)) return EP_ERR_NO_LAYOUT;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (fresh) {
+        ep_status s = enqueue_rank_layout(ctx, d_topk_idx, d_topk_weights, tokens_per_rank, nullptr, d_recv_topk_idx,
+                                          d_recv_topk_weights, /*want_ranges=*/true, handle, st);
+        if (s != EP_OK) return s;
+        ep::RankSendParams rp;
+        rp.topk_idx = d_topk_idx;
+        rp.slot = handle->slot;
+        rp.cnt_er = handle->cnt_er;
+        rp.off_er = handle->off_er;
+        rp.base = handle->base;
+        rp.send_slot = handle->send_slot;
+        rp.N = N;
+        rp.R = c.num_ranks;
+        rp.T = tokens_per_rank;
+        rp.K = c.topk;
+        rp.L = c.num_experts / c.num_ranks;
+        if (N > 0 && ep::launch_rank_send_slots(rp, ctx->num_sms, st) != cudaSuccess) {
+            cudaGetLastError();
+            handle->tokens_per_rank = -1;
+            return EP_ERR_CUDA;
+        }
+    }
+    if (N > 0) {
+        const ep_status s = enqueue_dispatch(ctx, handle, d_x, 0, N, use_fp8 != 0, d_send_x, d_send_scales, nullptr,
+                                             fresh, st, /*identity_rows=*/false, handle->send_slot);
+        if (s != EP_OK) {
+            if (fresh) handle->tokens_per_rank = -1;
+            return s;
+        }
+    }
+    if (fresh) {  // the run sizes, for the host that issues the wire's copies
+        const size_t rr = (size_t)c.num_ranks * c.num_ranks;
+        if (cudaMemcpyAsync(handle->h_runs, handle->cnt_er, rr * sizeof(int32_t), cudaMemcpyDeviceToHost, st) !=
+                cudaSuccess ||
+            cudaEventRecord(handle->runs_ev, st) != cudaSuccess) {
+            cudaGetLastError();
+            handle->tokens_per_rank = -1;
+            return EP_ERR_CUDA;
+        }
+        handle->runs_state = 1;
+        handle->has_send = 1;
+    }
+    return EP_OK;
+}
+
+namespace {
+// Checks and run table shared by the two wire calls.
+ep_status wire_prologue(ep_ctx *ctx, ep_handle *h, int32_t wire, const void *h_stage, RankRuns *t) {
+    if (ctx == nullptr || h == nullptr || h->ctx != ctx) return EP_ERR_INVALID_ARG;
+    if (wire != EP_WIRE_DEVICE && wire != EP_WIRE_HOST) return EP_ERR_INVALID_ARG;
+    if (!h->has_send || h->tokens_per_rank < 0) return EP_ERR_NO_LAYOUT;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    if (wire == EP_WIRE_HOST && (h_stage == nullptr || !aligned(h_stage, 16) || !pinned_host(h_stage)))
+        return EP_ERR_INVALID_ARG;
+    return rank_runs(ctx, h, t);
+}
+}  // namespace
+
+ep_status ep_rank_dispatch_recv(ep_ctx *ctx, ep_handle *handle, int32_t use_fp8, const void *d_send_x,
+                                const float *d_send_scales, void *d_recv_x, float *d_recv_scales,
+                                int32_t *d_recv_count, int32_t wire, void *h_stage, void *stream) {
+    NvtxRange nvtx("ep_rank_dispatch_recv");
+    if (use_fp8 != 0 && use_fp8 != 1) return EP_ERR_INVALID_ARG;
+    if (ctx != nullptr && use_fp8 && ctx->cfg.hidden % 128 != 0) return EP_ERR_UNSUPPORTED;
+    if (!aligned(d_send_x, 16) || !aligned(d_recv_x, 16) || !aligned(d_send_scales, 16) ||
+        !aligned(d_recv_scales, 16) || !aligned(d_recv_count, 4))
+        return EP_ERR_INVALID_ARG;
+    RankRuns t;
+    ep_status s = wire_prologue(ctx, handle, wire, h_stage, &t);
+    if (s != EP_OK) return s;
+    const ep_config &c = ctx->cfg;
+    if (t.send_rows > 0 && (d_send_x == nullptr || d_recv_x == nullptr ||
+                            (use_fp8 && (d_send_scales == nullptr || d_recv_scales == nullptr))))
+        return EP_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (d_recv_count != nullptr &&
+        cudaMemcpyAsync(d_recv_count, handle->tokens_per_expert, (size_t)c.num_ranks * sizeof(int32_t),
+                        cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
+        cudaGetLastError();
+        return EP_ERR_CUDA;
+    }
+    if (t.send_rows == 0) return EP_OK;
+    RowArrays a;
+    a.src = static_cast<const uint8_t *>(d_send_x);
+    a.dst = static_cast<uint8_t *>(d_recv_x);
+    a.row = use_fp8 ? (size_t)c.hidden : 2 * (size_t)c.hidden;
+    a.src2 = use_fp8 ? reinterpret_cast<const uint8_t *>(d_send_scales) : nullptr;
+    a.dst2 = use_fp8 ? reinterpret_cast<uint8_t *>(d_recv_scales) : nullptr;
+    a.row2 = use_fp8 ? (size_t)c.hidden / 32 : 0;
+    int64_t rows_max = 0;
+    ep_rank_send_rows(&c, &rows_max);
+    return wire == EP_WIRE_DEVICE ? wire_device(ctx, t, a, true, st)
+                                  : wire_host(ctx, t, a, true, static_cast<uint8_t *>(h_stage), rows_max, st);
+}
+
+ep_status ep_rank_combine_send(ep_ctx *ctx, ep_handle *handle, const void *d_y, void *d_send_y, int32_t wire,
+                               void *h_stage, void *stream) {
+    NvtxRange nvtx("ep_rank_combine_send");
+    if (!aligned(d_y, 16) || !aligned(d_send_y, 16)) return EP_ERR_INVALID_ARG;
+    RankRuns t;
+    ep_status s = wire_prologue(ctx, handle, wire, h_stage, &t);
+    if (s != EP_OK) return s;
+    if (t.send_rows == 0) return EP_OK;
+    if (d_y == nullptr || d_send_y == nullptr) return EP_ERR_INVALID_ARG;
+    const ep_config &c = ctx->cfg;
+    RowArrays a;
+    a.src = static_cast<const uint8_t *>(d_y);
+    a.dst = static_cast<uint8_t *>(d_send_y);
+    a.row = 2 * (size_t)c.hidden;
+    a.src2 = nullptr;
+    a.dst2 = nullptr;
+    a.row2 = 0;
+    int64_t rows_max = 0;
+    ep_rank_send_rows(&c, &rows_max);
+    cudaStream_t st = (cudaStream_t)stream;
+    return wire == EP_WIRE_DEVICE ? wire_device(ctx, t, a, false, st)
+                                  : wire_host(ctx, t, a, false, static_cast<uint8_t *>(h_stage), rows_max, st);
+}
+
+ep_status ep_rank_combine_recv(ep_ctx *ctx, const ep_handle *handle, const void *d_send_y, void *d_out,
+                               void *stream) {
+    NvtxRange nvtx("ep_rank_combine_recv");
+    if (ctx == nullptr || handle == nullptr || handle->ctx != ctx) return EP_ERR_INVALID_ARG;
+    if (!handle->has_send || handle->tokens_per_rank < 0) return EP_ERR_NO_LAYOUT;
+    const int64_t N = (int64_t)ctx->cfg.num_ranks * handle->tokens_per_rank;
+    if (N == 0) return EP_OK;
+    if (d_send_y == nullptr || d_out == nullptr) return EP_ERR_INVALID_ARG;
+    if (!aligned(d_send_y, 16) || !aligned(d_out, 16)) return EP_ERR_INVALID_ARG;
+    if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
+    return enqueue_combine(ctx, handle, d_send_y, nullptr, 0, N, d_out, (cudaStream_t)stream,
+                           /*token_major=*/false, handle->send_slot);
+}
+
+ep_status ep_rank_runs(ep_handle *handle, int32_t *run_cnt, int64_t *send_off, int64_t *recv_off) {
+    if (handle == nullptr) return EP_ERR_INVALID_ARG;
+    if (!on_ctx_device(handle->ctx)) return EP_ERR_INVALID_ARG;
+    RankRuns t;
+    const ep_status s = rank_runs(handle->ctx, handle, &t);
+    if (s != EP_OK) return s;
+    for (size_t i = 0; i < t.cnt.size(); ++i) {
+        if (run_cnt) run_cnt[i] = (int32_t)t.cnt[i];
+        if (send_off) send_off[i] = t.send_off[i];
+        if (recv_off) recv_off[i] = t.recv_off[i];
+    }
+    return EP_OK;
 }
 
 ep_status ep_round_trip_auto_chunk(const ep_ctx *ctx, int32_t use_fp8, int32_t rank_layout, int32_t *chunk_tokens) {
@@ -1009,7 +1427,16 @@ ep_status ep_get_device_status(ep_ctx *ctx, void *stream) {
     }
     if (bits & ep::kStatusBadExpert) return EP_ERR_BAD_EXPERT;
     if (bits & ep::kStatusCapacity) return EP_ERR_CAPACITY;
+    if (bits & ep::kStatusInFlight) return EP_ERR_TIMEOUT_IN_FLIGHT;
     if (bits & ep::kStatusTimeout) return EP_ERR_TIMEOUT;
+    return EP_OK;
+}
+
+ep_status ep_set_test_hooks(ep_ctx *ctx, const ep_test_hooks *hooks) {
+    if (ctx == nullptr || hooks == nullptr) return EP_ERR_INVALID_ARG;
+    if (hooks->move_withhold_item < -1 || hooks->move_wait_ns < 0 || hooks->move_wait_ns > 10000000000ll)
+        return EP_ERR_INVALID_ARG;
+    ctx->hooks = *hooks;
     return EP_OK;
 }
 

@@ -11,6 +11,7 @@ namespace ep {
 constexpr uint32_t kStatusBadExpert = 1u;  // topk_idx entry outside [-1, E)
 constexpr uint32_t kStatusCapacity = 2u;   // padded expert buffer offered > R*Tmax entries
 constexpr uint32_t kStatusTimeout = 4u;    // a bounded wait of a copy kernel gave up
+constexpr uint32_t kStatusInFlight = 8u;   // ... and its loads may still land in freed shared memory
 
 constexpr int kLayoutPadded = 0;
 constexpr int kLayoutPacked = 1;
@@ -78,10 +79,13 @@ struct DispatchParams {
     int32_t *count_dst;
     int32_t E;
     int32_t row_sms;           // SMs for the row kernel (H % 512 == 0), 0 = use the warp-item kernel
-    int32_t prestage;          // row kernel: tokens per CTA cast before waiting for the slots (>= 1;
-                               // more than one pays when a layout kernel runs just before)
     // slot == nullptr: token g goes to row g (K must be 1): the send buffer of a split dispatch
     int32_t row_bps;           // row kernel CTAs per SM, 0 = the built-in rule (from H)
+    uint32_t *status;          // row kernel: kStatusTimeout if one of its bounded waits gave up
+    int32_t early_x;           // 1: the kernel is launched behind this library's layout kernel(s),
+                               // which started after x was written, so x may be read before
+                               // griddepcontrol.wait; 0: wait first (x may come from the kernel
+                               // just before)
 };
 
 cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks,
@@ -139,7 +143,10 @@ struct MoveParams {
     int32_t *count_dst;
     int32_t E;
     uint32_t *status;
+    int64_t withhold;           // test hook: item whose load is never issued (-1: none)
+    int64_t wait_ns;            // bound of each mbarrier wait, 0 = kMoveWaitNs
 };
+constexpr uint64_t kMoveWaitNs = 1000000000ull;  // one second
 
 // Launch on `sms` SMs (as many CTAs per SM as shared memory allows).
 cudaError_t launch_move(MoveParams p, int sms, bool pdl, cudaStream_t stream);
@@ -147,6 +154,22 @@ cudaError_t launch_move(MoveParams p, int sms, bool pdl, cudaStream_t stream);
 void move_init();
 // Read `bytes` (> L2) of `buf`: afterwards L2 holds only clean lines.
 cudaError_t launch_l2_evict(const void *buf, size_t bytes, int sms, cudaStream_t stream);
+
+// ------------------------------------------------------------------ rank runs
+// Send rows of the rank-deduplicated transport (source-major runs; see
+// rank_transport.cu).  R <= kRankRunsMaxRanks.
+constexpr int kRankRunsMaxRanks = 32;
+struct RankSendParams {
+    const int64_t *topk_idx;   // [N*K]
+    const int32_t *slot;       // [N*K] receive rows of the rank layout
+    const int32_t *cnt_er;     // [R*R] cnt_er[d*R + r]: tokens source r carries to d
+    const int32_t *off_er;     // [R*R] first row of (d, r) relative to base[d]
+    const int64_t *base;       // [R]
+    int32_t *send_slot;        // [N*K] out
+    int64_t N;
+    int32_t R, T, K, L;
+};
+cudaError_t launch_rank_send_slots(const RankSendParams &p, int sms, cudaStream_t stream);
 
 // ------------------------------------------------------------------ identity expert
 struct IdentityParams {

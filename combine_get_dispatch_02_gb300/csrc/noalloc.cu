@@ -4,12 +4,14 @@
 // The regular path keeps that state (receive row of every entry, first row
 // and count of every expert, the device status word) in buffers that
 // ep_create / ep_handle_create obtain with cudaMalloc.  Some callers cannot
-// call cudaMalloc: code running inside a CUDA-graph capture that must not
-// allocate, runtimes that hand every byte of device memory to their own
-// allocator up front, or plugins that may only touch memory they are given.
-// For them this entry point takes only the inputs and outputs and keeps the
-// rest in g_noalloc_scratch below, which the CUDA module of libep.so holds on
-// every GPU that loads the library until the process exits (about 4.3 MB).
+// call cudaMalloc: runtimes that hand every byte of device memory to their
+// own allocator up front (a cudaMalloc of theirs would fail or steal from
+// that pool), plugins that may only touch the memory they are given, and
+// code on a latency-critical path where a cudaMalloc could synchronise the
+// device.  For them this entry point takes only the inputs and outputs and
+// keeps the rest in g_noalloc_scratch below, which the CUDA module of
+// libep.so holds on every GPU that loads the library until the process
+// exits (about 4.3 MB).
 //
 // Limits (calls beyond them return EP_ERR_UNSUPPORTED and enqueue nothing):
 //   R * tokens_per_rank * K  <= 65536 entries
@@ -44,6 +46,9 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 // Per-device set-up: the device address of g_noalloc_scratch (host code may
 // not use the symbol itself as an address), the SM count, resident blocks of
 // the dispatch kernels and the layout kernel's shape for the last (E, R).
+// The address is looked up again on every call: after a cudaDeviceReset the
+// module is loaded anew and the array may sit elsewhere, and then the whole
+// set-up (kernel attributes included) is repeated.
 struct DeviceSetup {
     bool ready;
     unsigned char *scratch;
@@ -88,10 +93,13 @@ extern "C" ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, 
     {
         std::lock_guard<std::mutex> lock(g_setup_mutex);
         DeviceSetup &d = g_setup[dev];
-        if (!d.ready) {
-            void *ptr = nullptr;
-            if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr ||
-                cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return EP_ERR_CUDA;
+        }
+        if (!d.ready || d.scratch != static_cast<unsigned char *>(ptr)) {
+            if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
                 cudaGetLastError();
                 return EP_ERR_CUDA;
             }
@@ -143,9 +151,10 @@ extern "C" ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, 
     lp.is_token_in_rank = nullptr;
     lp.status = status;
     lp.cta_hist = nullptr;  // at most 65536 entries here: always the cluster form
-    if (ep::launch_layout(lp, s.cluster, s.threads, st) != cudaSuccess) {
+    const cudaError_t le = ep::launch_layout(lp, s.cluster, s.threads, st);
+    if (le != cudaSuccess) {  // the status clear above is already enqueued (harmless)
         cudaGetLastError();
-        return EP_ERR_CUDA;
+        return le == cudaErrorInvalidConfiguration ? EP_ERR_UNSUPPORTED : EP_ERR_CUDA;
     }
     if (N == 0) return EP_OK;
 
@@ -165,12 +174,14 @@ extern "C" ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, 
     // short FP8 rows go to the warp-item kernel (the rule of ep_dispatch)
     const bool short_fp8 = use_fp8 && (c.hidden <= 1024 || (c.hidden <= 2048 && c.topk <= 4));
     dp.row_sms = short_fp8 ? 0 : sms;
-    dp.prestage = 8;  // behind the layout kernel
     dp.row_bps = 0;
+    dp.status = status;
+    dp.early_x = 1;  // behind the layout kernel
     const int cap = sms * (use_fp8 ? s.bps_fp8 : s.bps_bf16);
-    if (ep::launch_dispatch(dp, use_fp8 != 0, cap, /*pdl=*/true, st) != cudaSuccess) {
+    const cudaError_t de = ep::launch_dispatch(dp, use_fp8 != 0, cap, /*pdl=*/true, st);
+    if (de != cudaSuccess) {
         cudaGetLastError();
-        return EP_ERR_CUDA;
+        return de == cudaErrorInvalidConfiguration ? EP_ERR_UNSUPPORTED : EP_ERR_CUDA;
     }
     return EP_OK;
 }

@@ -14,9 +14,15 @@
 // loads in flight; when a row has landed, lane k < K issues the copy to the
 // k-th destination (one bulk group per lane and row), and the buffer is
 // refilled once the copies of the row before it have read it.  Every
-// mbarrier wait is bounded (about one second of %globaltimer): on expiry the
-// kernel sets kStatusTimeout in the status word, waits (bounded again) for
-// the loads it issued, drains its stores and returns.
+// mbarrier wait is bounded (about one second of %globaltimer, or the
+// parameter's bound): on expiry the kernel sets kStatusTimeout in the status
+// word, then waits, bounded again, for every load it issued that has not
+// landed.  If one of those waits also gives up, a bulk load may still be
+// writing into this CTA's shared memory after the kernel exits: the kernel
+// sets kStatusInFlight as well (the device's later kernels cannot be trusted).
+// Its own stores are drained before it returns.  A test can make the first
+// wait run out without any load in flight: the item `withhold` is never
+// loaded, so its barrier phase never completes.
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -24,7 +30,6 @@ namespace ep {
 namespace {
 
 constexpr int kMaxRing = 8;
-constexpr uint64_t kWaitNs = 1000000000ull;  // bound of one mbarrier wait
 
 __device__ __forceinline__ uint32_t saddr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -52,12 +57,13 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase with this parity; false when it gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Bounded wait (limit_ns of %globaltimer) for the phase with this parity;
+// false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = now_ns();
     while (!mbar_try(bar, parity))
-        if (now_ns() - t0 > kWaitNs) return false;
+        if (now_ns() - t0 > limit_ns) return false;
     return true;
 }
 
@@ -84,6 +90,7 @@ __global__ void __launch_bounds__(32) move_rows_kernel(const MoveParams p) {
     const uint32_t buf = rb + sb;
     const int64_t G = gridDim.x;
     const int64_t cnt = p.n > (int64_t)blockIdx.x ? (p.n - 1 - blockIdx.x) / G + 1 : 0;
+    const uint64_t limit = p.wait_ns > 0 ? (uint64_t)p.wait_ns : kMoveWaitNs;
 
     if (lane == 0) {
         for (int b = 0; b < NB; ++b) mbar_init(saddr(&bars[b]), 1);
@@ -100,11 +107,14 @@ __global__ void __launch_bounds__(32) move_rows_kernel(const MoveParams p) {
         const int64_t j = blockIdx.x + i * G;
         return p.gather ? (int64_t)p.slot[j] : j;
     };
+    auto withheld = [&](int64_t i) { return blockIdx.x + i * G == p.withhold; };
     auto issue = [&](int64_t i) {  // lane 0
         const int b = (int)(i % NB);
         const uint32_t bar = saddr(&bars[b]);
         const int64_t s = src_row(i);
-        if (s >= 0) {
+        if (withheld(i)) {
+            // test hook: no load and no arrival, so this phase never completes
+        } else if (s >= 0) {
             mbar_arrive_tx(bar, buf);
             bulk_load(saddr(ring + (size_t)b * buf), p.src + s * rb, rb, bar);
             if (sb) bulk_load(saddr(ring + (size_t)b * buf + rb), p.src_scales + s * sb, sb, bar);
@@ -124,7 +134,7 @@ __global__ void __launch_bounds__(32) move_rows_kernel(const MoveParams p) {
         const int b = (int)(i % NB);
         // every lane waits (the stores it issues read the landed row); the
         // outcome is made warp-uniform before anyone leaves the loop
-        const bool landed = mbar_wait(saddr(&bars[b]), (uint32_t)((i / NB) & 1));
+        const bool landed = mbar_wait(saddr(&bars[b]), (uint32_t)((i / NB) & 1), limit);
         if (!__all_sync(0xFFFFFFFFu, landed)) {
             ok = false;
             break;
@@ -151,10 +161,14 @@ __global__ void __launch_bounds__(32) move_rows_kernel(const MoveParams p) {
         ++issued;
     }
     if (!ok) {
-        if (lane == 0) atomicOr(p.status, kStatusTimeout);
-        // loads still in flight land in this CTA's shared memory: wait for them (bounded)
+        // Loads issued for items i .. issued-1 (one per ring buffer, the item
+        // that timed out included) land in this CTA's shared memory: wait for
+        // each of them, bounded, before the CTA gives its shared memory up.
+        // Every one is waited for, even after one wait gives up.
+        bool drained = true;
         for (int64_t k = i; k < issued && k < cnt; ++k)
-            if (!mbar_wait(saddr(&bars[k % NB]), (uint32_t)((k / NB) & 1))) break;
+            if (!withheld(k) && !mbar_wait(saddr(&bars[k % NB]), (uint32_t)((k / NB) & 1), limit)) drained = false;
+        if (lane == 0) atomicOr(p.status, drained ? kStatusTimeout : (kStatusTimeout | kStatusInFlight));
     }
     if (lane < p.K) bulk_wait_all();
 }

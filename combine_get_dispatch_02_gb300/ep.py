@@ -25,9 +25,13 @@ EP_ERR_BAD_EXPERT = 5
 EP_ERR_CAPACITY = 6
 EP_ERR_NO_LAYOUT = 7
 EP_ERR_TIMEOUT = 8
+EP_ERR_TIMEOUT_IN_FLIGHT = 9
 
 EP_LAYOUT_PADDED = 0
 EP_LAYOUT_PACKED = 1
+
+EP_WIRE_DEVICE = 0
+EP_WIRE_HOST = 1
 
 # Every entry point include/ep.h declares (checked against the header and the
 # library by the tests).
@@ -38,7 +42,9 @@ ENTRY_POINTS = (
     "ep_get_device_status", "ep_dispatch_noalloc", "ep_get_rank_layout", "ep_rank_recv_rows",
     "ep_dispatch_range", "ep_combine_range", "ep_expert_identity", "ep_round_trip",
     "ep_round_trip_auto_chunk", "ep_dispatch_send", "ep_dispatch_recv", "ep_combine_send", "ep_combine_recv",
-    "ep_get_tuning", "ep_set_tuning", "ep_autotune", "ep_get_autotune_log",
+    "ep_get_tuning", "ep_set_tuning", "ep_autotune", "ep_get_autotune_log", "ep_set_test_hooks",
+    "ep_rank_send_rows", "ep_rank_dispatch_send", "ep_rank_dispatch_recv", "ep_rank_combine_send",
+    "ep_rank_combine_recv", "ep_rank_runs",
 )
 
 TUNE_KNOBS = {0: "dispatch", 1: "combine_chunks", 2: "round_trip_chunk"}  # dispatch: 100 * kernel + CTAs/SM
@@ -69,6 +75,10 @@ class ep_tuning(ctypes.Structure):
 
 class ep_tune_record(ctypes.Structure):
     _fields_ = [("knob", ctypes.c_int32), ("value", ctypes.c_int32), ("median_us", ctypes.c_float)]
+
+
+class ep_test_hooks(ctypes.Structure):
+    _fields_ = [("move_withhold_item", ctypes.c_int64), ("move_wait_ns", ctypes.c_int64)]
 
 
 class ep_handle_info(ctypes.Structure):
@@ -124,6 +134,13 @@ def lib() -> ctypes.CDLL:
             "ep_set_tuning": (I32, [P, ctypes.POINTER(ep_tuning)]),
             "ep_autotune": (I32, [P, P, P, I32, P, I32, P, P, P, P, I32, ctypes.POINTER(ep_tuning), P]),
             "ep_get_autotune_log": (I32, [P, ctypes.POINTER(ep_tune_record), I32, ctypes.POINTER(I32)]),
+            "ep_set_test_hooks": (I32, [P, ctypes.POINTER(ep_test_hooks)]),
+            "ep_rank_send_rows": (I32, [CFG, ctypes.POINTER(I64)]),
+            "ep_rank_dispatch_send": (I32, [P, P, P, P, I32, I32, P, P, P, P, P, P]),
+            "ep_rank_dispatch_recv": (I32, [P, P, I32, P, P, P, P, P, I32, P, P]),
+            "ep_rank_combine_send": (I32, [P, P, P, P, I32, P, P]),
+            "ep_rank_combine_recv": (I32, [P, P, P, P, P]),
+            "ep_rank_runs": (I32, [P, ctypes.POINTER(I32), ctypes.POINTER(I64), ctypes.POINTER(I64)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -373,3 +390,67 @@ def ep_dispatch_noalloc(cfg: ep_config, x: torch.Tensor, topk_idx: torch.Tensor,
         int(tokens_per_rank), int(bool(use_fp8)), _ptr(recv_x, None, "recv_x"),
         _ptr(recv_scales, torch.float32, "recv_scales"), _ptr(recv_count, torch.int32, "recv_count"),
         _stream(stream)), "ep_dispatch_noalloc")
+
+
+def ep_set_test_hooks(ctx, move_withhold_item: int = -1, move_wait_ns: int = 0) -> None:
+    """Test-only switches (see include/ep.h): the copy kernels' item whose
+    load is never issued, and the bound of their waits."""
+    h = ep_test_hooks(int(move_withhold_item), int(move_wait_ns))
+    _check(lib().ep_set_test_hooks(ctx, ctypes.byref(h)), "ep_set_test_hooks")
+
+
+def ep_rank_send_rows(cfg: ep_config) -> int:
+    rows = ctypes.c_int64()
+    _check(lib().ep_rank_send_rows(ctypes.byref(cfg), ctypes.byref(rows)), "ep_rank_send_rows")
+    return rows.value
+
+
+def _host_ptr(t: torch.Tensor | None, name: str = "h_stage"):
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous host tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def ep_rank_dispatch_send(ctx, x: torch.Tensor, topk_idx: torch.Tensor | None, topk_weights: torch.Tensor | None,
+                          tokens_per_rank: int, use_fp8: bool, recv_topk_idx: torch.Tensor | None,
+                          recv_topk_weights: torch.Tensor | None, handle, send_x: torch.Tensor,
+                          send_scales: torch.Tensor | None, stream=None) -> None:
+    _check(lib().ep_rank_dispatch_send(
+        ctx, _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int64, "topk_idx"),
+        _ptr(topk_weights, torch.float32, "topk_weights"), int(tokens_per_rank), int(bool(use_fp8)),
+        _ptr(recv_topk_idx, torch.int32, "recv_topk_idx"), _ptr(recv_topk_weights, torch.float32, "recv_topk_weights"),
+        handle, _ptr(send_x, None, "send_x"), _ptr(send_scales, torch.float32, "send_scales"), _stream(stream)),
+        "ep_rank_dispatch_send")
+
+
+def ep_rank_dispatch_recv(ctx, handle, use_fp8: bool, send_x: torch.Tensor, send_scales: torch.Tensor | None,
+                          recv_x: torch.Tensor, recv_scales: torch.Tensor | None, recv_count: torch.Tensor | None,
+                          wire: int = EP_WIRE_DEVICE, stage: torch.Tensor | None = None, stream=None) -> None:
+    _check(lib().ep_rank_dispatch_recv(
+        ctx, handle, int(bool(use_fp8)), _ptr(send_x, None, "send_x"), _ptr(send_scales, torch.float32, "send_scales"),
+        _ptr(recv_x, None, "recv_x"), _ptr(recv_scales, torch.float32, "recv_scales"),
+        _ptr(recv_count, torch.int32, "recv_count"), int(wire), _host_ptr(stage), _stream(stream)),
+        "ep_rank_dispatch_recv")
+
+
+def ep_rank_combine_send(ctx, handle, y: torch.Tensor, send_y: torch.Tensor, wire: int = EP_WIRE_DEVICE,
+                         stage: torch.Tensor | None = None, stream=None) -> None:
+    _check(lib().ep_rank_combine_send(ctx, handle, _ptr(y, torch.bfloat16, "y"),
+                                      _ptr(send_y, torch.bfloat16, "send_y"), int(wire), _host_ptr(stage),
+                                      _stream(stream)), "ep_rank_combine_send")
+
+
+def ep_rank_combine_recv(ctx, handle, send_y: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    _check(lib().ep_rank_combine_recv(ctx, handle, _ptr(send_y, torch.bfloat16, "send_y"),
+                                      _ptr(out, torch.bfloat16, "out"), _stream(stream)), "ep_rank_combine_recv")
+
+
+def ep_rank_runs(handle, num_ranks: int):
+    """(run_cnt, send_off, recv_off), each an R x R list of lists indexed [r][d]."""
+    n = num_ranks * num_ranks
+    cnt, so, ro = (ctypes.c_int32 * n)(), (ctypes.c_int64 * n)(), (ctypes.c_int64 * n)()
+    _check(lib().ep_rank_runs(handle, cnt, so, ro), "ep_rank_runs")
+    mat = lambda a: [list(a[r * num_ranks:(r + 1) * num_ranks]) for r in range(num_ranks)]
+    return mat(cnt), mat(so), mat(ro)

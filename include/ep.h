@@ -69,7 +69,7 @@
 extern "C" {
 #endif
 
-#define EP_ABI_VERSION 1
+#define EP_ABI_VERSION 2
 
 typedef enum ep_status {
     EP_OK = 0,
@@ -80,7 +80,11 @@ typedef enum ep_status {
     EP_ERR_BAD_EXPERT = 5,   /* device: a topk_idx entry was outside [-1, E) */
     EP_ERR_CAPACITY = 6,     /* device: padded layout, an expert was offered more than R*Tmax entries */
     EP_ERR_NO_LAYOUT = 7,    /* the handle holds no layout yet, or one for other sizes */
-    EP_ERR_TIMEOUT = 8       /* device: a bounded wait of a copy kernel gave up (about 1 s) */
+    EP_ERR_TIMEOUT = 8,      /* device: a bounded wait of a copy kernel gave up (about 1 s) */
+    EP_ERR_TIMEOUT_IN_FLIGHT = 9  /* device: as EP_ERR_TIMEOUT, and the kernel's wait for its own
+                                     row loads gave up too: a bulk load may have landed in shared
+                                     memory after the kernel exited, so nothing the device ran
+                                     afterwards can be trusted (start a new process) */
 } ep_status;
 
 typedef enum ep_layout {
@@ -322,6 +326,79 @@ ep_status ep_combine_send(ep_ctx *ctx, const ep_handle *handle, const void *d_y,
 ep_status ep_combine_recv(ep_ctx *ctx, const ep_handle *handle, const void *d_send_y,
                           const float *d_topk_weights, void *d_out, void *stream);
 
+/* Rank-deduplicated transport with a receive that runs no kernel (the hook-
+ * based overlap of "如何突破MoE通信瓶颈：DeepEP跨节点优化技术终极指南", section
+ * 技术解析, 通信-计算重叠技术: the receive occupies no SM, and the page's figure
+ * of the flow shows the CPU and GPU cooperating on the layout; the DeepTech
+ * announcement of DeepEP, 010bt.com: the normal kernels forward tokens per
+ * destination domain).  Tokens travel as in ep_get_rank_layout (once per
+ * destination rank), and everything source rank r sends to rank d is ONE
+ * contiguous run on both sides: the send buffer is ordered by (source rank,
+ * destination rank, token), and the rows rank d receives hold its tokens in
+ * ascending g = r*T + t.  A receive is then R*R copies, one per non-empty
+ * run, issued from the host; no kernel of this library runs.  R <= 32
+ * (EP_ERR_UNSUPPORTED otherwise).  Two wires move the runs:
+ *   EP_WIRE_DEVICE  one device-to-device cudaMemcpyAsync per run (and one
+ *                   per run of FP8 scales), spread over two internal
+ *                   streams forked from and joined back into `stream`.
+ *                   Runs at HBM speed; note that the CUDA driver carries out
+ *                   same-device copies with its own kernels on the SMs (on
+ *                   GB300 such copies wait for SMs held by other kernels).
+ *   EP_WIRE_HOST    through the caller's pinned host buffer h_stage on the
+ *                   copy engines only (device -> host, then host -> device,
+ *                   pipelined per source rank): occupies no SM, at the host
+ *                   link's speed (about 200 GB/s each way on GB300), the
+ *                   role the network plays on the pages.  h_stage holds
+ *                   ep_rank_send_rows rows of payload (H*2 bytes BF16, H
+ *                   FP8), followed (FP8 dispatch) by as many rows of H/32
+ *                   scale bytes; it must come from cudaMallocHost /
+ *                   cudaHostAlloc (EP_ERR_INVALID_ARG otherwise).
+ * The host needs the run sizes to issue the copies: the first wire call
+ * after a new layout waits (host synchronisation) for the end of the
+ * ep_rank_dispatch_send that computed it; later calls on the same layout
+ * wait for nothing and only enqueue.
+ *
+ * ep_rank_send_rows: rows of a send buffer, R*Tmax*min(K, R).  Host only.
+ * ep_rank_dispatch_send: the rank layout (as ep_get_rank_layout, outputs
+ *   d_recv_topk_idx / d_recv_topk_weights optional) plus its run sizes and
+ *   send rows, then each token cast once (FP8) and written to its send row
+ *   for every destination rank; d_topk_idx NULL reuses the handle's layout
+ *   (one made by this call, same tokens_per_rank: EP_ERR_NO_LAYOUT
+ *   otherwise) and only casts.  Kernels: layout, send rows, dispatch.
+ *     d_send_x       device [ep_rank_send_rows, H] e4m3 (FP8) or bf16
+ *     d_send_scales  device fp32 [ep_rank_send_rows, H/128] (FP8)
+ * ep_rank_dispatch_recv: the wire, send rows -> receive rows (and scales),
+ *   receive buffers as ep_dispatch writes them for a rank layout
+ *   (ep_rank_recv_rows rows), d_recv_count [R] the rows per rank.
+ * ep_rank_combine_send: the wire back: the expert output of each received
+ *   row (d_y, receive layout, bf16) to its send row of d_send_y
+ *   [ep_rank_send_rows, H] bf16.
+ * ep_rank_combine_recv: the rank-mode reduce (as ep_combine with weights
+ *   NULL on a rank layout) reading each token's rows from d_send_y, into
+ *   d_out [R*T, H].  One kernel.
+ * ep_rank_runs: the run table (host arrays of R*R entries, [r*R + d]; any
+ *   may be NULL): tokens source r sends to rank d, and the first send and
+ *   receive row of each run.  May wait like the wire calls.
+ * Results are identical, bit for bit, to ep_get_rank_layout + ep_dispatch /
+ * ep_combine on the same routing. */
+typedef enum ep_wire {
+    EP_WIRE_DEVICE = 0,
+    EP_WIRE_HOST = 1
+} ep_wire;
+ep_status ep_rank_send_rows(const ep_config *cfg, int64_t *rows);
+ep_status ep_rank_dispatch_send(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
+                                const float *d_topk_weights, int32_t tokens_per_rank, int32_t use_fp8,
+                                int32_t *d_recv_topk_idx, float *d_recv_topk_weights, ep_handle *handle,
+                                void *d_send_x, float *d_send_scales, void *stream);
+ep_status ep_rank_dispatch_recv(ep_ctx *ctx, ep_handle *handle, int32_t use_fp8, const void *d_send_x,
+                                const float *d_send_scales, void *d_recv_x, float *d_recv_scales,
+                                int32_t *d_recv_count, int32_t wire, void *h_stage, void *stream);
+ep_status ep_rank_combine_send(ep_ctx *ctx, ep_handle *handle, const void *d_y, void *d_send_y,
+                               int32_t wire, void *h_stage, void *stream);
+ep_status ep_rank_combine_recv(ep_ctx *ctx, const ep_handle *handle, const void *d_send_y, void *d_out,
+                               void *stream);
+ep_status ep_rank_runs(ep_handle *handle, int32_t *run_cnt, int64_t *send_off, int64_t *recv_off);
+
 /* chunk_tokens of ep_round_trip that asks for the automatic chunk size. */
 #define EP_CHUNK_AUTO (-1)
 
@@ -363,7 +440,7 @@ ep_status ep_round_trip_auto_chunk(const ep_ctx *ctx, int32_t use_fp8, int32_t r
  *   dispatch_kernel       0 = the built-in rule (the warp-item kernel for FP8
  *                         rows of H <= 1024, or H <= 2048 with topk <= 4, else
  *                         the row kernel where it applies), 1 = the row kernel (bulk copies of whole
- *                         rows; only where H % 512 == 0 and H <= 16384, the
+ *                         rows; only where H % 512 == 0 and H <= 15872, the
  *                         warp-item kernel elsewhere), 2 = the warp-item kernel
  *                         (16-byte stores by every lane) */
 typedef struct ep_tuning {
@@ -423,26 +500,50 @@ ep_status ep_get_autotune_log(const ep_ctx *ctx, ep_tune_record *records, int32_
  * no context or handle: every intermediate buffer lives in one static device
  * array that libep.so holds on each GPU that loads it (about 4.3 MB, kept
  * until the process exits).  It calls no cudaMalloc, cudaFree or allocating
- * library routine, so code inside a stream capture that must not allocate,
- * runtimes that give all device memory to their own allocator, and plugins
- * that may only use the memory they are handed can still dispatch.
+ * library routine, so runtimes that give all device memory to their own
+ * allocator up front, plugins that may only use the memory they are handed,
+ * and latency-critical code where a cudaMalloc could synchronise the device
+ * can still dispatch.
  *   cfg            sizes and layout, as for ep_create (host pointer)
  *   other args     as for ep_dispatch
  * Limits: R*tokens_per_rank*K <= 65536 entries, receive rows <= 1048576,
  * num_experts <= 1024; beyond them it returns EP_ERR_UNSUPPORTED and enqueues
- * nothing.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) and sets kernel attributes; make it before any stream
- * capture.  All calls share the array and each clears the status word it uses
- * first: calls whose work overlaps on the GPU race.  Device-detected errors
- * (ids outside [-1, E), padded overflow) drop the offending entries as in
- * ep_dispatch but are not reported (there is no context to report them to). */
+ * nothing (a launch the device refuses returns EP_ERR_UNSUPPORTED too, after
+ * the clear of the array's status word has been enqueued).  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) and sets
+ * kernel attributes; make it before any stream capture.  Every call looks the
+ * address up again and repeats that set-up if it moved (a cudaDeviceReset
+ * loads the module anew).  All calls share the array and each clears the
+ * status word it uses first: calls whose work overlaps on the GPU race.
+ * Device-detected errors (ids outside [-1, E), padded overflow) drop the
+ * offending entries as in ep_dispatch but are not reported (there is no
+ * context to report them to). */
 ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, const int64_t *d_topk_idx,
                               int32_t tokens_per_rank, int32_t use_fp8, void *d_recv_x,
                               float *d_recv_scales, int32_t *d_recv_count, void *stream);
 
 /* Synchronise `stream`, read and clear the context's device status word.
- * Returns EP_OK, EP_ERR_BAD_EXPERT, EP_ERR_CAPACITY, EP_ERR_TIMEOUT or EP_ERR_CUDA. */
+ * Returns EP_OK, EP_ERR_BAD_EXPERT, EP_ERR_CAPACITY, EP_ERR_TIMEOUT_IN_FLIGHT,
+ * EP_ERR_TIMEOUT or EP_ERR_CUDA (the first that applies, in this order). */
 ep_status ep_get_device_status(ep_ctx *ctx, void *stream);
+
+/* Test-only switches of a context (this library's own addition; the pages
+ * have no counterpart), for running a failure path that real inputs never
+ * reach without faulting or hanging the GPU:
+ *   move_withhold_item  an item of the copy kernels of ep_dispatch_recv (token
+ *                       g) and ep_combine_send (entry g*K + k) whose row load
+ *                       is never issued, so the bounded wait for it runs out
+ *                       and ep_get_device_status reports EP_ERR_TIMEOUT (no
+ *                       load is in flight for it); -1 = none (the default)
+ *   move_wait_ns        bound of each of those waits in ns; 0 = 1 s (the
+ *                       default), at most 10 s
+ * Values out of range: EP_ERR_INVALID_ARG and the switches are unchanged.
+ * Host only. */
+typedef struct ep_test_hooks {
+    int64_t move_withhold_item;
+    int64_t move_wait_ns;
+} ep_test_hooks;
+ep_status ep_set_test_hooks(ep_ctx *ctx, const ep_test_hooks *hooks);
 
 #ifdef __cplusplus
 }

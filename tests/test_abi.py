@@ -52,7 +52,7 @@ def _ctype_of(ctype: str, name: str):
     base = base.replace("*", "")
     scalars = {"int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64, "uint64_t": ctypes.c_uint64}
     structs = {"ep_config": ep.ep_config, "ep_handle_info": ep.ep_handle_info, "ep_tuning": ep.ep_tuning,
-               "ep_tune_record": ep.ep_tune_record}
+               "ep_tune_record": ep.ep_tune_record, "ep_test_hooks": ep.ep_test_hooks}
     if stars == 0:
         return scalars[base]
     if stars == 2:  # ep_ctx ** / ep_handle **: an opaque pointer written back
@@ -80,7 +80,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(9):
+    for s in range(10):
         assert ep.status_str(s) and ep.status_str(s) != "unknown status"
     assert ep.status_str(99) == "unknown status"
 
@@ -197,6 +197,22 @@ def test_host_rejections_of_the_range_split_and_tuning_calls(lib):
     assert lib.ep_autotune(None, None, None, 1, None, 0, None, None, None, None, 1, ctypes.byref(t), None) == E
     assert lib.ep_get_autotune_log(None, None, 0, ctypes.byref(n)) == E
     assert lib.ep_status_str(ep.EP_ERR_TIMEOUT).decode() == "a bounded wait on the device gave up"
+    h = ep.ep_test_hooks(-1, 0)
+    assert lib.ep_set_test_hooks(None, ctypes.byref(h)) == E
+
+
+def test_host_rejections_of_the_rank_transport(lib):
+    """The rank transport's calls reject a NULL context / handle before any
+    CUDA call, and its send-buffer size query answers R*Tmax*min(K, R)."""
+    E = ep.EP_ERR_INVALID_ARG
+    assert lib.ep_rank_dispatch_send(None, None, None, None, 0, 0, None, None, None, None, None, None) == E
+    assert lib.ep_rank_dispatch_recv(None, None, 0, None, None, None, None, None, 0, None, None) == E
+    assert lib.ep_rank_combine_send(None, None, None, None, 0, None, None) == E
+    assert lib.ep_rank_combine_recv(None, None, None, None, None) == E
+    assert lib.ep_rank_runs(None, None, None, None) == E
+    for R, Tmax, K in ((8, 4096, 8), (32, 128, 8), (4, 32, 2), (2, 7, 6)):
+        cfg = ep.make_config(R, Tmax, 1024, 4 * R, K)
+        assert ep.ep_rank_send_rows(cfg) == R * Tmax * min(K, R)
 
 
 def test_receive_row_counts_match_the_definitions_and_the_oracle(lib):
@@ -226,7 +242,8 @@ def test_struct_layouts_match_header(tmp_path):
     if shutil.which("gcc") is None:
         pytest.skip("needs gcc")
     structs = {"ep_config": ep.ep_config, "ep_tuning": ep.ep_tuning,
-               "ep_tune_record": ep.ep_tune_record, "ep_handle_info": ep.ep_handle_info}
+               "ep_tune_record": ep.ep_tune_record, "ep_handle_info": ep.ep_handle_info,
+               "ep_test_hooks": ep.ep_test_hooks}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "ep.h"', "int main(void) {"]
     for s, cls in structs.items():
         lines.append(f'    printf("{s} size %zu\\n", sizeof({s}));')

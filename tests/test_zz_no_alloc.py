@@ -1,20 +1,25 @@
 """ep_dispatch_noalloc, the dispatch for callers that cannot allocate device
-memory (inside a capture that must not allocate, under a runtime that owns all
-device memory, in a plugin limited to the buffers it is handed): it keeps its
-intermediate state in the library's static device array instead of buffers
-from cudaMalloc.  Its receive rows, FP8 scales and per-expert counts must be
-bit-identical to ep_dispatch's, on two calls in a row with different inputs
-(the second call reuses the array the first one left behind).
+memory (under a runtime that owns all device memory, in a plugin limited to
+the buffers it is handed, on a path where a cudaMalloc could synchronise the
+device): it keeps its intermediate state in the library's static device array
+instead of buffers from cudaMalloc.  Its receive rows, FP8 scales and
+per-expert counts must be bit-identical to ep_dispatch's, on two calls in a
+row with different inputs (the second call reuses the array the first one
+left behind); they must also equal the oracle's when some entries are
+dropped (ids outside [-1, E), a padded expert buffer offered more entries
+than it holds), with nothing written past the oracle's rows; and repeated
+calls must not change the device's free memory.
 
 Kept in a file of its own that pytest collects last."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from combine_get_dispatch_02_gb300 import build as epbuild
 from combine_get_dispatch_02_gb300 import ep
 from combine_get_dispatch_02_gb300 import workloads as wl
-from helpers import bits_to_bf16, make_buffer
+from helpers import ORACLE_LAYOUT, bits_to_bf16, e4m3_to_bits, make_buffer
 
 pytestmark = pytest.mark.gpu
 
@@ -24,6 +29,7 @@ def _setup():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     epbuild.build()
+    oracle.build()
     torch.cuda.set_device(0)
 
 
@@ -76,3 +82,79 @@ def test_noalloc_rejects_sizes_beyond_its_limit():
     with pytest.raises(ep.EPError) as e:
         ep.ep_dispatch_noalloc(cfg, x, idx, w.tokens_per_rank, False, recv, None, None)
     assert e.value.status == ep.EP_ERR_UNSUPPORTED
+
+
+SENTINEL = 0x3C
+
+
+def _drop_cases():
+    w = wl.TINY
+    d = wl.generate(w)
+    bad = d["topk_idx"].copy()
+    rng = np.random.default_rng(77)
+    pick = rng.random(bad.shape) < 0.08
+    bad[pick] = rng.choice([-3, -2, w.num_experts, w.num_experts + 5, 1 << 40], size=int(pick.sum()))
+    bad[0, 0, :] = -1
+    over = np.zeros_like(d["topk_idx"])  # every entry on expert 0: 512 entries for 128 rows
+    over[:, :, 1] = 3
+    return [("bad_ids_bf16", w, bad), ("bad_ids_fp8", w.with_(use_fp8=True, x_scale="loguniform"), bad),
+            ("overflow_fp8", w.with_(use_fp8=True), over),
+            ("bad_ids_packed_fp8", w.with_(use_fp8=True, layout=wl.PACKED), bad)]
+
+
+@pytest.mark.parametrize("case", range(4))
+def test_noalloc_matches_oracle_and_drops_bad_entries(case):
+    name, w, idx = _drop_cases()[case]
+    d = wl.generate(w)
+    N, H = w.num_tokens, w.hidden
+    o = oracle.layout(idx, w.num_experts, w.max_tokens_per_rank, ORACLE_LAYOUT[w.layout])
+    assert (o["n_bad"] > 0) or (o["n_overflow"] > 0), name
+    cfg = ep.make_config(w.num_ranks, w.max_tokens_per_rank, H, w.num_experts, w.topk,
+                         ep.EP_LAYOUT_PADDED if w.layout == wl.PADDED else ep.EP_LAYOUT_PACKED)
+    rows = ep.ep_recv_rows(cfg)
+    if w.use_fp8:
+        recv = torch.full((rows, H), SENTINEL, dtype=torch.uint8, device="cuda")
+        sc = torch.full((rows, H // 128), -1.0, dtype=torch.float32, device="cuda")
+    else:
+        recv, sc = torch.full((rows, 2 * H), SENTINEL, dtype=torch.uint8, device="cuda"), None
+    cnt = torch.full((w.num_experts,), -9, dtype=torch.int32, device="cuda")
+    x = bits_to_bf16(d["x_bits"])
+    ep.ep_dispatch_noalloc(cfg, x, torch.from_numpy(idx).cuda(), w.tokens_per_rank, w.use_fp8,
+                           recv.view(torch.float8_e4m3fn) if w.use_fp8 else recv.view(torch.bfloat16), sc, cnt)
+    torch.cuda.synchronize()
+    assert np.array_equal(cnt.cpu().numpy(), o["tokens_per_expert"])
+    got = recv.cpu().numpy()
+    x2 = d["x_bits"].reshape(N, H)
+    written = o["slot"][o["slot"] >= 0]
+    if w.use_fp8:
+        q, s = oracle.dispatch(x2, o["slot"], o["rows"], True)
+        assert np.array_equal(got[written], q[written])
+        assert np.array_equal(sc.cpu().numpy()[written].view(np.uint32), s[written].view(np.uint32))
+        untouched_sc = np.setdiff1d(np.arange(rows), written)
+        assert np.all(sc.cpu().numpy()[untouched_sc] == -1.0)
+    else:
+        ref = oracle.dispatch(x2, o["slot"], o["rows"], False)
+        assert np.array_equal(got[written].view(np.uint16), ref[written])
+    untouched = np.setdiff1d(np.arange(rows), written)
+    assert np.all(got[untouched] == SENTINEL)  # dropped entries and unused rows are not written
+
+
+def test_noalloc_repeated_calls_leave_free_memory_unchanged():
+    w = wl.LL.with_(tokens_per_rank=64, max_tokens_per_rank=64)
+    d = wl.generate(w)
+    x = bits_to_bf16(d["x_bits"])
+    idx = torch.from_numpy(d["topk_idx"]).cuda()
+    _noalloc(w, x, idx)  # warm-up: the module and its kernels are loaded
+    cfg = ep.make_config(w.num_ranks, w.max_tokens_per_rank, w.hidden, w.num_experts, w.topk)
+    rows = ep.ep_recv_rows(cfg)
+    recv = torch.empty(rows, w.hidden, dtype=torch.float8_e4m3fn, device="cuda")
+    sc = torch.empty(rows, w.hidden // 128, dtype=torch.float32, device="cuda")
+    cnt = torch.empty(w.num_experts, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    for _ in range(3):
+        ep.ep_dispatch_noalloc(cfg, x, idx, w.tokens_per_rank, True, recv, sc, cnt)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == alloc0
