@@ -67,6 +67,8 @@ def _args():
                     help="reps of each split (send / receive-hook) call (0: skip)")
     ap.add_argument("--round-trip-reps", type=int, default=50,
                     help="reps per chunk size of the dispatch -> identity expert -> combine round trip (0: skip)")
+    ap.add_argument("--wire-reps", type=int, default=10,
+                    help="with --rank: reps of the rank transport's wire calls (device and host wire; 0: skip)")
     return ap.parse_args()
 
 
@@ -628,6 +630,14 @@ def run_ours(args):
         }
         del send_y
 
+    # the rank transport whose receive runs no kernel: send (layout + send
+    # rows + cast), then the runs moved by the device wire (driver copies) or
+    # the host wire (copy engines through pinned host memory), and each wire
+    # beside GEMMs on another stream
+    wire = None
+    if args.rank and args.wire_reps > 0 and w.num_ranks <= 32:
+        wire = _rank_wire(args, w, buf, ctx, x, idx, wts, h, y, out, stream, timed)
+
     # HBM copy bandwidth of this GPU through torch (context for the fractions)
     cbuf = torch.empty(2 << 30, dtype=torch.uint8, device="cuda")
     cdst = torch.empty_like(cbuf)
@@ -645,9 +655,84 @@ def run_ours(args):
             torch.distributed.destroy_process_group()
         return
     _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
-            e2e, clk, graph_us, copy_gbs, round_trip, split, tuning, split_step_ms, backward)
+            e2e, clk, graph_us, copy_gbs, round_trip, split, tuning, split_step_ms, backward, wire)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def _rank_wire(args, w, buf, ctx, x, idx, wts, h, y, out, stream, timed):
+    """Timings of the rank transport with a kernel-free receive (see
+    ep_rank_dispatch_recv): each call alone, and each wire on a second stream
+    beside back-to-back 4096^3 bf16 GEMMs on this stream (as many as take
+    about as long as the wire), with the fraction of the wire's time hidden."""
+    import torch
+    from combine_get_dispatch_02_gb300 import ep
+    N, K, H, R = w.num_tokens, w.topk, w.hidden, w.num_ranks
+    fp8 = w.use_fp8
+    reps = args.wire_reps
+    rows = ep.ep_rank_send_rows(buf.cfg)
+    if fp8:
+        send_x = torch.empty(rows, H, dtype=torch.float8_e4m3fn, device="cuda")
+        send_sc = torch.empty(rows, H // 128, dtype=torch.float32, device="cuda")
+    else:
+        send_x, send_sc = torch.empty(rows, H, dtype=torch.bfloat16, device="cuda"), None
+    send_y = torch.empty(rows, H, dtype=torch.bfloat16, device="cuda")
+    row_b = H + H // 32 if fp8 else 2 * H
+    stage = torch.empty(rows * max(row_b, 2 * H), dtype=torch.uint8).pin_memory()
+    recv, scales = buf.alloc_rank_recv(fp8)
+    hw = buf.new_handle()
+    T = w.tokens_per_rank
+    send_us = timed(lambda: ep.ep_rank_dispatch_send(ctx, x, idx, wts, T, fp8, None, None, hw.raw, send_x, send_sc,
+                                                     stream), reps)[0]
+    runs, _, _ = ep.ep_rank_runs(hw.raw, R)
+    moved = sum(map(sum, runs))
+    res = {"send_with_layout_median_us": send_us, "rows_moved": moved, "runs": sum(c > 0 for r in runs for c in r)}
+    ga = torch.randn(4096, 4096, device="cuda").to(torch.bfloat16)
+    gb = torch.randn(4096, 4096, device="cuda").to(torch.bfloat16)
+    gc = torch.empty(4096, 4096, dtype=torch.bfloat16, device="cuda")
+    s2 = torch.cuda.Stream()
+    t_one = timed(lambda: torch.matmul(ga, gb, out=gc), reps)[0]
+    for name, wire_id in (("device", ep.EP_WIRE_DEVICE), ("host", ep.EP_WIRE_HOST)):
+        st = stage if wire_id == ep.EP_WIRE_HOST else None
+
+        def recv_hook(s, wire_id=wire_id, st=st):
+            ep.ep_rank_dispatch_recv(ctx, hw.raw, fp8, send_x, send_sc, recv, scales, None, wire_id, st, s)
+
+        def csend(s, wire_id=wire_id, st=st):
+            ep.ep_rank_combine_send(ctx, hw.raw, y_w, send_y, wire_id, st, s)
+
+        # expert outputs in the receive layout: the bf16 receive rows themselves (timing only)
+        y_w = recv if not fp8 else torch.zeros(buf.rank_rows, H, dtype=torch.bfloat16, device="cuda")
+        t_recv = timed(lambda: recv_hook(stream), reps)[0]
+        t_csend = timed(lambda: csend(stream), reps)[0]
+        n_gemm = max(1, int(round(t_recv / t_one)))
+
+        def gemms():
+            for _ in range(n_gemm):
+                torch.matmul(ga, gb, out=gc)
+
+        def both():
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            s2.wait_event(ev)
+            gemms()
+            recv_hook(s2)
+            stream.wait_stream(s2)
+
+        t_g = timed(gemms, reps)[0]
+        t_b = timed(both, reps)[0]
+        moved_b = moved * row_b
+        res[name] = {"dispatch_recv_median_us": t_recv, "dispatch_recv_gbs": moved_b / t_recv / 1e3,
+                     "combine_send_median_us": t_csend, "combine_send_gbs": moved * 2 * H / t_csend / 1e3,
+                     "beside_gemms": {"gemms": n_gemm, "gemms_us": t_g, "recv_us": t_recv, "both_us": t_b,
+                                      "hidden_fraction_of_recv": (t_g + t_recv - t_b) / t_recv}}
+        del y_w
+    res["combine_recv_median_us"] = timed(lambda: ep.ep_rank_combine_recv(ctx, hw.raw, send_y, out, stream), reps)[0]
+    res["note"] = ("receive = one copy per (source rank, destination rank) run issued from the host, no kernel of "
+                   "this library; device wire: same-device cudaMemcpyAsync (the driver runs these on SMs); host "
+                   "wire: device->pinned host->device on the copy engines (no SM); GB/s count each moved byte once")
+    del ga, gb, gc, send_x, send_sc, send_y, stage
+    return res
 
 
 def _e2e(args, w, d, x, idx, wts, out, enqueue, stream):
@@ -747,7 +832,7 @@ def _e2e(args, w, d, x, idx, wts, out, enqueue, stream):
 
 def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, lay_us, disp_us, comb_us,
             e2e, clk, graph_us=None, copy_gbs=None, round_trip=None, split=None, tuning=None,
-            split_step_ms=None, backward=None):
+            split_step_ms=None, backward=None, wire=None):
     peak, peak_kind = _peaks()
     disp_bytes, disp_kernel_bytes, comb_bytes = _algorithmic_bytes(w, M)
     comb_avg_s = statistics.mean(comb_ms) / 1e3
@@ -795,9 +880,16 @@ def _report(args, w, ws, M, N, step_ms, disp_ms, comb_ms, ms_per_step, value, la
                               "peak": peak, "unit": "GB/s", "frac": disp_gbs / peak if disp_gbs else None,
                               "traffic": _traffic("dispatch", DISPATCH_SRC, w.name),
                               "algorithmic_bytes": disp_kernel_bytes},
+        "roofline_step": {"bound": "hbm", "achieved": (disp_bytes + comb_bytes) / (ms_per_step / 1e3) / 1e9,
+                          "peak": peak, "unit": "GB/s",
+                          "frac": (disp_bytes + comb_bytes) / (ms_per_step / 1e3) / 1e9 / peak,
+                          "algorithmic_bytes": disp_bytes + comb_bytes,
+                          "note": "the whole step (layout + dispatch + combine) over its mean time: no kernel's "
+                                  "writes are still in L2 when it ends"},
         "e2e": e2e,
         "round_trip": round_trip,
         "split": split,
+        "rank_wire": wire,
         "backward": backward,
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
