@@ -294,6 +294,10 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
             if (lane == 0 && it >= kLag) mbar_arrive(smem_addr(&empty[(it - kLag) % NB]));
         }
         if (!ok && lane == 0 && p.status != nullptr) atomicOr(p.status, kStatusTimeout);
+        // every copy of this CTA is issued: the kernel queued behind (e.g. the
+        // combine) may start its CTAs now; its griddepcontrol.wait still
+        // waits for this grid to complete and its writes to be visible
+        pdl_launch_dependents();
         if (lane < K) bulk_wait_all();  // copies read shared memory until they finish
         return;
     }

@@ -148,7 +148,11 @@ int grid_cap(const ep_ctx *ctx, int blocks_per_sm) {
 cudaError_t launch_layout_any(const ep_ctx *ctx, ep::LayoutParams &p, const ep_handle *h, cudaStream_t stream) {
     const int64_t entries = p.N * p.K;
     p.cta_hist = h->cta_hist;
-    if (entries >= (p.rank_mode ? ep::kLayoutGridEntriesRank : ep::kLayoutGridEntries)) {
+    p.grid_bar = reinterpret_cast<uint32_t *>(h->cta_hist + grid_hist_ints(ctx));
+    const int form = ctx->tune.layout_form;
+    const bool grid = form == 2 || (form == 0 && entries >= (p.rank_mode ? ep::kLayoutGridEntriesRank
+                                                                         : ep::kLayoutGridEntries));
+    if (grid && p.N > 0) {
         int sms = ctx->num_sms;
         if (ctx->cfg.max_sms > 0 && ctx->cfg.max_sms < sms) sms = ctx->cfg.max_sms;
         const cudaError_t e = ep::launch_layout_grid(p, sms, stream);
@@ -1267,6 +1271,7 @@ ep_status ep_set_tuning(ep_ctx *ctx, const ep_tuning *t) {
         return EP_ERR_INVALID_ARG;
     if (t->round_trip_chunk < 0) return EP_ERR_INVALID_ARG;
     if (t->dispatch_kernel < 0 || t->dispatch_kernel > 2) return EP_ERR_INVALID_ARG;
+    if (t->layout_form < 0 || t->layout_form > 2) return EP_ERR_INVALID_ARG;
     if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
     ctx->tune = *t;
     ctx->combine_bps_tuned = t->combine_chunks > 0 ? ep::combine_blocks_per_sm(0, t->combine_chunks) : 0;

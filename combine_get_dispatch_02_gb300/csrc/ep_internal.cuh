@@ -42,6 +42,7 @@ struct LayoutParams {
     int32_t er_span;           // set by launch_layout: ranks per CTA for the (e, r) counts
     // grid form (launch_layout_grid): per-CTA key totals -> prefixes [grid_ctas][E]
     int32_t *cta_hist;
+    uint32_t *grid_bar;           // grid form: barrier counter (zeroed before each launch)
     int32_t grid_ctas, grid_tpc;  // set by launch_layout_grid: CTAs, tokens per CTA
 };
 
@@ -56,16 +57,19 @@ size_t layout_smem_bytes(int E, int R, int threads, int cluster_size);
 bool layout_pick_shape(int E, int R, int *cluster_size, int *threads, bool many_entries = false);
 // Entries (R*T*K) from which the many-entries shape is used.
 constexpr int64_t kLayoutManyEntries = 65536;
-// The same layout from three kernels spread over `ctas` CTAs (count, scan,
-// write), for many entries: the single cluster leaves most SMs idle.  Needs
-// p.cta_hist with ctas * E ints.  Zeroes tokens_per_rank / cnt_er itself.
+// The same layout from one cooperative kernel over `ctas` CTAs (count, scan,
+// write, between grid barriers), for many entries: the single cluster leaves
+// most SMs idle.  Needs p.cta_hist with ctas * E ints and p.grid_bar.  Zeroes
+// the barrier, tokens_per_rank and cnt_er itself.  ctas <= 512.
 cudaError_t launch_layout_grid(LayoutParams p, int ctas, cudaStream_t stream);
-// Entries from which the grid form is used (measured crossovers, layout +
-// dispatch: below them the single cluster wins because the dispatch casts
-// rows on the SMs the cluster leaves free; the rank-deduplicated keys cost
-// more per entry, so that layout switches earlier).
-constexpr int64_t kLayoutGridEntries = 524288;
-constexpr int64_t kLayoutGridEntriesRank = 262144;
+// Entries from which the grid form is used (measured crossovers of the time
+// layout + dispatch adds to dispatch alone: expert layout 32K / 64K entries
+// cluster ahead by 9 / 3-5 us, 256K grid ahead by 14 us; rank layout grid
+// ahead from 48K entries, tied at 32K; below them the single cluster wins
+// because it has no grid barriers and no zeroing copies, and the dispatch
+// casts rows on the SMs it leaves free).
+constexpr int64_t kLayoutGridEntries = 131072;
+constexpr int64_t kLayoutGridEntriesRank = 49152;
 
 // ------------------------------------------------------------------ dispatch
 struct DispatchParams {

@@ -427,39 +427,89 @@ bool fits(int E, int R, int cl) {
 }
 
 // ---------------------------------------------------------------- grid form
-// The same layout for many entries, from three kernels over the whole GPU
-// (the single cluster above uses 16 SMs):
-//   count  (C CTAs)  pass 1 over the CTA's token range, as in the cluster
-//                    kernel; each entry's (position among the CTA's entries of
-//                    its key, key) is staged in its slot cell; the CTA's key
-//                    totals go to cta_hist[c][key]
-//   scan   (1 CTA)   cta_hist[c][e] -> entries of e in CTAs below c; totals,
-//                    bases and counts; per-(expert, rank) offsets
-//   write  (C CTAs)  slot = base + prefix + position, src_info, rank-mode rows
-// Chained with programmatic dependent launch; the write kernel lets the
-// dispatch queued behind it start casting rows at once.
+// The same layout for many entries from ONE cooperative kernel over the whole
+// GPU (the single cluster above uses 16 SMs), C CTAs, all resident at once
+// (cooperative launch), with two grid barriers:
+//   count    pass 1 over the CTA's token range, as in the cluster kernel:
+//            each entry's (position among its warp's entries of its key,
+//            key) is staged in its slot cell, the warp prefixes stay in
+//            shared memory, the CTA's key totals go to cta_hist[c][key]
+//   barrier
+//   scan     CTA c owns keys [c*E/C, (c+1)*E/C): per owned key one block scan
+//            over the C CTA totals turns cta_hist[.][key] into entries of the
+//            key in lower CTAs; totals, counts, padded bases, per-(expert,
+//            rank) offsets
+//   barrier
+//   write    packed bases (a block scan of the totals, in every CTA), then
+//            slot = base + prefix + position, src_info, rank-mode rows
+// The barriers are a counter the host zeroes before the launch; each wait is
+// bounded (about one second): on expiry the kernel sets kStatusTimeout and
+// returns.  The dispatch queued behind (programmatic dependent launch) may
+// start casting rows at once.
 constexpr int kGridThreads = 512;
+constexpr uint64_t kGridWaitNs = 1000000000ull;
 
-__global__ void __launch_bounds__(kGridThreads) layout_count_kernel(const LayoutParams p) {
+__device__ __forceinline__ uint64_t grid_now_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Arrive at the grid barrier and wait (bounded) until `target` CTAs have
+// arrived.  Every CTA of the grid is resident (cooperative launch), so the
+// wait ends unless something is broken.  False when it gave up.
+__device__ bool grid_barrier(uint32_t *bar, uint32_t target, int *flag) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();  // this CTA's writes before the arrival
+        atomicAdd(bar, 1u);
+        bool ok = true;
+        const uint64_t t0 = grid_now_ns();
+        while (ld_acquire_gpu(bar) < target) {
+            if (grid_now_ns() - t0 > kGridWaitNs) {
+                ok = false;
+                break;
+            }
+        }
+        __threadfence();
+        *flag = ok ? 1 : 0;
+    }
+    __syncthreads();
+    return *flag != 0;
+}
+
+__global__ void __launch_bounds__(kGridThreads, 1) layout_grid_kernel(const LayoutParams p) {
+    // the dispatch kernel queued behind this one may start loading and
+    // casting token rows now; it waits for these results before it reads a slot
+    pdl_launch_dependents();
     constexpr int NT = kGridThreads, NW = NT / 32;
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int E = p.E, R = p.R, K = p.K, T = p.T;
     const int N = (int)p.N;
-    const int c = blockIdx.x;
+    const int c = blockIdx.x, C = gridDim.x;
     const int ebits = bits_for(E + 1);
     extern __shared__ int32_t sm[];
     int32_t *hist_w = sm;                 // [NW][E] warp counts -> warp start positions in the CTA
     int32_t *tok_rank = hist_w + NW * E;  // [R]
     const int span = p.er_span;
-    int32_t *hist_er = tok_rank + R;      // [E][span]
+    int32_t *hist_er = tok_rank + R;      // [E][span] (at least [E]: the bases in the write phase)
+    int32_t *pre = hist_er + max(E * span, E);  // [E] entries of each key in lower CTAs
+    int32_t *scan = pre + E;              // [NW + 1]
+    __shared__ int bar_ok;
     const int cta_t0 = min(N, c * p.grid_tpc), cta_t1 = min(N, cta_t0 + p.grid_tpc);
     const int tpw = (p.grid_tpc + NW - 1) / NW;
     const int t0 = min(cta_t1, cta_t0 + w * tpw), t1 = min(cta_t1, t0 + tpw);
     const int i0 = t0 * K, i1 = t1 * K;
-    int32_t *stage = p.slot;  // (position, key) of each entry until the write kernel
+    int32_t *stage = p.slot;  // (position in warp, key) of each entry until the write phase
     const bool want_er = p.cnt_er != nullptr;
     const int r0 = T > 0 ? cta_t0 / T : 0;
 
+    // ---------------- count
     int64_t raw[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) raw[u] = load_raw(p.topk_idx, i0 + u * 32 + lane, i1);
@@ -469,7 +519,6 @@ __global__ void __launch_bounds__(kGridThreads) layout_count_kernel(const Layout
         for (int b = cta_t0 * R + tid; b < cta_t1 * R; b += NT) p.is_token_in_rank[b] = 0;
     }
     __syncthreads();
-
     const int erbits = bits_for(E * span + 1);
     for (int ib = i0; ib < i1; ib += 32 * kU) {
         if (ib != i0) {
@@ -514,7 +563,7 @@ __global__ void __launch_bounds__(kGridThreads) layout_count_kernel(const Layout
         }
     }
     __syncthreads();
-    // per key: exclusive prefix over the CTA's warps; the CTA total to global
+    // per key: exclusive prefix over the CTA's warps (kept); the CTA total to global
     for (int e = tid; e < E; e += NT) {
         int s = 0;
         for (int ww = 0; ww < NW; ++ww) {
@@ -530,85 +579,75 @@ __global__ void __launch_bounds__(kGridThreads) layout_count_kernel(const Layout
     if (want_er)  // zeroed before this kernel
         for (int j = tid; j < E * span; j += NT)
             if (hist_er[j] != 0) atomicAdd(&p.cnt_er[(j / span) * R + r0 + j % span], hist_er[j]);
-    __syncthreads();
-    // positions relative to the CTA (the lane that staged an entry rewrites it)
-    for (int i = i0 + lane; i < i1; i += 32) {
-        const int v = stage[i];
-        const int e = (v & 2047) - 1;
-        if (e >= 0) stage[i] = ((hist_w[w * E + e] + (v >> 11)) << 11) | (e + 1);
+    if (!grid_barrier(p.grid_bar, (uint32_t)C, &bar_ok)) {
+        if (tid == 0) atomicOr(p.status, kStatusTimeout);
+        return;
     }
-}
 
-__global__ void __launch_bounds__(1024) layout_scan_kernel(const LayoutParams p) {
-    __shared__ int32_t tot[1024];
-    __shared__ int32_t scan[1024 / 32 + 1];
-    pdl_wait();
-    const int E = p.E, C = p.grid_ctas, R = p.R;
-    // Q lanes per key (a power of two <= 32, so a key's lanes share a warp),
-    // each summing a contiguous slice of the CTAs with independent loads;
-    // a shuffle scan inside the group gives each slice its start
-    int Q = 1;
-    while (Q < 32 && Q * 2 * E <= 1024) Q *= 2;
-    const int ke = threadIdx.x / Q, q = threadIdx.x % Q;
-    const int per = (C + Q - 1) / Q;
-    const int c0 = min(C, q * per), c1 = min(C, c0 + per);
-    int local = 0;
-    if (ke < E)
-        for (int c = c0; c < c1; ++c) local += p.cta_hist[(int64_t)c * E + ke];
-    int incl = local;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d, Q);  // within groups of Q lanes
-        if (q >= d) incl += y;
-    }
-    if (ke < E) {
-        int run = incl - local;
-        for (int c = c0; c < c1; ++c) {
-            const int v = p.cta_hist[(int64_t)c * E + ke];
-            p.cta_hist[(int64_t)c * E + ke] = run;
-            run += v;
+    // ---------------- scan of the keys this CTA owns
+    const int ke0 = (int)((int64_t)c * E / C), ke1 = (int)((int64_t)(c + 1) * E / C);
+    for (int e = ke0; e < ke1; ++e) {
+        const int v = tid < C ? __ldcg(&p.cta_hist[(int64_t)tid * E + e]) : 0;
+        int total;
+        const int excl = block_exclusive_scan<NT>(v, scan, &total);
+        if (tid < C) p.cta_hist[(int64_t)tid * E + e] = excl;
+        if (tid == 0) {
+            const int n = (int)min((int64_t)total, p.cap);
+            p.tokens_per_expert[e] = n;
+            if (p.user_tokens_per_expert) p.user_tokens_per_expert[e] = n;
+            if (p.layout == kLayoutPadded) p.base[e] = (int64_t)e * p.cap;
         }
-        if (q == Q - 1) tot[ke] = incl;
-    }
-    __syncthreads();
-    const int e = threadIdx.x;  // E <= 1024
-    int total;
-    const int excl = block_exclusive_scan<1024>(e < E ? tot[e] : 0, scan, &total);
-    if (e < E) {
-        const int64_t b = p.layout == kLayoutPadded ? (int64_t)e * p.cap : (int64_t)excl;
-        const int n = (int)min((int64_t)tot[e], p.cap);
-        p.tokens_per_expert[e] = n;
-        if (p.user_tokens_per_expert) p.user_tokens_per_expert[e] = n;
-        p.base[e] = b;
-        if (p.cnt_er != nullptr) {  // offsets over the source ranks
+        if (want_er && w == 0) {  // offsets over the source ranks
             int run = 0;
-            for (int r = 0; r < R; ++r) {
-                const int v = p.cnt_er[e * R + r];
-                p.off_er[e * R + r] = run;
-                run += v;
+            for (int rr = 0; rr < R; rr += 32) {
+                const int r = rr + lane;
+                const int cv = r < R ? __ldcg(&p.cnt_er[e * R + r]) : 0;
+                int x = cv;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int y = __shfl_up_sync(0xFFFFFFFFu, x, d);
+                    if (lane >= d) x += y;
+                }
+                if (r < R) p.off_er[e * R + r] = run + x - cv;
+                run += __shfl_sync(0xFFFFFFFFu, x, 31);
             }
         }
     }
-}
+    if (!grid_barrier(p.grid_bar, 2u * (uint32_t)C, &bar_ok)) {
+        if (tid == 0) atomicOr(p.status, kStatusTimeout);
+        return;
+    }
 
-__global__ void __launch_bounds__(kGridThreads) layout_write_kernel(const LayoutParams p) {
-    // the dispatch queued behind may start loading and casting rows now; it
-    // waits for this kernel's results before it reads a slot
-    pdl_launch_dependents();
-    pdl_wait();
-    const int E = p.E, K = p.K, N = (int)p.N;
-    const int c = blockIdx.x;
-    const int cta_t0 = min(N, c * p.grid_tpc), cta_t1 = min(N, cta_t0 + p.grid_tpc);
-    const int i0 = cta_t0 * K, i1 = cta_t1 * K;
+    // ---------------- write
+    // pre[e] = first row of key e for this CTA's entries: base + lower CTAs
+    {
+        const int chunk = (E + NT - 1) / NT;
+        const int e_lo = min(E, tid * chunk), e_hi = min(E, e_lo + chunk);
+        int local = 0;
+        if (p.layout != kLayoutPadded)
+            for (int e = e_lo; e < e_hi; ++e) local += __ldcg(&p.tokens_per_expert[e]);
+        int total;
+        int run = block_exclusive_scan<NT>(local, scan, &total);
+        for (int e = e_lo; e < e_hi; ++e) {
+            const int64_t b = p.layout == kLayoutPadded ? (int64_t)e * p.cap : (int64_t)run;
+            if (p.layout != kLayoutPadded) {
+                run += __ldcg(&p.tokens_per_expert[e]);
+                if (c == 0) p.base[e] = b;
+            }
+            pre[e] = __ldcg(&p.cta_hist[(int64_t)c * E + e]);
+            hist_er[e] = (int32_t)b;  // the (e, r) counts are done with: reuse for the bases
+        }
+    }
+    __syncthreads();
     const int cap = (int)min(p.cap, (int64_t)0x7FFFFFFF);
-    for (int i = i0 + threadIdx.x; i < i1; i += kGridThreads) {
-        const int v = p.slot[i];
+    for (int i = i0 + lane; i < i1; i += 32) {
+        const int v = stage[i];
         const int e = (v & 2047) - 1;
         int32_t s = -1;
         if (e >= 0) {
-            const int pos = p.cta_hist[(int64_t)c * E + e] + (v >> 11);
+            const int pos = pre[e] + hist_w[w * E + e] + (v >> 11);
             if (pos < cap) {
-                s = (int32_t)(p.base[e] + pos);
+                s = hist_er[e] + pos;
                 p.src_info[s] = i;
                 if (p.recv_topk_idx != nullptr) {  // rank mode: the token's experts on rank e
                     const int g0 = (i / K) * K;
@@ -629,15 +668,16 @@ __global__ void __launch_bounds__(kGridThreads) layout_write_kernel(const Layout
     }
 }
 
-size_t grid_count_smem(int E, int R, int span) {
-    return ((size_t)(kGridThreads / 32) * E + R + (size_t)E * span) * sizeof(int32_t);
+size_t grid_smem(int E, int R, int span) {
+    const int hist_er = E * span > E ? E * span : E;  // reused for the bases in the write phase
+    return ((size_t)(kGridThreads / 32) * E + R + (size_t)hist_er + E + kGridThreads / 32 + 1) * sizeof(int32_t);
 }
 
 void grid_init() {
     int dev = 0, optin = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    cudaFuncSetAttribute(layout_grid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 64);
     cudaGetLastError();
 }
 
@@ -664,8 +704,8 @@ bool layout_pick_shape(int E, int R, int *cluster_size, int *threads, bool many_
 
 cudaError_t launch_layout_grid(LayoutParams p, int ctas, cudaStream_t stream) {
     const int64_t N = p.N;
-    if (N <= 0 || ctas < 1) return cudaErrorInvalidValue;
-    // tokens per CTA; a CTA's entries are packed into 20 bits between the kernels
+    if (N <= 0 || ctas < 1 || ctas > kGridThreads || p.grid_bar == nullptr) return cudaErrorInvalidValue;
+    // tokens per CTA; a warp's entries are packed into 20 bits until the write phase
     int64_t tpc = (N + ctas - 1) / ctas;
     if (tpc * p.K >= (int64_t(1) << 20)) return cudaErrorInvalidConfiguration;
     const int C = (int)((N + tpc - 1) / tpc);
@@ -677,35 +717,27 @@ cudaError_t launch_layout_grid(LayoutParams p, int ctas, cudaStream_t stream) {
         const int64_t span = p.T > 0 ? (tpc + p.T - 1) / p.T + 1 : 1;
         p.er_span = (int)(span < p.R ? span : p.R);
     }
-    const size_t smem = grid_count_smem(p.E, p.R, p.er_span);
+    const size_t smem = grid_smem(p.E, p.R, p.er_span);
     if (smem > kMaxSmem) return cudaErrorInvalidConfiguration;
-    cudaError_t e = cudaSuccess;
-    if (p.tokens_per_rank != nullptr) e = cudaMemsetAsync(p.tokens_per_rank, 0, (size_t)p.R * sizeof(int32_t), stream);
+    cudaError_t e = cudaMemsetAsync(p.grid_bar, 0, sizeof(uint32_t), stream);
+    if (e == cudaSuccess && p.tokens_per_rank != nullptr)
+        e = cudaMemsetAsync(p.tokens_per_rank, 0, (size_t)p.R * sizeof(int32_t), stream);
     if (e == cudaSuccess && p.cnt_er != nullptr)
         e = cudaMemsetAsync(p.cnt_er, 0, (size_t)p.E * p.R * sizeof(int32_t), stream);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: the grid barriers end
+    attr[0].val.cooperative = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.stream = stream;
-    // count: after the previous work in full (it rewrites the slot array)
     cfg.gridDim = dim3((unsigned)C, 1, 1);
     cfg.blockDim = dim3(kGridThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
-    cfg.numAttrs = 0;
-    e = cudaLaunchKernelEx(&cfg, layout_count_kernel, p);
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(1, 1, 1);
-    cfg.blockDim = dim3(1024, 1, 1);
-    cfg.dynamicSmemBytes = 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, layout_scan_kernel, p);
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3((unsigned)C, 1, 1);
-    cfg.blockDim = dim3(kGridThreads, 1, 1);
-    return cudaLaunchKernelEx(&cfg, layout_write_kernel, p);
+    e = cudaLaunchKernelEx(&cfg, layout_grid_kernel, p);
+    if (e == cudaErrorCooperativeLaunchTooLarge) return cudaErrorInvalidConfiguration;
+    return e;
 }
 
 cudaError_t launch_layout(const LayoutParams &p, int cluster_size, int threads,

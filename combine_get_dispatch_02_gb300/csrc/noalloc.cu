@@ -151,6 +151,7 @@ extern "C" ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, 
     lp.is_token_in_rank = nullptr;
     lp.status = status;
     lp.cta_hist = nullptr;  // at most 65536 entries here: always the cluster form
+    lp.grid_bar = nullptr;
     const cudaError_t le = ep::launch_layout(lp, s.cluster, s.threads, st);
     if (le != cudaSuccess) {  // the status clear above is already enqueued (harmless)
         cudaGetLastError();

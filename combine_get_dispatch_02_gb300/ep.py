@@ -67,7 +67,8 @@ class ep_config(ctypes.Structure):
 
 class ep_tuning(ctypes.Structure):
     _fields_ = [("dispatch_ctas_per_sm", ctypes.c_int32), ("combine_chunks", ctypes.c_int32),
-                ("round_trip_chunk", ctypes.c_int32), ("dispatch_kernel", ctypes.c_int32)]
+                ("round_trip_chunk", ctypes.c_int32), ("dispatch_kernel", ctypes.c_int32),
+                ("layout_form", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -175,9 +175,10 @@ ep_status ep_handle_get_info(const ep_handle *handle, ep_handle_info *out);
  *   d_is_token_in_rank    device uint8 [R*T, R] or NULL: 1 if token g has an
  *                         entry on rank d, else 0
  *   handle                receives slot / src_info / counts / bases
- * One kernel (a thread-block cluster), or from 512K entries (rank layout:
- * 256K) three kernels over all SMs plus zeroing copies of the counts they
- * accumulate; no host synchronisation.  If a launch fails (EP_ERR_CUDA /
+ * One kernel: a thread-block cluster, or from 128K entries (rank layout:
+ * 48K) a cooperative kernel over all SMs after zeroing copies of its grid
+ * barrier and of the counts it accumulates (ep_tuning.layout_form forces
+ * either); no host synchronisation.  If a launch fails (EP_ERR_CUDA /
  * EP_ERR_UNSUPPORTED) the handle holds no layout afterwards (the calls that
  * need one return EP_ERR_NO_LAYOUT); host-side argument errors leave it as
  * it was. */
@@ -442,12 +443,17 @@ ep_status ep_round_trip_auto_chunk(const ep_ctx *ctx, int32_t use_fp8, int32_t r
  *                         the row kernel where it applies), 1 = the row kernel (bulk copies of whole
  *                         rows; only where H % 512 == 0 and H <= 15872, the
  *                         warp-item kernel elsewhere), 2 = the warp-item kernel
- *                         (16-byte stores by every lane) */
+ *                         (16-byte stores by every lane)
+ *   layout_form           0 = the built-in rule (one thread-block cluster below
+ *                         a size, the grid form over all SMs from it), 1 = the
+ *                         cluster, 2 = the grid form (one cooperative kernel;
+ *                         the cluster where it cannot run) */
 typedef struct ep_tuning {
     int32_t dispatch_ctas_per_sm;
     int32_t combine_chunks;
     int32_t round_trip_chunk;
     int32_t dispatch_kernel;
+    int32_t layout_form;
 } ep_tuning;
 
 /* One candidate ep_autotune timed: knob (EP_TUNE_*), its value, median µs. */

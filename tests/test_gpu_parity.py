@@ -75,10 +75,10 @@ LAYOUT_CASES = {
     "r128_e128": wl.TINY.with_(num_ranks=128, num_experts=128, topk=8, tokens_per_rank=16,
                                max_tokens_per_rank=16),
     "empty": wl.TINY.with_(tokens_per_rank=0),
-    # 1M entries: too many to keep a shared-memory copy per CTA, so the
-    # second pass re-reads topk_idx
+    # 1M entries (the grid form; the cluster form at this size, which keeps
+    # no shared-memory copy of the entries, runs in test_gpu_layout_forms)
     "unstaged_packed": wl.LL.with_(tokens_per_rank=4096, max_tokens_per_rank=4096, layout=wl.PACKED),
-    # 512K+ entries: the grid form (count / scan / write kernels over all SMs)
+    # 128K+ entries: the grid form (one cooperative kernel over all SMs)
     "grid_ll_padded": wl.LL.with_(tokens_per_rank=2048, max_tokens_per_rank=2048),
     "grid_skew_packed": wl.SKEW.with_(tokens_per_rank=6000, max_tokens_per_rank=6000, layout=wl.PACKED),
     "grid_ragged_e1024": wl.TINY.with_(num_ranks=8, num_experts=1024, topk=8, tokens_per_rank=8193,

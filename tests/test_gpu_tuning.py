@@ -79,16 +79,16 @@ def test_every_launch_shape_gives_the_same_bits(name):
 def test_set_tuning_validates():
     buf = make_buffer(wl.TINY)
     assert ep.ep_get_tuning(buf.ctx).as_dict() == {"dispatch_ctas_per_sm": 0, "combine_chunks": 0,
-                                                   "round_trip_chunk": 0, "dispatch_kernel": 0}
+                                                   "round_trip_chunk": 0, "dispatch_kernel": 0, "layout_form": 0}
     for bad in (ep.ep_tuning(17, 0, 0), ep.ep_tuning(-1, 0, 0), ep.ep_tuning(0, 3, 0), ep.ep_tuning(0, 0, -5),
-                ep.ep_tuning(0, 0, 0, 3)):
+                ep.ep_tuning(0, 0, 0, 3), ep.ep_tuning(0, 0, 0, 0, 3), ep.ep_tuning(0, 0, 0, 0, -1)):
         with pytest.raises(ep.EPError) as e:
             ep.ep_set_tuning(buf.ctx, bad)
         assert e.value.status == ep.EP_ERR_INVALID_ARG
     assert ep.ep_get_tuning(buf.ctx).as_dict()["combine_chunks"] == 0
     ep.ep_set_tuning(buf.ctx, ep.ep_tuning(2, 4, 640))
     assert ep.ep_get_tuning(buf.ctx).as_dict() == {"dispatch_ctas_per_sm": 2, "combine_chunks": 4,
-                                                   "round_trip_chunk": 640, "dispatch_kernel": 0}
+                                                   "round_trip_chunk": 640, "dispatch_kernel": 0, "layout_form": 0}
     assert ep.ep_round_trip_auto_chunk(buf.ctx, True) == 640
 
 
