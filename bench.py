@@ -59,6 +59,8 @@ def _args():
     ap.add_argument("--sweep-reps", type=int, default=10)
     ap.add_argument("--dtype", choices=["fp8", "bf16"], default=None,
                     help="override the workload's dispatch payload")
+    ap.add_argument("--hidden", type=int, default=None,
+                    help="override the workload's hidden size (a profiled run of the layout stays small)")
     ap.add_argument("--backward-reps", type=int, default=20,
                     help="reps of the backward pair (BF16 expert-major workloads; 0: skip)")
     ap.add_argument("--autotune", action="store_true",
@@ -349,6 +351,8 @@ def run_ours(args):
         w = w.with_(layout=args.layout)
     if args.dtype is not None:
         w = w.with_(use_fp8=(args.dtype == "fp8"))
+    if args.hidden is not None:
+        w = w.with_(hidden=args.hidden)
     d = wl.generate(w)
     N, K, H = w.num_tokens, w.topk, w.hidden
 

@@ -43,7 +43,7 @@ struct ep_ctx {
     int64_t l2_bytes;
     ep_tuning tune;        // launch shapes set by ep_set_tuning / ep_autotune (0: built-in rules)
     int combine_bps_tuned; // resident combine CTAs per SM for tune.combine_chunks
-    ep_tune_record tune_log[16];  // the candidates the last ep_autotune timed
+    ep_tune_record tune_log[24];  // the candidates the last ep_autotune timed
     int tune_log_n;
     ep_test_hooks hooks;   // test-only switches (ep_set_test_hooks)
     // copy-engine streams of the rank transport, forked from and joined back
@@ -559,7 +559,7 @@ bool pinned_host(const void *p) {
 namespace {
 
 void log_candidate(ep_ctx *ctx, int32_t knob, int32_t value, float us) {
-    if (ctx->tune_log_n < 16) ctx->tune_log[ctx->tune_log_n++] = ep_tune_record{knob, value, us};
+    if (ctx->tune_log_n < 24) ctx->tune_log[ctx->tune_log_n++] = ep_tune_record{knob, value, us};
 }
 
 // Median CUDA-event time (µs) of `reps` runs of enqueue().  Before each,
@@ -1321,6 +1321,32 @@ ep_status ep_autotune(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, i
     // start behind a large write differ by a few per cent from run to run).
     constexpr float kMargin = 0.97f;
 
+    // layout form: the rule's, the cluster and the grid form, each timed as
+    // layout + dispatch (the rule's dispatch shape)
+    if (s == EP_OK) {
+        float best_us = 0.0f;
+        for (int j = 0; s == EP_OK && j < 3; ++j) {
+            ep_tuning t = best;
+            t.layout_form = j;
+            s = ep_set_tuning(ctx, &t);
+            float us = 0.0f;
+            if (s == EP_OK)
+                s = median_us(
+                    [&] {
+                        ep_status e = enqueue_layout(ctx, d_topk_idx, tokens_per_rank, nullptr, nullptr, nullptr,
+                                                     false, h, st);
+                        return e != EP_OK ? e
+                                          : enqueue_dispatch(ctx, h, d_x, 0, N, fp8, d_recv_x, d_recv_scales,
+                                                             nullptr, true, st);
+                    },
+                    reps, flush, flush_bytes, sms, st, &us);
+            if (s == EP_OK) log_candidate(ctx, EP_TUNE_LAYOUT_FORM, j, us);
+            if (s == EP_OK && (j == 0 || us < kMargin * best_us)) {
+                best_us = us;
+                best.layout_form = j;
+            }
+        }
+    }
     // dispatch: (kernel, row-kernel CTAs per SM), timed as the common call
     // runs it (layout kernel, then the dispatch behind it); the rule first
     if (s == EP_OK) {

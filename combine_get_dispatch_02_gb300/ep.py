@@ -47,7 +47,8 @@ ENTRY_POINTS = (
     "ep_rank_combine_recv", "ep_rank_runs",
 )
 
-TUNE_KNOBS = {0: "dispatch", 1: "combine_chunks", 2: "round_trip_chunk"}  # dispatch: 100 * kernel + CTAs/SM
+TUNE_KNOBS = {0: "dispatch", 1: "combine_chunks", 2: "round_trip_chunk",
+              3: "layout_form"}  # dispatch: 100 * kernel + CTAs/SM
 
 EP_CHUNK_AUTO = -1
 
@@ -371,10 +372,10 @@ def ep_autotune(ctx, x: torch.Tensor, topk_idx: torch.Tensor, tokens_per_rank: i
 
 def ep_get_autotune_log(ctx) -> list[tuple[str, int, float]]:
     """(knob, value, median µs) of each candidate the last ep_autotune timed."""
-    recs = (ep_tune_record * 16)()
+    recs = (ep_tune_record * 24)()
     n = ctypes.c_int32(0)
-    _check(lib().ep_get_autotune_log(ctx, recs, 16, ctypes.byref(n)), "ep_get_autotune_log")
-    return [(TUNE_KNOBS.get(r.knob, str(r.knob)), r.value, r.median_us) for r in recs[:min(n.value, 16)]]
+    _check(lib().ep_get_autotune_log(ctx, recs, 24, ctypes.byref(n)), "ep_get_autotune_log")
+    return [(TUNE_KNOBS.get(r.knob, str(r.knob)), r.value, r.median_us) for r in recs[:min(n.value, 24)]]
 
 
 def ep_get_device_status(ctx, stream=None) -> int:

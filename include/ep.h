@@ -461,7 +461,8 @@ typedef enum ep_tune_knob {
     EP_TUNE_DISPATCH = 0,              /* value 100 * dispatch_kernel + dispatch_ctas_per_sm;
                                           timed as layout + dispatch */
     EP_TUNE_COMBINE_CHUNKS = 1,
-    EP_TUNE_ROUND_TRIP_CHUNK = 2       /* INT32_MAX: one chunk */
+    EP_TUNE_ROUND_TRIP_CHUNK = 2,      /* INT32_MAX: one chunk */
+    EP_TUNE_LAYOUT_FORM = 3            /* timed as layout + dispatch */
 } ep_tune_knob;
 typedef struct ep_tune_record {
     int32_t knob;
@@ -476,8 +477,9 @@ ep_status ep_set_tuning(ep_ctx *ctx, const ep_tuning *tuning);
 /* Time each launch shape above on the caller's own inputs and keep the
  * fastest in the context (also written to *out; the built-in rule's choice is
  * timed first and kept unless another candidate is at least 3% faster):
- * layout + dispatch with the rule's kernel, the row kernel at 1..4 CTAs per
- * SM (H % 512 == 0, H <= 16384) and the warp-item kernel, the combine with
+ * layout + dispatch with the rule's layout form, the cluster and the grid
+ * form, then with the rule's kernel, the row kernel at 1..4 CTAs per
+ * SM (H % 512 == 0, H <= 15872) and the warp-item kernel, the combine with
  * 1, 2 and 4 chunks per item,
  * then the round trip in one chunk and in chunks of half, one and two times
  * the L2 rule.  Each candidate: the median of `reps` (1..1000) runs, before
@@ -494,7 +496,7 @@ ep_status ep_autotune(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx,
                       ep_tuning *out, void *stream);
 
 /* The candidates the last ep_autotune on this context timed, in order (at
- * most 16): *count gets their number, records[0 .. min(count, capacity))
+ * most 24): *count gets their number, records[0 .. min(count, capacity))
  * their values.  Host only. */
 ep_status ep_get_autotune_log(const ep_ctx *ctx, ep_tune_record *records, int32_t capacity,
                               int32_t *count);

@@ -113,7 +113,8 @@ def test_autotune_then_round_trip_matches_the_oracle():
     log = ep.ep_get_autotune_log(buf.ctx)
     assert t.dispatch_kernel in (0, 1, 2)
     chosen_value = dict(t.as_dict(), dispatch=100 * t.dispatch_kernel + t.dispatch_ctas_per_sm)
-    for knob in ("dispatch", "combine_chunks", "round_trip_chunk"):
+    assert t.layout_form in (0, 1, 2)
+    for knob in ("layout_form", "dispatch", "combine_chunks", "round_trip_chunk"):
         cands = [(v, us) for k, v, us in log if k == knob]
         assert cands and all(us > 0 for _, us in cands)
         # the first candidate is the built-in rule's; another is kept only when 3% faster than it
