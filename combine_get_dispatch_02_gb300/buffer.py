@@ -261,6 +261,96 @@ class Buffer:
         ep.ep_combine(self._ctx, hidden_states, topk_weights, handle.raw, out)
         return out
 
+    def _rank_buffers(self, key: str, use_fp8: bool, wire: int):
+        """Send buffer of the rank transport ([ep_rank_send_rows, H] + scales,
+        or bf16 for the combine) and, for the host wire, its pinned staging
+        buffer; kept for reuse."""
+        k = ("rank", key, use_fp8)
+        if k not in self._send:
+            dev = torch.device("cuda", torch.cuda.current_device())
+            n = ep.ep_rank_send_rows(self.cfg)
+            fp8 = use_fp8 and key == "dispatch"
+            x = torch.empty(n, self.hidden, dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16, device=dev)
+            sc = torch.empty(n, self.hidden // 128, dtype=torch.float32, device=dev) if fp8 else None
+            self._send[k] = (x, sc)
+        x, sc = self._send[k]
+        stage = None
+        if wire == ep.EP_WIRE_HOST:
+            ks = ("rank_stage",)
+            if ks not in self._send:
+                n = ep.ep_rank_send_rows(self.cfg)
+                self._send[ks] = torch.empty(n * (2 * self.hidden + self.hidden // 32), dtype=torch.uint8).pin_memory()
+            stage = self._send[ks]
+        return x, sc, stage
+
+    def rank_dispatch(self, hidden_states: torch.Tensor, topk_idx: torch.Tensor | None,
+                      topk_weights: torch.Tensor | None = None, use_fp8: bool = False,
+                      handle: Handle | None = None, wire: int = ep.EP_WIRE_DEVICE,
+                      return_recv_hook: bool = False):
+        """Rank-deduplicated dispatch whose receive runs no kernel: the send
+        half (layout, send rows, one cast per token) now, the receive as one
+        copy per (source rank, destination rank) run over ``wire``
+        (EP_WIRE_DEVICE: device copies at HBM speed; EP_WIRE_HOST: through
+        pinned host memory on the copy engines, no SM).  Returns
+        ((recv_x, recv_scales) if use_fp8 else recv_x, recv_count [R],
+        recv_topk_idx [rows, K], recv_topk_weights [rows, K] (None when the
+        layout is reused), handle), plus
+        ``hook`` when return_recv_hook is True (the receive is enqueued when
+        it is called; otherwise it is enqueued before returning).
+        topk_idx=None reuses the layout in ``handle``."""
+        T = hidden_states.numel() // (self.num_ranks * self.hidden)
+        if hidden_states.numel() != self.num_ranks * T * self.hidden:
+            raise ValueError("hidden_states must be [R, T, H]")
+        if topk_idx is not None and self._tokens_per_rank(topk_idx) != T:
+            raise ValueError("topk_idx and hidden_states disagree on T")
+        if topk_idx is None and handle is None:
+            raise ValueError("reusing a layout needs a handle")
+        handle = handle or Handle(self)
+        dev = hidden_states.device
+        rows = self.rank_rows
+        ridx = torch.empty(rows, self.topk, dtype=torch.int32, device=dev)
+        rw = torch.empty(rows, self.topk, dtype=torch.float32, device=dev)
+        send_x, send_sc, stage = self._rank_buffers("dispatch", use_fp8, wire)
+        w = None if topk_weights is None else topk_weights.reshape(-1, self.topk)
+        ep.ep_rank_dispatch_send(self._ctx, hidden_states, topk_idx, w, T, use_fp8,
+                                 ridx if topk_idx is not None else None,
+                                 rw if topk_idx is not None else None, handle.raw, send_x, send_sc)
+        recv_x, recv_scales = self.alloc_rank_recv(use_fp8)
+        recv_count = torch.empty(self.num_ranks, dtype=torch.int32, device=dev)
+
+        def hook(stream=None):
+            ep.ep_rank_dispatch_recv(self._ctx, handle.raw, use_fp8, send_x, send_sc, recv_x,
+                                     recv_scales if use_fp8 else None, recv_count, wire, stage, stream)
+        if topk_idx is None:  # a reused layout: the rows' local top-k came with the first call
+            ridx = rw = None
+        res = (((recv_x, recv_scales) if use_fp8 else recv_x), recv_count, ridx, rw, handle)
+        if return_recv_hook:
+            return res + (hook,)
+        hook()
+        return res
+
+    def rank_combine(self, hidden_states: torch.Tensor, handle: Handle, wire: int = ep.EP_WIRE_DEVICE,
+                     out: torch.Tensor | None = None, return_recv_hook: bool = False):
+        """The rank transport's combine: the expert outputs ``hidden_states``
+        (rank receive layout, bf16, local weights already applied) travel back
+        over ``wire`` now, and the per-token sum over its rank rows follows
+        (in ``hook`` when return_recv_hook is True).  Returns out [R*T, H]
+        (and hook)."""
+        info = handle.info()
+        if info.tokens_per_rank < 0:
+            raise ep.EPError(ep.EP_ERR_NO_LAYOUT, "rank_combine")
+        if out is None:
+            out = torch.empty(info.num_tokens, self.hidden, dtype=torch.bfloat16, device=hidden_states.device)
+        send_y, _, stage = self._rank_buffers("combine", False, wire)
+        ep.ep_rank_combine_send(self._ctx, handle.raw, hidden_states, send_y, wire, stage)
+
+        def hook(stream=None):
+            ep.ep_rank_combine_recv(self._ctx, handle.raw, send_y, out, stream)
+        if return_recv_hook:
+            return out, hook
+        hook()
+        return out
+
     def round_trip(self, hidden_states: torch.Tensor, topk_idx: torch.Tensor | None,
                    topk_weights: torch.Tensor | None, use_fp8: bool = True, chunk_tokens: int = 0,
                    handle: Handle | None = None, recv=None, y: torch.Tensor | None = None,

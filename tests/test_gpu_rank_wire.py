@@ -200,3 +200,38 @@ def test_rank_wire_rejects_pageable_stage_and_other_layouts():
         ep.ep_rank_dispatch_recv(buf.ctx, h.raw, False, send_x, None, recv, None, None)
     assert e.value.status == ep.EP_ERR_NO_LAYOUT
     assert buf.device_status() == ep.EP_OK
+
+
+@pytest.mark.parametrize("wire", [ep.EP_WIRE_DEVICE, ep.EP_WIRE_HOST])
+def test_buffer_rank_dispatch_and_combine_hooks(wire):
+    """Buffer.rank_dispatch / rank_combine with return_recv_hook=True equal the
+    oracle's rank dispatch and rank combine."""
+    w = wl.SKEW.with_(tokens_per_rank=96, max_tokens_per_rank=96, use_fp8=True, layout=wl.PACKED)
+    d = wl.generate(w)
+    N, K, H = w.num_tokens, w.topk, w.hidden
+    wts = d["topk_weights"].reshape(N, K)
+    buf = make_buffer(w)
+    x = bits_to_bf16(d["x_bits"])
+    (recv, sc), cnt, ridx, rw, h, hook = buf.rank_dispatch(
+        x, torch.from_numpy(d["topk_idx"]).cuda(), torch.from_numpy(wts).cuda(), use_fp8=True, wire=wire,
+        return_recv_hook=True)
+    hook()
+    assert buf.device_status() == ep.EP_OK
+    o = oracle.rank_layout(d["topk_idx"], wts, w.num_experts, w.max_tokens_per_rank, ORACLE_LAYOUT[w.layout])
+    rows = o["rank_slot"][o["rank_slot"] >= 0]
+    q, s = oracle.dispatch(d["x_bits"].reshape(N, H), o["rank_slot"], o["rows"], True)
+    rd = torch.from_numpy(rows.astype(np.int64)).cuda()
+    assert np.array_equal(e4m3_to_bits(recv.view(torch.uint8)[rd]), q[rows])
+    assert np.array_equal(sc[rd].cpu().numpy().view(np.uint32), s[rows].view(np.uint32))
+    assert np.array_equal(cnt.cpu().numpy(), o["tokens_per_rank"])
+    assert np.array_equal(rw.cpu().numpy()[rows].view(np.uint32), o["recv_topk_weights"][rows].view(np.uint32))
+    tokens = np.arange(N)
+    ye = wl.expert_outputs(w, tokens)
+    y = place_rows(buf.rank_rows, H, o["rank_slot"], ye, tokens)
+    out, chook = buf.rank_combine(y, h, wire=wire, return_recv_hook=True)
+    chook()
+    assert buf.device_status() == ep.EP_OK
+    m = o["rank_slot"] >= 0
+    ref = oracle.combine(ye.reshape(N * K, H), np.where(m, np.arange(N * K).reshape(N, K), -1).astype(np.int32),
+                         None)
+    assert np.array_equal(bf16_to_bits(out), ref)
