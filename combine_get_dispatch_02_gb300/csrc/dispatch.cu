@@ -136,9 +136,12 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const DispatchParams
 //             buffer (one arrival per warp, after a proxy fence that makes
 //             the writes visible to the copy engine);
 //   empty[b]  completes when the copies of the buffer's row have read it
-//             (the issuer's cp.async.bulk.wait_group.read, kLag tokens
+//             (the issuer's cp.async.bulk.wait_group.read, LAG tokens
 //             later), so the producers may refill it.
-// No CTA-wide barrier per token: the producer warps run up to NB - kLag
+// LAG < NB: the producers of token t wait for the release of token t - NB,
+// which the issuer gives after token t - NB + LAG; with LAG >= NB that would
+// be token t itself, which they have not written yet.
+// No CTA-wide barrier per token: the producer warps run up to NB - LAG
 // tokens ahead of the issuer and independently of one another.  Only the
 // issuer waits for the layout kernel before it (programmatic dependent
 // launch: it reads the slots); behind the library's own layout kernel the
@@ -147,13 +150,20 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const DispatchParams
 // mbarrier wait is bounded (about one second); if one gives up the kernel
 // sets kStatusTimeout, stops issuing, lets its copies finish and returns.
 // Needs H % 512 == 0 and H/16 + 32 <= 1024 threads.
-// CTAs per SM: about 1024 threads, at least 2 (measured best at H = 7168)
-int row_blocks_per_sm(int H) {
-    const int b = 16384 / H;
+// CTAs per SM: about 1024 threads, at least 2 (measured best at H = 7168);
+// FP8 rows at most 4 (H = 2048, top-6 / top-8: 0.90 of peak on 4 CTAs per SM
+// against 0.77-0.85 on 8)
+int row_blocks_per_sm(int H, bool fp8) {
+    int b = 16384 / H;
+    if (fp8 && b > 4) b = 4;
     return b < 2 ? 2 : (b > 16 ? 16 : b);
 }
 
-constexpr int kLag = 2;                            // tokens the issuer lets its copies run before a release
+// tokens the issuer lets its copies run before it releases their buffer (< NB)
+template <int NB>
+struct Lag {
+    static constexpr int value = NB > 2 ? 2 : 1;
+};
 constexpr uint64_t kRowWaitNs = 1000000000ull;     // bound of one mbarrier wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -288,10 +298,10 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
                         bulk_store(p.recv_scales + (int64_t)my_slot * (H / 128), smem_addr(row + H), H / 32);
                 }
                 bulk_commit();
-                bulk_wait_read<kLag>();  // the copies of token it - kLag have read their buffer
+                bulk_wait_read<Lag<NB>::value>();  // the copies of token it - LAG have read their buffer
             }
             __syncwarp();
-            if (lane == 0 && it >= kLag) mbar_arrive(smem_addr(&empty[(it - kLag) % NB]));
+            if (lane == 0 && it >= Lag<NB>::value) mbar_arrive(smem_addr(&empty[(it - Lag<NB>::value) % NB]));
         }
         if (!ok && lane == 0 && p.status != nullptr) atomicOr(p.status, kStatusTimeout);
         // every copy of this CTA is issued: the kernel queued behind (e.g. the
@@ -355,7 +365,7 @@ int blocks_per_sm() {
 
 }  // namespace
 
-int dispatch_row_ctas_rule(int H) { return row_blocks_per_sm(H); }
+int dispatch_row_ctas_rule(int H, bool fp8) { return row_blocks_per_sm(H, fp8); }
 
 int dispatch_blocks_per_sm(bool fp8) { return fp8 ? blocks_per_sm<true>() : blocks_per_sm<false>(); }
 
@@ -400,25 +410,38 @@ void dispatch_init() {
     // the row kernel asks for more than the 48 KB default (see above)
     allow_smem(dispatch_row_kernel<false, 2>);
     allow_smem(dispatch_row_kernel<false, 4>);
+    allow_smem(dispatch_row_kernel<false, 6>);
     allow_smem(dispatch_row_kernel<false, 8>);
     allow_smem(dispatch_row_kernel<true, 2>);
     allow_smem(dispatch_row_kernel<true, 4>);
+    allow_smem(dispatch_row_kernel<true, 6>);
     allow_smem(dispatch_row_kernel<true, 8>);
     cudaGetLastError();
 }
 
 namespace {
-// Row buffers in the ring: as many of 8, 4, 2 as the shared memory the
-// occupancy cap grants anyway holds.
-int ring_buffers(bool fp8, int H, size_t smem) {
+// Row buffers in the ring and the dynamic shared memory of one CTA: as many
+// buffers (8, 6, 4 or 2) as fit in one CTA's share of the SM when `blocks`
+// CTAs share it, and at least the size that keeps a further CTA off the SM
+// (row_smem_for_occupancy).  Deeper rings let the producers run further
+// ahead of the copies (BF16 rows of 14 KB: 8 buffers instead of 4).
+void row_ring(bool fp8, int H, int blocks, int *nb, size_t *smem) {
     const size_t rowb = fp8 ? (size_t)H + H / 32 : 2 * (size_t)H;
-    return smem >= 8 * rowb ? 8 : (smem >= 4 * rowb ? 4 : 2);
+    const size_t cap = row_smem_for_occupancy(fp8, H, blocks);
+    int64_t share = g_smem_per_sm > 0 ? (int64_t)g_smem_per_sm / blocks - g_smem_reserved - 256 : 0;
+    if (share > (int64_t)g_smem_per_block - 256) share = (int64_t)g_smem_per_block - 256;
+    const int64_t fit = share > 0 ? share / (int64_t)rowb : 0;
+    const int n = fit >= 8 ? 8 : (fit >= 6 ? 6 : (fit >= 4 ? 4 : 2));
+    const size_t want = (size_t)n * rowb;
+    *nb = n;
+    *smem = ((want > cap ? want : cap) + 15) / 16 * 16;
 }
 
 template <bool FP8>
 cudaError_t launch_row(const cudaLaunchConfig_t &cfg, int nb, const DispatchParams &p) {
     switch (nb) {
         case 8: return cudaLaunchKernelEx(&cfg, dispatch_row_kernel<FP8, 8>, p);
+        case 6: return cudaLaunchKernelEx(&cfg, dispatch_row_kernel<FP8, 6>, p);
         case 4: return cudaLaunchKernelEx(&cfg, dispatch_row_kernel<FP8, 4>, p);
         default: return cudaLaunchKernelEx(&cfg, dispatch_row_kernel<FP8, 2>, p);
     }
@@ -431,15 +454,16 @@ cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks, b
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     if (row_kernel_fits(p.H) && p.row_sms > 0) {
-        const int bps = p.row_bps > 0 ? p.row_bps : row_blocks_per_sm(p.H);
+        const int bps = p.row_bps > 0 ? p.row_bps : row_blocks_per_sm(p.H, fp8);
         int64_t blocks = (int64_t)p.row_sms * bps;
         if (blocks > p.N) blocks = p.N;
         if (blocks < 1) blocks = 1;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)blocks, 1, 1);
         cfg.blockDim = dim3(p.H / 16 + 32, 1, 1);
-        const size_t smem = row_smem_for_occupancy(fp8, p.H, bps);
-        const int nb = ring_buffers(fp8, p.H, smem);
+        int nb = 2;
+        size_t smem = 0;
+        row_ring(fp8, p.H, bps, &nb, &smem);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cfg.attrs = attr;

@@ -81,13 +81,11 @@ namespace {
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 // A new layout in the handle: the rank transport's send rows and runs no
-// longer belong to it.
+// longer belong to it.  A copy of old run sizes into h_runs may still be
+// queued; the host reads h_runs only after the event of a later send, whose
+// copy is queued behind it, and ep_handle_destroy waits for it.
 void forget_send(ep_handle *h) {
     h->has_send = 0;
-    if (h->runs_state == 1) {  // a copy into h_runs may still be queued: let it land first
-        cudaEventSynchronize(h->runs_ev);
-        cudaGetLastError();
-    }
     h->runs_state = 0;
 }
 
@@ -761,7 +759,7 @@ ep_status ep_handle_destroy(ep_handle *h) {
     cudaFree(h->base);
     cudaFree(h->tokens_per_expert);
     cudaFree(h->cta_hist);
-    if (h->runs_state == 1 && h->runs_ev) cudaEventSynchronize(h->runs_ev);  // the copy into h_runs lands first
+    if (h->runs_ev) cudaEventSynchronize(h->runs_ev);  // a queued copy into h_runs lands first
     cudaFree(h->send_slot);
     if (h->h_runs) cudaFreeHost(h->h_runs);
     if (h->runs_ev) cudaEventDestroy(h->runs_ev);

@@ -94,8 +94,8 @@ struct DispatchParams {
 
 cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks,
                             bool pdl, cudaStream_t stream);
-// The row dispatch kernel's CTAs per SM by the built-in rule (from H).
-int dispatch_row_ctas_rule(int H);
+// The row dispatch kernel's CTAs per SM by the built-in rule (from H and the payload).
+int dispatch_row_ctas_rule(int H, bool fp8);
 // Resident blocks per SM of the warp-item dispatch kernel (for grid sizing).
 int dispatch_blocks_per_sm(bool fp8);
 // One-time kernel attribute set-up (call with the device current).

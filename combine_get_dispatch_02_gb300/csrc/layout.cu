@@ -475,6 +475,7 @@ __device__ bool grid_barrier(uint32_t *bar, uint32_t target, int *flag) {
                 ok = false;
                 break;
             }
+            __nanosleep(32);  // fewer polls of the counter's line while the arrivals land
         }
         __threadfence();
         *flag = ok ? 1 : 0;

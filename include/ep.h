@@ -432,7 +432,7 @@ ep_status ep_round_trip_auto_chunk(const ep_ctx *ctx, int32_t use_fp8, int32_t r
  * "如何突破MoE通信瓶颈：DeepEP跨节点优化技术终极指南", section 功能4).  None of
  * them changes a result bit: they only decide how the work is spread.
  *   dispatch_ctas_per_sm  CTAs per SM of the row dispatch kernel (1..16),
- *                         0 = the built-in rule (from H)
+ *                         0 = the built-in rule (from H; at most 4 for FP8)
  *   combine_chunks        256-channel chunks per combine work item (1, 2 or 4),
  *                         0 = the built-in rule (from the entries per token)
  *   round_trip_chunk      tokens per chunk that EP_CHUNK_AUTO stands for in

@@ -161,7 +161,11 @@ DISPATCH_CASES = {
     "h384_fp8": wl.TINY.with_(hidden=384, use_fp8=True, x_scale="loguniform"),  # chunk tail
     "h200_bf16": wl.TINY.with_(hidden=200),                                     # half-segment tail
     "k32_fp8": wl.TINY.with_(num_experts=64, topk=32, use_fp8=True),
-    "h16384_bf16": wl.TINY.with_(hidden=16384),                                 # row kernel, 64 KB smem
+    "h16384_bf16": wl.TINY.with_(hidden=16384),                                 # warp-item kernel (above 15872)
+    # the largest rows of the row kernel: a ring of 2 buffers (BF16, 31 KB rows) and of 6 (FP8)
+    "h15872_bf16": wl.TINY.with_(hidden=15872, tokens_per_rank=24, max_tokens_per_rank=24),
+    "h15872_fp8": wl.TINY.with_(hidden=15872, tokens_per_rank=24, max_tokens_per_rank=24, use_fp8=True),
+    "h12288_bf16": wl.TINY.with_(hidden=12288, tokens_per_rank=24, max_tokens_per_rank=24),
     "h32768_fp8": wl.TINY.with_(hidden=32768, use_fp8=True, tokens_per_rank=8,
                                 max_tokens_per_rank=8),                          # warp-item kernel
     "packed_fp8": wl.SKEW.with_(layout=wl.PACKED),

@@ -41,10 +41,13 @@ def _run(buf, w, x, idx_d, wts_d, y, rank=False):
     return (recv.view(torch.uint8)[rows].clone(), None if scales is None else scales[rows].clone(), out.clone())
 
 
-@pytest.mark.parametrize("name", ["ll", "skew_masked", "normal_rank", "tiny_bf16"])
+@pytest.mark.parametrize("name", ["ll", "skew_masked", "normal_rank", "tiny_bf16", "bf16_h7168"])
 def test_every_launch_shape_gives_the_same_bits(name):
+    # bf16_h7168: 14 KB rows, so 1 / 2 / 3 / 4 row-kernel CTAs per SM give rings of 8 / 8 / 4 / 2
+    # row buffers (the 2-buffer ring releases each buffer one token later instead of two)
     w = {"ll": wl.LL, "skew_masked": wl.SKEW.with_(tokens_per_rank=300), "tiny_bf16": wl.TINY,
-         "normal_rank": wl.NORMAL.with_(tokens_per_rank=256, max_tokens_per_rank=256, use_fp8=True)}[name]
+         "normal_rank": wl.NORMAL.with_(tokens_per_rank=256, max_tokens_per_rank=256, use_fp8=True),
+         "bf16_h7168": wl.NORMAL.with_(tokens_per_rank=300, max_tokens_per_rank=300)}[name]
     rank = name == "normal_rank"
     d = wl.generate(w)
     idx = d["topk_idx"] if name != "skew_masked" else wl.inject_masks(d["topk_idx"], 0.1, 3)
