@@ -291,14 +291,15 @@ ep_status ep_expert_identity(ep_ctx *ctx, const ep_handle *handle, int32_t use_f
 /* Split dispatch and combine: the send half returns and a later "hook" call
  * finishes the receive (the hook-based communication-computation overlap of
  * "如何突破MoE通信瓶颈：DeepEP跨节点优化技术终极指南", section 技术解析,
- * 通信-计算重叠技术: the receive occupies no SM; the DeepTech announcement of
- * DeepEP, 010bt.com, says the same).  On one GPU the wire is HBM and the
- * engine that moves rows without SM work is the bulk-copy (TMA) unit: the
- * receive hooks and the combine send are copy kernels whose threads only
- * issue cp.async.bulk copies, so they can run on num_sms SMs (<= 0: the
- * context's limit) while other work uses the rest.  The results are
- * identical, bit for bit, to ep_dispatch / ep_combine; the price is that
- * every row crosses HBM once more (through a send buffer).
+ * 通信-计算重叠技术; the DeepTech announcement of DeepEP, 010bt.com, says the
+ * same).  Here the receive hooks and the combine send are copy kernels whose
+ * threads only issue cp.async.bulk copies (the bulk-copy unit moves the
+ * rows), so they can run on num_sms SMs (<= 0: the context's limit) while
+ * other work uses the rest; they still occupy those SMs.  For a receive that
+ * occupies no SM at all see the rank transport (ep_rank_dispatch_recv,
+ * EP_WIRE_HOST) below.  The results are identical, bit for bit, to
+ * ep_dispatch / ep_combine; the price is that every row crosses HBM once more
+ * (through a send buffer).
  *
  * ep_dispatch_send: the layout (when d_topk_idx is given, as in ep_dispatch),
  *   then each token cast once (FP8) into its row of the send buffer:
