@@ -235,3 +235,56 @@ def test_buffer_rank_dispatch_and_combine_hooks(wire):
     ref = oracle.combine(ye.reshape(N * K, H), np.where(m, np.arange(N * K).reshape(N, K), -1).astype(np.int32),
                          None)
     assert np.array_equal(bf16_to_bits(out), ref)
+
+
+@pytest.mark.parametrize("wire", [ep.EP_WIRE_DEVICE, ep.EP_WIRE_HOST])
+def test_rank_wire_calls_replay_from_a_cuda_graph(wire):
+    """Once the run sizes are on the host (after the first wire call on a
+    layout), the send on the cached layout, the receive and the combine's
+    wire + reduce only enqueue: captured into a CUDA graph and replayed with
+    new token values, they give the oracle's bits."""
+    w = wl.SKEW.with_(tokens_per_rank=64, max_tokens_per_rank=64, use_fp8=True, layout=wl.PACKED)
+    d = wl.generate(w)
+    N, K, H = w.num_tokens, w.topk, w.hidden
+    buf = make_buffer(w)
+    h = buf.new_handle()
+    x = bits_to_bf16(d["x_bits"])
+    send_x, send_sc = _send_buffers(buf, w)
+    stage = _stage(buf, w) if wire == ep.EP_WIRE_HOST else None
+    recv, sc = buf.alloc_rank_recv(True)
+    send_y = torch.empty(ep.ep_rank_send_rows(buf.cfg), H, dtype=torch.bfloat16, device="cuda")
+    o = oracle.rank_layout(d["topk_idx"], None, w.num_experts, w.max_tokens_per_rank, ORACLE_LAYOUT[w.layout])
+    tokens = np.arange(N)
+    ye = wl.expert_outputs(w, tokens)
+    y = place_rows(buf.rank_rows, H, o["rank_slot"], ye, tokens)
+    out = torch.empty(N, H, dtype=torch.bfloat16, device="cuda")
+    ep.ep_rank_dispatch_send(buf.ctx, x, torch.from_numpy(d["topk_idx"]).cuda(), None, w.tokens_per_rank, True,
+                             None, None, h.raw, send_x, send_sc)
+    ep.ep_rank_dispatch_recv(buf.ctx, h.raw, True, send_x, send_sc, recv, sc, None, wire, stage)  # runs -> host
+    assert buf.device_status() == ep.EP_OK
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ep.ep_rank_dispatch_send(buf.ctx, x, None, None, w.tokens_per_rank, True, None, None, h.raw, send_x,
+                                 send_sc, s)
+        ep.ep_rank_dispatch_recv(buf.ctx, h.raw, True, send_x, send_sc, recv, sc, None, wire, stage, s)
+        ep.ep_rank_combine_send(buf.ctx, h.raw, y, send_y, wire, stage, s)
+        ep.ep_rank_combine_recv(buf.ctx, h.raw, send_y, out, s)
+    x2_bits = wl.generate(w.with_(seed=w.seed + 7))["x_bits"]
+    x.copy_(bits_to_bf16(x2_bits))
+    recv.view(torch.uint8).zero_()
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert buf.device_status() == ep.EP_OK
+    rows = o["rank_slot"][o["rank_slot"] >= 0]
+    q, s_ = oracle.dispatch(x2_bits.reshape(N, H), o["rank_slot"], o["rows"], True)
+    rd = torch.from_numpy(rows.astype(np.int64)).cuda()
+    assert np.array_equal(e4m3_to_bits(recv.view(torch.uint8)[rd]), q[rows])
+    assert np.array_equal(sc[rd].cpu().numpy().view(np.uint32), s_[rows].view(np.uint32))
+    m = o["rank_slot"] >= 0
+    ref = oracle.combine(ye.reshape(N * K, H), np.where(m, np.arange(N * K).reshape(N, K), -1).astype(np.int32),
+                         None)
+    assert np.array_equal(bf16_to_bits(out), ref)
