@@ -446,7 +446,10 @@ bool fits(int E, int R, int cl) {
 // bounded (about one second): on expiry the kernel sets kStatusTimeout and
 // returns.  The dispatch queued behind (programmatic dependent launch) may
 // start casting rows at once.
-constexpr int kGridThreads = 512;
+// threads per CTA of the grid form: 1024 from kGridBigEntries entries on (more
+// warps per CTA shorten the count and write phases), 512 below (cheaper
+// block scans and barriers when each CTA holds few entries)
+constexpr int kGridBigEntries = 262144;
 constexpr uint64_t kGridWaitNs = 1000000000ull;
 
 __device__ __forceinline__ uint64_t grid_now_ns() {
@@ -484,11 +487,12 @@ __device__ bool grid_barrier(uint32_t *bar, uint32_t target, int *flag) {
     return *flag != 0;
 }
 
-__global__ void __launch_bounds__(kGridThreads, 1) layout_grid_kernel(const LayoutParams p) {
+template <int NT>
+__global__ void __launch_bounds__(NT, 1) layout_grid_kernel(const LayoutParams p) {
     // the dispatch kernel queued behind this one may start loading and
     // casting token rows now; it waits for these results before it reads a slot
     pdl_launch_dependents();
-    constexpr int NT = kGridThreads, NW = NT / 32;
+    constexpr int NW = NT / 32;
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int E = p.E, R = p.R, K = p.K, T = p.T;
     const int N = (int)p.N;
@@ -669,16 +673,17 @@ __global__ void __launch_bounds__(kGridThreads, 1) layout_grid_kernel(const Layo
     }
 }
 
-size_t grid_smem(int E, int R, int span) {
+size_t grid_smem(int E, int R, int span, int NT) {
     const int hist_er = E * span > E ? E * span : E;  // reused for the bases in the write phase
-    return ((size_t)(kGridThreads / 32) * E + R + (size_t)hist_er + E + kGridThreads / 32 + 1) * sizeof(int32_t);
+    return ((size_t)(NT / 32) * E + R + (size_t)hist_er + E + NT / 32 + 1) * sizeof(int32_t);
 }
 
 void grid_init() {
     int dev = 0, optin = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    cudaFuncSetAttribute(layout_grid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 64);
+    cudaFuncSetAttribute(layout_grid_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 64);
+    cudaFuncSetAttribute(layout_grid_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 64);
     cudaGetLastError();
 }
 
@@ -705,7 +710,8 @@ bool layout_pick_shape(int E, int R, int *cluster_size, int *threads, bool many_
 
 cudaError_t launch_layout_grid(LayoutParams p, int ctas, cudaStream_t stream) {
     const int64_t N = p.N;
-    if (N <= 0 || ctas < 1 || ctas > kGridThreads || p.grid_bar == nullptr) return cudaErrorInvalidValue;
+    if (N <= 0 || ctas < 1 || ctas > 512 || p.grid_bar == nullptr) return cudaErrorInvalidValue;
+    const int NT = N * p.K >= kGridBigEntries ? 1024 : 512;
     // tokens per CTA; a warp's entries are packed into 20 bits until the write phase
     int64_t tpc = (N + ctas - 1) / ctas;
     if (tpc * p.K >= (int64_t(1) << 20)) return cudaErrorInvalidConfiguration;
@@ -718,7 +724,7 @@ cudaError_t launch_layout_grid(LayoutParams p, int ctas, cudaStream_t stream) {
         const int64_t span = p.T > 0 ? (tpc + p.T - 1) / p.T + 1 : 1;
         p.er_span = (int)(span < p.R ? span : p.R);
     }
-    const size_t smem = grid_smem(p.E, p.R, p.er_span);
+    const size_t smem = grid_smem(p.E, p.R, p.er_span, NT);
     if (smem > kMaxSmem) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaMemsetAsync(p.grid_bar, 0, sizeof(uint32_t), stream);
     if (e == cudaSuccess && p.tokens_per_rank != nullptr)
@@ -732,11 +738,12 @@ cudaError_t launch_layout_grid(LayoutParams p, int ctas, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.stream = stream;
     cfg.gridDim = dim3((unsigned)C, 1, 1);
-    cfg.blockDim = dim3(kGridThreads, 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, layout_grid_kernel, p);
+    e = NT == 1024 ? cudaLaunchKernelEx(&cfg, layout_grid_kernel<1024>, p)
+                   : cudaLaunchKernelEx(&cfg, layout_grid_kernel<512>, p);
     if (e == cudaErrorCooperativeLaunchTooLarge) return cudaErrorInvalidConfiguration;
     return e;
 }

@@ -129,3 +129,34 @@ def test_fused_dispatch_on_the_grid_form():
     rd = torch.from_numpy(rows[pick].astype(np.int64)).cuda()
     assert np.array_equal(e4m3_to_bits(q.view(torch.uint8)[rd]), qo)
     assert np.array_equal(sc[rd].cpu().numpy().view(np.uint32), so.view(np.uint32))
+
+
+@pytest.mark.parametrize("max_sms", [7, 40])
+def test_grid_form_under_an_sm_cap(max_sms):
+    """The grid form on a few CTAs (ep_config.max_sms), each CTA taking
+    thousands of tokens: layout and fused FP8 dispatch still equal the oracle."""
+    w = wl.NORMAL.with_(use_fp8=True, hidden=512)
+    d = wl.generate(w)
+    buf = make_buffer(w, max_sms=max_sms)
+    t = ep.ep_get_tuning(buf.ctx)
+    t.layout_form = 2
+    ep.ep_set_tuning(buf.ctx, t)
+    from helpers import bits_to_bf16
+    (q, sc), cnt, h = buf.low_latency_dispatch(bits_to_bf16(d["x_bits"]), torch.from_numpy(d["topk_idx"]).cuda(),
+                                               w.max_tokens_per_rank, w.num_experts, use_fp8=True)
+    assert buf.device_status() == ep.EP_OK
+    o = oracle.layout(d["topk_idx"], w.num_experts, w.max_tokens_per_rank, ORACLE_LAYOUT[w.layout])
+    assert np.array_equal(h.tensors()["slot"].cpu().numpy(), o["slot"])
+    assert np.array_equal(cnt.cpu().numpy(), o["tokens_per_expert"])
+    rows = valid_rows(o["slot"])
+    qo, so = oracle.dispatch(d["x_bits"].reshape(w.num_tokens, w.hidden), o["slot"], o["rows"], True)
+    rd = torch.from_numpy(rows.astype(np.int64)).cuda()
+    assert np.array_equal(e4m3_to_bits(q.view(torch.uint8)[rd]), qo[rows])
+    assert np.array_equal(sc[rd].cpu().numpy().view(np.uint32), so[rows].view(np.uint32))
+    ntr, nte, itr, h2 = buf.get_dispatch_layout(torch.from_numpy(d["topk_idx"]).cuda())
+    assert buf.device_status() == ep.EP_OK
+    t2 = h2.tensors()
+    for k in ("cnt_er", "off_er", "base", "tokens_per_expert"):
+        assert np.array_equal(t2[k].cpu().numpy(), o[k]), k
+    assert np.array_equal(ntr.cpu().numpy(), o["tokens_per_rank"])
+    assert np.array_equal(itr.cpu().numpy().astype(np.uint8), o["is_token_in_rank"])
