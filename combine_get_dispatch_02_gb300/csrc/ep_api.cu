@@ -746,6 +746,12 @@ ep_status ep_handle_create(ep_ctx *ctx, ep_handle **out) {
         ep_handle_destroy(h);
         return EP_ERR_OOM;
     }
+    // the grid-form layout's barrier counter starts at zero (each launch puts it back)
+    if (cudaMemset(h->cta_hist + grid_hist_ints(ctx), 0, 16 * sizeof(int32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        ep_handle_destroy(h);
+        return EP_ERR_CUDA;
+    }
     *out = h;
     return EP_OK;
 }

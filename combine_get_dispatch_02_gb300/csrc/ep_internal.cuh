@@ -42,7 +42,8 @@ struct LayoutParams {
     int32_t er_span;           // set by launch_layout: ranks per CTA for the (e, r) counts
     // grid form (launch_layout_grid): per-CTA key totals -> prefixes [grid_ctas][E]
     int32_t *cta_hist;
-    uint32_t *grid_bar;           // grid form: barrier counter (zeroed before each launch)
+    uint32_t *grid_bar;           // grid form: barrier counter (zero between launches; each launch
+                                  // puts it back to zero as its last CTA leaves)
     int32_t grid_ctas, grid_tpc;  // set by launch_layout_grid: CTAs, tokens per CTA
 };
 
@@ -59,8 +60,9 @@ bool layout_pick_shape(int E, int R, int *cluster_size, int *threads, bool many_
 constexpr int64_t kLayoutManyEntries = 65536;
 // The same layout from one cooperative kernel over `ctas` CTAs (count, scan,
 // write, between grid barriers), for many entries: the single cluster leaves
-// most SMs idle.  Needs p.cta_hist with ctas * E ints and p.grid_bar.  Zeroes
-// the barrier, tokens_per_rank and cnt_er itself.  ctas <= 512.
+// most SMs idle.  Needs p.cta_hist with ctas * E ints and p.grid_bar (zero
+// before the first launch).  Zeroes tokens_per_rank and cnt_er itself; no
+// host-side copy precedes it.  ctas <= 512.
 cudaError_t launch_layout_grid(LayoutParams p, int ctas, cudaStream_t stream);
 // Entries from which the grid form is used (measured crossovers of the time
 // layout + dispatch adds to dispatch alone: expert layout 32K / 64K entries

@@ -99,14 +99,26 @@ __device__ __forceinline__ int64_t load_raw(const int64_t *idx, int i, int i1) {
 
 // Key of entry i with raw id e: its expert, or in rank mode the rank that
 // owns the expert when no earlier k of the same token goes to that rank; -1
-// for none.  Ids outside [-1, num_experts) are flagged and skipped.
+// for none.  Ids outside [-1, num_experts) are flagged and skipped.  Called
+// by all 32 lanes of a warp on 32 consecutive entries that start at a token
+// boundary (rounds of 32 entries from a token-aligned start): when K divides
+// 32 the earlier entries of a lane's token are the K - 1 lanes before it, so
+// rank mode compares with them by shuffles instead of re-reading topk_idx.
 __device__ __forceinline__ int to_key(const LayoutParams &p, int64_t e, int i) {
-    if (e < 0 || e >= p.num_experts) {
-        if (e != -1) atomicOr(p.status, kStatusBadExpert);
-        return -1;
+    const bool valid = e >= 0 && e < p.num_experts;
+    if (!valid && e != -1) atomicOr(p.status, kStatusBadExpert);
+    if (!p.rank_mode) return valid ? (int)e : -1;
+    const int d = valid ? (int)e / p.L : -1;
+    if ((32 % p.K) == 0) {  // warp-uniform
+        const int kk = i % p.K;  // this entry's k
+        bool first = d >= 0;
+        for (int s = 1; s < p.K; ++s) {
+            const int dp = __shfl_up_sync(0xFFFFFFFFu, d, s);
+            if (s <= kk && dp == d) first = false;
+        }
+        return first ? d : -1;
     }
-    if (!p.rank_mode) return (int)e;
-    const int d = (int)e / p.L;
+    if (d < 0) return -1;
     for (int j = (i / p.K) * p.K; j < i; ++j) {
         const int64_t e2 = __ldg(p.topk_idx + j);
         if (e2 >= 0 && e2 < p.num_experts && (int)e2 / p.L == d) return -1;
@@ -442,9 +454,12 @@ bool fits(int E, int R, int cl) {
 //   barrier
 //   write    packed bases (a block scan of the totals, in every CTA), then
 //            slot = base + prefix + position, src_info, rank-mode rows
-// The barriers are a counter the host zeroes before the launch; each wait is
-// bounded (about one second): on expiry the kernel sets kStatusTimeout and
-// returns.  The dispatch queued behind (programmatic dependent launch) may
+// The barriers are one counter (zero between launches: the last CTA to leave
+// puts it back); each wait is bounded (about one second): on expiry the
+// kernel sets kStatusTimeout, still counts the arrivals it owes and leaves.
+// The counts the layout accumulates with atomics are zeroed in the kernel
+// before the first barrier and accumulated after it, so no host-side copy
+// precedes the launch.  The dispatch queued behind (programmatic dependent launch) may
 // start casting rows at once.
 // threads per CTA of the grid form: 1024 from kGridBigEntries entries on (more
 // warps per CTA shorten the count and write phases), 512 below (cheaper
@@ -462,6 +477,9 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ void red_add_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 // Arrive at the grid barrier and wait (bounded) until `target` CTAs have
 // arrived.  Every CTA of the grid is resident (cooperative launch), so the
@@ -469,8 +487,9 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
 __device__ bool grid_barrier(uint32_t *bar, uint32_t target, int *flag) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();  // this CTA's writes before the arrival
-        atomicAdd(bar, 1u);
+        // the arrival releases this CTA's writes (ordered before it by the
+        // CTA barrier above); the polling load acquires the other CTAs'
+        red_add_release_gpu(bar, 1u);
         bool ok = true;
         const uint64_t t0 = grid_now_ns();
         while (ld_acquire_gpu(bar) < target) {
@@ -478,13 +497,21 @@ __device__ bool grid_barrier(uint32_t *bar, uint32_t target, int *flag) {
                 ok = false;
                 break;
             }
-            __nanosleep(32);  // fewer polls of the counter's line while the arrivals land
         }
-        __threadfence();
         *flag = ok ? 1 : 0;
     }
     __syncthreads();
     return *flag != 0;
+}
+
+// Leaving the grid's barriers (thread 0 of a CTA): one more count per CTA,
+// and the last of the 3C counts (C arrivals at each of the two barriers, C
+// departures) puts the counter back to zero for the next launch.  A CTA
+// that gave up waiting still adds every count it owes (`owed` arrivals it
+// skipped, then its departure), so the counter always ends at zero.
+__device__ void grid_depart(uint32_t *bar, uint32_t C, uint32_t owed) {
+    const uint32_t old = atomicAdd(bar, owed + 1u);
+    if (old + owed + 1u == 3u * C) atomicExch(bar, 0u);
 }
 
 template <int NT>
@@ -578,32 +605,90 @@ __global__ void __launch_bounds__(NT, 1) layout_grid_kernel(const LayoutParams p
         }
         p.cta_hist[(int64_t)c * E + e] = s;
     }
-    if (p.tokens_per_rank)  // zeroed before this kernel
-        for (int d = tid; d < R; d += NT)
-            if (tok_rank[d] != 0) atomicAdd(&p.tokens_per_rank[d], tok_rank[d]);
-    if (want_er)  // zeroed before this kernel
-        for (int j = tid; j < E * span; j += NT)
-            if (hist_er[j] != 0) atomicAdd(&p.cnt_er[(j / span) * R + r0 + j % span], hist_er[j]);
+    // the per-rank and per-(expert, rank) counts are zeroed here, in slices,
+    // and accumulated after the barrier
+    if (p.tokens_per_rank && c == 0)
+        for (int d = tid; d < R; d += NT) p.tokens_per_rank[d] = 0;
+    if (want_er) {
+        const int64_t n = (int64_t)E * R, sl = (n + C - 1) / C;
+        for (int64_t j = c * sl + tid; j < min(n, (c + 1) * sl); j += NT) p.cnt_er[j] = 0;
+    }
     if (!grid_barrier(p.grid_bar, (uint32_t)C, &bar_ok)) {
-        if (tid == 0) atomicOr(p.status, kStatusTimeout);
+        if (tid == 0) {
+            atomicOr(p.status, kStatusTimeout);
+            grid_depart(p.grid_bar, (uint32_t)C, 1u);
+        }
         return;
     }
+    if (p.tokens_per_rank)
+        for (int d = tid; d < R; d += NT)
+            if (tok_rank[d] != 0) atomicAdd(&p.tokens_per_rank[d], tok_rank[d]);
+    if (want_er)
+        for (int j = tid; j < E * span; j += NT)
+            if (hist_er[j] != 0) atomicAdd(&p.cnt_er[(j / span) * R + r0 + j % span], hist_er[j]);
 
     // ---------------- scan of the keys this CTA owns
-    const int ke0 = (int)((int64_t)c * E / C), ke1 = (int)((int64_t)(c + 1) * E / C);
-    for (int e = ke0; e < ke1; ++e) {
-        const int v = tid < C ? __ldcg(&p.cta_hist[(int64_t)tid * E + e]) : 0;
-        int total;
-        const int excl = block_exclusive_scan<NT>(v, scan, &total);
-        if (tid < C) p.cta_hist[(int64_t)tid * E + e] = excl;
-        if (tid == 0) {
-            const int n = (int)min((int64_t)total, p.cap);
-            p.tokens_per_expert[e] = n;
-            if (p.user_tokens_per_expert) p.user_tokens_per_expert[e] = n;
-            if (p.layout == kLayoutPadded) p.base[e] = (int64_t)e * p.cap;
+    // one warp per owned key: lane l takes CTAs [l*per, (l+1)*per) (all its
+    // loads in flight at once), a shuffle scan over the lanes gives each
+    // slice its start; the same warp then turns the key's per-rank counts
+    // into offsets
+    {
+        const int ke0 = (int)((int64_t)c * E / C), ke1 = (int)((int64_t)(c + 1) * E / C);
+        const int per = (C + 31) / 32;  // CTAs per lane: at most 8 up to 256 CTAs, 16 up to 512
+        for (int e = ke0 + w; e < ke1; e += NW) {
+            int v[8];
+            int local = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int cc = lane * per + j;
+                v[j] = (j < per && cc < C) ? __ldcg(&p.cta_hist[(int64_t)cc * E + e]) : 0;
+                local += v[j];
+            }
+            for (int j = 8; j < per; ++j) {  // more than 256 CTAs
+                const int cc = lane * per + j;
+                if (cc < C) local += __ldcg(&p.cta_hist[(int64_t)cc * E + e]);
+            }
+            int incl = local;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= d) incl += y;
+            }
+            int run = incl - local;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int cc = lane * per + j;
+                if (j < per && cc < C) p.cta_hist[(int64_t)cc * E + e] = run;
+                run += v[j];
+            }
+            for (int j = 8; j < per; ++j) {
+                const int cc = lane * per + j;
+                if (cc < C) {
+                    const int x = __ldcg(&p.cta_hist[(int64_t)cc * E + e]);
+                    p.cta_hist[(int64_t)cc * E + e] = run;
+                    run += x;
+                }
+            }
+            const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            if (lane == 0) {
+                const int n = (int)min((int64_t)total, p.cap);
+                p.tokens_per_expert[e] = n;
+                if (p.user_tokens_per_expert) p.user_tokens_per_expert[e] = n;
+                if (p.layout == kLayoutPadded) p.base[e] = (int64_t)e * p.cap;
+            }
         }
-        if (want_er && w == 0) {  // offsets over the source ranks
-            int run = 0;
+    }
+    if (!grid_barrier(p.grid_bar, 2u * (uint32_t)C, &bar_ok)) {
+        if (tid == 0) {
+            atomicOr(p.status, kStatusTimeout);
+            grid_depart(p.grid_bar, (uint32_t)C, 0u);
+        }
+        return;
+    }
+    if (want_er) {  // the (expert, rank) counts are complete: offsets over the source ranks
+        const int ke0 = (int)((int64_t)c * E / C), ke1 = (int)((int64_t)(c + 1) * E / C);
+        for (int e = ke0 + w; e < ke1; e += NW) {
+            int rrun = 0;
             for (int rr = 0; rr < R; rr += 32) {
                 const int r = rr + lane;
                 const int cv = r < R ? __ldcg(&p.cnt_er[e * R + r]) : 0;
@@ -613,14 +698,10 @@ __global__ void __launch_bounds__(NT, 1) layout_grid_kernel(const LayoutParams p
                     const int y = __shfl_up_sync(0xFFFFFFFFu, x, d);
                     if (lane >= d) x += y;
                 }
-                if (r < R) p.off_er[e * R + r] = run + x - cv;
-                run += __shfl_sync(0xFFFFFFFFu, x, 31);
+                if (r < R) p.off_er[e * R + r] = rrun + x - cv;
+                rrun += __shfl_sync(0xFFFFFFFFu, x, 31);
             }
         }
-    }
-    if (!grid_barrier(p.grid_bar, 2u * (uint32_t)C, &bar_ok)) {
-        if (tid == 0) atomicOr(p.status, kStatusTimeout);
-        return;
     }
 
     // ---------------- write
@@ -671,6 +752,7 @@ __global__ void __launch_bounds__(NT, 1) layout_grid_kernel(const LayoutParams p
         }
         p.slot[i] = s;
     }
+    if (tid == 0) grid_depart(p.grid_bar, (uint32_t)C, 0u);
 }
 
 size_t grid_smem(int E, int R, int span, int NT) {
@@ -726,12 +808,6 @@ cudaError_t launch_layout_grid(LayoutParams p, int ctas, cudaStream_t stream) {
     }
     const size_t smem = grid_smem(p.E, p.R, p.er_span, NT);
     if (smem > kMaxSmem) return cudaErrorInvalidConfiguration;
-    cudaError_t e = cudaMemsetAsync(p.grid_bar, 0, sizeof(uint32_t), stream);
-    if (e == cudaSuccess && p.tokens_per_rank != nullptr)
-        e = cudaMemsetAsync(p.tokens_per_rank, 0, (size_t)p.R * sizeof(int32_t), stream);
-    if (e == cudaSuccess && p.cnt_er != nullptr)
-        e = cudaMemsetAsync(p.cnt_er, 0, (size_t)p.E * p.R * sizeof(int32_t), stream);
-    if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: the grid barriers end
     attr[0].val.cooperative = 1;
@@ -742,8 +818,8 @@ cudaError_t launch_layout_grid(LayoutParams p, int ctas, cudaStream_t stream) {
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = NT == 1024 ? cudaLaunchKernelEx(&cfg, layout_grid_kernel<1024>, p)
-                   : cudaLaunchKernelEx(&cfg, layout_grid_kernel<512>, p);
+    cudaError_t e = NT == 1024 ? cudaLaunchKernelEx(&cfg, layout_grid_kernel<1024>, p)
+                               : cudaLaunchKernelEx(&cfg, layout_grid_kernel<512>, p);
     if (e == cudaErrorCooperativeLaunchTooLarge) return cudaErrorInvalidConfiguration;
     return e;
 }

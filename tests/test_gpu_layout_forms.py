@@ -160,3 +160,26 @@ def test_grid_form_under_an_sm_cap(max_sms):
         assert np.array_equal(t2[k].cpu().numpy(), o[k]), k
     assert np.array_equal(ntr.cpu().numpy(), o["tokens_per_rank"])
     assert np.array_equal(itr.cpu().numpy().astype(np.uint8), o["is_token_in_rank"])
+
+
+def test_grid_form_repeated_launches_with_changing_sizes():
+    """The grid form's barrier counter is back at zero after every launch:
+    many launches on one handle, with token counts that change the number of
+    CTAs, each give the oracle's layout."""
+    w0 = wl.NORMAL.with_(hidden=512)
+    buf = _buf(w0, 2)
+    h = buf.new_handle()
+    rng = np.random.default_rng(12)
+    for it in range(24):
+        T = int(rng.choice([1, 7, 100, 999, 2048, 4096]))
+        w = w0.with_(tokens_per_rank=T, seed=w0.seed + it)
+        idx = wl.generate(w, with_x=False)["topk_idx"]
+        ntr, nte, itr, _ = buf.get_dispatch_layout(torch.from_numpy(idx).cuda(), handle=h)
+        if it % 3 == 0 or it == 23:
+            assert buf.device_status() == ep.EP_OK
+            o = oracle.layout(idx, w.num_experts, w.max_tokens_per_rank, ORACLE_LAYOUT[w.layout])
+            t = h.tensors()
+            assert np.array_equal(t["slot"].cpu().numpy(), o["slot"]), (it, T)
+            assert np.array_equal(t["off_er"].cpu().numpy(), o["off_er"]), (it, T)
+            assert np.array_equal(ntr.cpu().numpy(), o["tokens_per_rank"]), (it, T)
+    assert buf.device_status() == ep.EP_OK
