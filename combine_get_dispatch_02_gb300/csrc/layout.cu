@@ -709,6 +709,7 @@ __global__ void __launch_bounds__(NT, 1) layout_grid_kernel(const LayoutParams p
     {
         const int chunk = (E + NT - 1) / NT;
         const int e_lo = min(E, tid * chunk), e_hi = min(E, e_lo + chunk);
+        for (int e = e_lo; e < e_hi; ++e) pre[e] = __ldcg(&p.cta_hist[(int64_t)c * E + e]);  // in flight during the scan
         int local = 0;
         if (p.layout != kLayoutPadded)
             for (int e = e_lo; e < e_hi; ++e) local += __ldcg(&p.tokens_per_expert[e]);
@@ -720,7 +721,6 @@ __global__ void __launch_bounds__(NT, 1) layout_grid_kernel(const LayoutParams p
                 run += __ldcg(&p.tokens_per_expert[e]);
                 if (c == 0) p.base[e] = b;
             }
-            pre[e] = __ldcg(&p.cta_hist[(int64_t)c * E + e]);
             hist_er[e] = (int32_t)b;  // the (e, r) counts are done with: reuse for the bases
         }
     }
