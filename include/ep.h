@@ -176,8 +176,7 @@ ep_status ep_handle_get_info(const ep_handle *handle, ep_handle_info *out);
  *                         entry on rank d, else 0
  *   handle                receives slot / src_info / counts / bases
  * One kernel: a thread-block cluster, or from 128K entries (rank layout:
- * 48K) a cooperative kernel over all SMs after zeroing copies of its grid
- * barrier and of the counts it accumulates (ep_tuning.layout_form forces
+ * 48K) a cooperative kernel over all SMs (ep_tuning.layout_form forces
  * either); no host synchronisation.  If a launch fails (EP_ERR_CUDA /
  * EP_ERR_UNSUPPORTED) the handle holds no layout afterwards (the calls that
  * need one return EP_ERR_NO_LAYOUT); host-side argument errors leave it as

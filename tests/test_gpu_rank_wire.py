@@ -288,3 +288,81 @@ def test_rank_wire_calls_replay_from_a_cuda_graph(wire):
     ref = oracle.combine(ye.reshape(N * K, H), np.where(m, np.arange(N * K).reshape(N, K), -1).astype(np.int32),
                          None)
     assert np.array_equal(bf16_to_bits(out), ref)
+
+
+def _random_case(i):
+    """Seeded random shape of the rank transport: 1-8 ranks including 3 and 5,
+    1-5 experts per rank, top-1 to top-10 (K not dividing 32 too), T in
+    [0, Tmax], masked entries and repeats, padded or packed, BF16 or FP8."""
+    rng = np.random.default_rng(7700 + i)
+    R = int(rng.choice([1, 2, 3, 4, 5, 8]))
+    L = int(rng.choice([1, 2, 3, 5]))
+    E = R * L
+    Tmax = int(rng.integers(1, 80))
+    T = 0 if i % 7 == 3 else int(rng.integers(1, Tmax + 1))
+    K = int(rng.integers(1, 11))
+    fp8 = i % 2 == 0
+    H = 128 * int(rng.integers(1, 9)) if fp8 else 8 * int(rng.integers(1, 129))
+    packed = bool(rng.integers(0, 2))
+    idx = rng.integers(-1, E, size=(R, T, K)).astype(np.int64)
+    return rng, idx, E, Tmax, H, fp8, packed
+
+
+@pytest.mark.parametrize("wire", [ep.EP_WIRE_DEVICE, ep.EP_WIRE_HOST])
+@pytest.mark.parametrize("i", range(10))
+def test_rank_wire_random_shapes(i, wire):
+    rng, idx, E, Tmax, H, fp8, packed = _random_case(i)
+    R, T, K = idx.shape
+    N = R * T
+    from combine_get_dispatch_02_gb300 import Buffer
+    buf = Buffer(R, Tmax, H, E, K, low_latency_mode=not packed)
+    xb = torch.from_numpy(rng.standard_normal((N, H)).astype(np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+    o = oracle.rank_layout(idx, None, E, Tmax, 1 if packed else 0)
+    runs = oracle.rank_runs(idx, E, o["rbase"])
+    h = buf.new_handle()
+    rows_s = ep.ep_rank_send_rows(buf.cfg)
+    if fp8:
+        send_x = torch.empty(rows_s, H, dtype=torch.float8_e4m3fn, device="cuda")
+        send_sc = torch.empty(rows_s, H // 128, dtype=torch.float32, device="cuda")
+    else:
+        send_x, send_sc = torch.empty(rows_s, H, dtype=torch.bfloat16, device="cuda"), None
+    stage = torch.empty(rows_s * (2 * H + H // 32), dtype=torch.uint8).pin_memory() \
+        if wire == ep.EP_WIRE_HOST else None
+    x = bits_to_bf16(xb) if N > 0 else torch.empty(0, H, dtype=torch.bfloat16, device="cuda")
+    ep.ep_rank_dispatch_send(buf.ctx, x, torch.from_numpy(idx).cuda(), None, T, fp8, None, None, h.raw,
+                             send_x, send_sc)
+    recv, sc = buf.alloc_rank_recv(fp8)
+    recv.view(torch.uint8).fill_(SENTINEL)
+    cnt = torch.full((R,), -1, dtype=torch.int32, device="cuda")
+    ep.ep_rank_dispatch_recv(buf.ctx, h.raw, fp8, send_x, send_sc, recv, sc, cnt, wire, stage)
+    assert buf.device_status() == ep.EP_OK
+    assert np.array_equal(cnt.cpu().numpy(), o["tokens_per_rank"])
+    cnt_r, so, ro = ep.ep_rank_runs(h.raw, R)
+    assert np.array_equal(np.array(cnt_r), runs["run_cnt"])
+    assert np.array_equal(np.array(so), runs["send_off"])
+    assert np.array_equal(np.array(ro), runs["recv_off"])
+    rows = o["rank_slot"][o["rank_slot"] >= 0]
+    got = recv.view(torch.uint8).cpu().numpy().reshape(o["rows"], -1)
+    if fp8:
+        q, s_ = oracle.dispatch(xb.reshape(N, H), o["rank_slot"], o["rows"], True)
+        assert np.array_equal(got[rows], q[rows])
+        rd = torch.from_numpy(rows.astype(np.int64)).cuda()
+        assert np.array_equal(sc[rd].cpu().numpy().view(np.uint32), s_[rows].view(np.uint32))
+    else:
+        ref = oracle.dispatch(xb.reshape(N, H), o["rank_slot"], o["rows"], False)
+        assert np.array_equal(got[rows].view(np.uint16), ref[rows])
+    assert np.all(np.delete(got, rows, axis=0) == SENTINEL)
+    # combine back over the same wire
+    ye = rng.standard_normal((N, K, H)).astype(np.float32)
+    ye = torch.from_numpy(ye).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    y = place_rows(buf.rank_rows, H, o["rank_slot"], ye, np.arange(N))
+    send_y = torch.empty(rows_s, H, dtype=torch.bfloat16, device="cuda")
+    out = torch.full((N, H), 7, dtype=torch.bfloat16, device="cuda")
+    ep.ep_rank_combine_send(buf.ctx, h.raw, y, send_y, wire, stage)
+    ep.ep_rank_combine_recv(buf.ctx, h.raw, send_y, out)
+    assert buf.device_status() == ep.EP_OK
+    m = o["rank_slot"] >= 0
+    ref = oracle.combine(ye.reshape(N * K, H), np.where(m, np.arange(N * K).reshape(N, K), -1).astype(np.int32),
+                         None) if N > 0 else np.zeros((0, H), np.uint16)
+    assert np.array_equal(bf16_to_bits(out), ref)
