@@ -31,6 +31,9 @@ int main(void) {
     CHECK(ep_recv_bytes(&c, 0, &payload, &scales) == EP_OK);
     CHECK(payload == (uint64_t)rows * 7168 * 2 && scales == 0);
     CHECK(ep_rank_recv_rows(&c, &rows) == EP_OK && rows == 32LL * 32 * 128);
+    CHECK(ep_rank_send_rows(&c, &rows) == EP_OK && rows == 32LL * 128 * 8);  /* R*Tmax*min(K, R) */
+    ep_test_hooks hooks = {-2, 0};
+    CHECK(ep_set_test_hooks(NULL, &hooks) == EP_ERR_INVALID_ARG);
 
     ep_config packed = c;
     packed.layout = EP_LAYOUT_PACKED;
