@@ -420,21 +420,19 @@ void dispatch_init() {
 }
 
 namespace {
-// Row buffers in the ring and the dynamic shared memory of one CTA: as many
-// buffers (8, 6, 4 or 2) as fit in one CTA's share of the SM when `blocks`
-// CTAs share it, and at least the size that keeps a further CTA off the SM
-// (row_smem_for_occupancy).  Deeper rings let the producers run further
-// ahead of the copies (BF16 rows of 14 KB: 8 buffers instead of 4).
+// Row buffers in the ring and the dynamic shared memory of one CTA: the
+// size that keeps a further row CTA off the SM (row_smem_for_occupancy),
+// and as many buffers (8, 6, 4 or 2) as fit in it.  The share of the SM this
+// leaves free is where the next kernel's CTAs start while the dispatch ends
+// (it lets them launch early): a ring sized to the whole share (8 BF16 rows
+// of 14 KB) left no room for them, and the BF16 step behind it took 1575
+// instead of 1338 us at 8 x 4096 tokens, for no gain in the dispatch itself.
 void row_ring(bool fp8, int H, int blocks, int *nb, size_t *smem) {
     const size_t rowb = fp8 ? (size_t)H + H / 32 : 2 * (size_t)H;
     const size_t cap = row_smem_for_occupancy(fp8, H, blocks);
-    int64_t share = g_smem_per_sm > 0 ? (int64_t)g_smem_per_sm / blocks - g_smem_reserved - 256 : 0;
-    if (share > (int64_t)g_smem_per_block - 256) share = (int64_t)g_smem_per_block - 256;
-    const int64_t fit = share > 0 ? share / (int64_t)rowb : 0;
-    const int n = fit >= 8 ? 8 : (fit >= 6 ? 6 : (fit >= 4 ? 4 : 2));
-    const size_t want = (size_t)n * rowb;
-    *nb = n;
-    *smem = ((want > cap ? want : cap) + 15) / 16 * 16;
+    const size_t fit = cap / rowb;
+    *nb = fit >= 8 ? 8 : (fit >= 6 ? 6 : (fit >= 4 ? 4 : 2));
+    *smem = cap;  // >= 2 rows
 }
 
 template <bool FP8>
