@@ -71,6 +71,9 @@ def _args():
                     help="reps per chunk size of the dispatch -> identity expert -> combine round trip (0: skip)")
     ap.add_argument("--wire-reps", type=int, default=10,
                     help="with --rank: reps of the rank transport's wire calls (device and host wire; 0: skip)")
+    ap.add_argument("--ceilings", action="store_true",
+                    help="time plain torch write-only, read-only and copy kernels over 8 GB (the HBM ceilings "
+                         "of each traffic mix) instead of the bench step")
     return ap.parse_args()
 
 
@@ -975,8 +978,52 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_ceilings(args):
+    """HBM bandwidth of plain torch kernels by traffic mix: a fill (writes
+    only), a sum (reads only) and a copy (half each), each over 8 GB, medians
+    of 20 runs.  The dispatch's traffic is mostly writes (K rows written per
+    row read), the combine's mostly reads: these say which ceiling each one
+    meets."""
+    import torch
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = _peaks()
+    n = 8 << 30
+    a = torch.empty(n, dtype=torch.uint8, device="cuda")
+    b = torch.empty(n // 2, dtype=torch.uint8, device="cuda")
+    f = a.view(torch.float32)
+    sink = torch.empty(1, device="cuda")
+
+    def timed(fn, reps=20):
+        ts = []
+        for i in range(reps + 3):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= 3:
+                ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.median([x.elapsed_time(y) * 1e-3 for x, y in ts])
+
+    a.fill_(1)
+    res = {
+        "write_only_gbs": n / timed(lambda: a.fill_(2)) / 1e9,
+        "read_only_gbs": n / timed(lambda: torch.sum(f, dim=0, keepdim=True, out=sink)) / 1e9,
+        "copy_gbs": n / timed(lambda: b.copy_(a[: n // 2])) / 1e9,
+    }
+    out = {"ceilings": {k: round(v, 1) for k, v in res.items()}, "bytes_each": n,
+           "peak_gbs": peak, "peak_kind": peak_kind}
+    out["ceilings_frac_of_peak"] = {k: round(v / peak, 3) for k, v in res.items()}
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = _args()
+    if args.ceilings:
+        run_ceilings(args)
+        return
     if args.sweep:
         run_sweep(args)
         return
