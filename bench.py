@@ -71,6 +71,9 @@ def _args():
                     help="reps per chunk size of the dispatch -> identity expert -> combine round trip (0: skip)")
     ap.add_argument("--wire-reps", type=int, default=10,
                     help="with --rank: reps of the rank transport's wire calls (device and host wire; 0: skip)")
+    ap.add_argument("--kernels", action="store_true",
+                    help="time the dispatch kernels (the rule's, row, warp-item, token) on the workload, "
+                         "cached layout and behind the layout kernel, instead of the bench step")
     ap.add_argument("--ceilings", action="store_true",
                     help="time plain torch write-only, read-only and copy kernels over 8 GB (the HBM ceilings "
                          "of each traffic mix) instead of the bench step")
@@ -978,6 +981,75 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_kernels(args):
+    """The dispatch of the workload with each kernel (ep_tuning.dispatch_kernel
+    0 = the rule's choice, 1 = row, 2 = warp-item, 3 = token): median µs of
+    20 runs on the cached layout and behind the layout kernel, L2 flushed
+    before each, and the cached time's fraction of the HBM peak."""
+    import torch
+    from combine_get_dispatch_02_gb300 import Buffer, ep
+    from combine_get_dispatch_02_gb300 import build as epbuild
+    from combine_get_dispatch_02_gb300 import workloads as wl
+    epbuild.build()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = _peaks()
+    w = wl.WORKLOADS[args.workload]
+    if args.layout is not None:
+        w = w.with_(layout=args.layout)
+    if args.dtype is not None:
+        w = w.with_(use_fp8=(args.dtype == "fp8"))
+    if args.hidden is not None:
+        w = w.with_(hidden=args.hidden)
+    d = wl.generate(w)
+    N, K, H = w.num_tokens, w.topk, w.hidden
+    x = torch.from_numpy(np.ascontiguousarray(d["x_bits"]).view(np.int16)).cuda().view(torch.bfloat16)
+    idx = torch.from_numpy(d["topk_idx"]).cuda()
+    buf = Buffer(w.num_ranks, w.max_tokens_per_rank, H, w.num_experts, K, low_latency_mode=(w.layout == wl.PADDED))
+    recv, scales = buf.alloc_recv(w.use_fp8)
+    h = buf.new_handle()
+    ctx = buf.ctx
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush_w = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
+    flush_r = torch.ones(2 * l2 // 4, dtype=torch.float32, device="cuda")
+    sink = torch.empty(1, device="cuda")
+
+    def timed(fn, reps=20):
+        ts = []
+        for i in range(reps + 3):
+            flush_w.fill_(1)
+            torch.sum(flush_r, dim=0, keepdim=True, out=sink)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            if i >= 3:
+                ts.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median([a.elapsed_time(b) * 1e3 for a, b in ts])
+
+    ep.ep_dispatch(ctx, x, idx, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales, None, stream)
+    M = int((h.tensors()["slot"] >= 0).sum().item())
+    _, disp_bytes, _ = _algorithmic_bytes(w, M)
+    res = {}
+    for kern, name in ((0, "rule"), (1, "row"), (2, "warp_item"), (3, "token")):
+        t = ep.ep_get_tuning(ctx)
+        t.dispatch_kernel = kern
+        t.dispatch_ctas_per_sm = 0
+        ep.ep_set_tuning(ctx, t)
+        cached = timed(lambda: ep.ep_dispatch(ctx, x, None, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales,
+                                              None, stream))
+        fresh = timed(lambda: ep.ep_dispatch(ctx, x, idx, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales,
+                                             None, stream))
+        res[name] = {"cached_us": round(cached, 1), "with_layout_us": round(fresh, 1),
+                     "cached_frac": round(disp_bytes / (cached / 1e6) / 1e9 / peak, 3)}
+    if buf.device_status() != ep.EP_OK:
+        raise RuntimeError("device status error")
+    print(json.dumps({"workload": _workload_desc(w), "rows": M, "dispatch_bytes": disp_bytes,
+                      "peak_gbs": peak, "peak_source": peak_kind, "kernels": res}), flush=True)
+
+
 def run_ceilings(args):
     """HBM bandwidth of plain torch kernels by traffic mix: a fill (writes
     only), a sum (reads only) and a copy (half each), each over 8 GB, medians
@@ -1007,9 +1079,10 @@ def run_ceilings(args):
         torch.cuda.synchronize()
         return statistics.median([x.elapsed_time(y) * 1e-3 for x, y in ts])
 
-    a.fill_(1)
+    f.fill_(1.0)
     res = {
-        "write_only_gbs": n / timed(lambda: a.fill_(2)) / 1e9,
+        # fp32 elements: torch's fill then stores 16 bytes per thread and vector
+        "write_only_gbs": n / timed(lambda: f.fill_(2.0)) / 1e9,
         "read_only_gbs": n / timed(lambda: torch.sum(f, dim=0, keepdim=True, out=sink)) / 1e9,
         "copy_gbs": n / timed(lambda: b.copy_(a[: n // 2])) / 1e9,
     }
@@ -1023,6 +1096,9 @@ def main():
     args = _args()
     if args.ceilings:
         run_ceilings(args)
+        return
+    if args.kernels:
+        run_kernels(args)
         return
     if args.sweep:
         run_sweep(args)

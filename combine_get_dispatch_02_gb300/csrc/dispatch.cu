@@ -7,11 +7,13 @@
 // cast is per 128 channels: amax = max |x|, a = max(amax, 1e-4),
 // scale = a / 448, q = e4m3(x * (448 / a)), nearest-even with saturation.
 //
-// Two kernels.  For hidden sizes that are a multiple of 512 (all the
-// workloads) the row kernel below stages a whole token row in shared memory
-// and writes it with bulk asynchronous copies (producer warps and an issuer
-// warp handing buffers over through mbarriers).  Otherwise the warp-item
-// kernel does:
+// Three kernels.  Large dispatches (from 64K receive rows) run the token
+// kernel: one CTA per token holds the row in registers and writes it to
+// every receive row with 16-byte stores.  Otherwise, for hidden sizes that
+// are a multiple of 512 (all the workloads), the row kernel stages a whole
+// token row in shared memory and writes it with bulk asynchronous copies
+// (producer warps and an issuer warp handing buffers over through
+// mbarriers).  Otherwise the warp-item kernel does:
 // the work item is (token, 512-channel chunk) for one warp, 16
 // channels (two 16-byte loads) per lane.  The token row is read once from
 // HBM (read-only, no L1 allocation), cast once, and written K times with
@@ -253,6 +255,79 @@ __device__ __forceinline__ void put_row(uint8_t *row, int t, int H, uint4 ca, ui
     }
 }
 
+// ---------------------------------------------------------------- token kernel
+// TPB tokens per CTA, a short-lived grid of N / TPB CTAs (or a persistent
+// grid looping over the tokens when the SMs are limited).  H/16 threads: for
+// FP8 thread t holds channels [16t, 16t + 16) (two 16-byte loads) and casts
+// them once (8 threads per 128-channel block, the amax by three xor
+// shuffles); for BF16 thread t holds the row's 16-byte vectors t and
+// t + H/16, so every store instruction of a warp writes 512 contiguous
+// bytes.  All TPB rows are loaded before the first is stored (more reads in
+// flight per CTA); each row then goes to the receive row of every top-k
+// entry with plain 16-byte stores, one contiguous row written by the whole
+// CTA within a few store instructions per warp.  Every CTA lets the next
+// kernel launch as it starts (the dependents start once the last CTA has
+// started); x may be read before the slots are waited for behind this
+// library's own layout kernel (early_x).
+template <bool FP8, int TPB>
+__global__ void __launch_bounds__(1024, 1) dispatch_token_kernel(const DispatchParams p) {
+    pdl_launch_dependents();
+    const int H = p.H, K = p.K, nt = H / 16;
+    const int t = threadIdx.x, lane = t & 31;
+    const bool act = t < nt;  // the block is rounded up to whole warps
+    bool waited = false;
+    if (p.count_dst != nullptr && blockIdx.x == 0) {
+        pdl_wait();
+        waited = true;
+        for (int e = t; e < p.E; e += blockDim.x) p.count_dst[e] = p.count_src[e];
+    }
+    if (!p.early_x && !waited) {  // x may be the output of the kernel just before
+        pdl_wait();
+        waited = true;
+    }
+    const uint4 *x = static_cast<const uint4 *>(p.x);  // H / 8 vectors per row
+    const int64_t nv = H / 8;
+    const int i0 = FP8 ? 2 * t : t, i1 = FP8 ? 2 * t + 1 : t + nt;
+    for (int64_t g0 = (int64_t)blockIdx.x * TPB; g0 < p.N; g0 += (int64_t)gridDim.x * TPB) {
+        uint4 a[TPB], b[TPB];
+#pragma unroll
+        for (int u = 0; u < TPB; ++u) {
+            a[u] = make_uint4(0, 0, 0, 0);
+            b[u] = a[u];
+            if (act && g0 + u < p.N) {
+                a[u] = ld_nc_na_v4(x + (g0 + u) * nv + i0);
+                b[u] = ld_nc_na_v4(x + (g0 + u) * nv + i1);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < TPB; ++u) {
+            const int64_t g = g0 + u;
+            if (g >= p.N) break;  // block-uniform
+            uint4 q = make_uint4(0, 0, 0, 0);
+            float scale = 0.0f;
+            if constexpr (FP8) cast16(a[u], b[u], q, scale);
+            if (!waited) {
+                pdl_wait();  // the slots of the layout kernel
+                waited = true;
+            }
+            const int32_t my_slot = slot_of(p, g, lane);
+            for (int k = 0; k < K; ++k) {
+                const int32_t s = __shfl_sync(0xFFFFFFFFu, my_slot, k);
+                if (s < 0 || !act) continue;
+                if constexpr (FP8) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.recv) + (int64_t)s * H);
+                    dst[t] = q;
+                    if ((t & 7) == 0) p.recv_scales[(int64_t)s * (H / 128) + (t >> 3)] = scale;
+                } else {
+                    uint4 *dst = static_cast<uint4 *>(p.recv) + (int64_t)s * nv;
+                    dst[i0] = a[u];
+                    dst[i1] = b[u];
+                }
+            }
+        }
+    }
+}
+
 template <bool FP8, int NB>
 __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchParams p) {
     extern __shared__ __align__(128) uint8_t row_smem[];
@@ -350,6 +425,23 @@ __global__ void __launch_bounds__(1024, 1) dispatch_row_kernel(const DispatchPar
 }
 
 bool row_kernel_fits(int H) { return H % 512 == 0 && H / 16 + 32 <= 1024; }
+
+}  // namespace
+
+bool token_kernel_fits(int H, bool fp8) { return H % (fp8 ? 128 : 16) == 0 && H / 16 <= 1024; }
+
+// Measured over the sweep grid (T >= 32 tokens per rank, R in {8, 32}, H in
+// {2048, 4096, 7168}, top-2/6/8, BF16 and FP8, cached layout): from 64K
+// receive rows the token kernel takes 0.88-0.94 of the row kernel's time,
+// except FP8 at top-2 (1.06-1.17: a 7 KB row written twice per 14 KB read,
+// where the row kernel's reads two tokens ahead matter more); at 32K rows and
+// below it ties or loses (the low-latency size, where the row kernel's ring
+// also overlaps more of the layout kernel before it).
+bool token_kernel_rule(int64_t N, int K, int H, bool fp8, bool sm_limited) {
+    return !sm_limited && token_kernel_fits(H, fp8) && N * K >= 65536 && !(fp8 && K <= 2);
+}
+
+namespace {
 
 size_t row_smem_bytes(bool fp8, int H) { return 2 * (size_t)(fp8 ? H + H / 32 : 2 * H); }
 
@@ -451,6 +543,24 @@ cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks, b
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (p.token_grid > 0 && token_kernel_fits(p.H, fp8)) {
+        const int tpb = p.token_tpb >= 2 ? 2 : 1;
+        const int64_t need = (p.N + tpb - 1) / tpb;
+        int64_t blocks = need < p.token_grid ? need : p.token_grid;
+        if (blocks < 1) blocks = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+        cfg.blockDim = dim3((unsigned)((p.H / 16 + 31) / 32 * 32), 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        if (p.token_tpb >= 2)
+            return fp8 ? cudaLaunchKernelEx(&cfg, dispatch_token_kernel<true, 2>, p)
+                       : cudaLaunchKernelEx(&cfg, dispatch_token_kernel<false, 2>, p);
+        return fp8 ? cudaLaunchKernelEx(&cfg, dispatch_token_kernel<true, 1>, p)
+                   : cudaLaunchKernelEx(&cfg, dispatch_token_kernel<false, 1>, p);
+    }
     if (row_kernel_fits(p.H) && p.row_sms > 0) {
         const int bps = p.row_bps > 0 ? p.row_bps : row_blocks_per_sm(p.H, fp8);
         int64_t blocks = (int64_t)p.row_sms * bps;

@@ -239,6 +239,19 @@ ep_status enqueue_dispatch(ep_ctx *ctx, const ep_handle *h, const void *x, int64
     const bool short_fp8 = fp8 && (c.hidden <= 1024 || (c.hidden <= 2048 && c.topk <= 4));
     if (kern == 2 || (kern == 0 && short_fp8)) p.row_sms = 0;
     p.row_bps = ctx->tune.dispatch_ctas_per_sm;
+    p.token_grid = 0;
+    p.token_tpb = ctx->tune.dispatch_ctas_per_sm >= 2 ? 2 : 1;
+    // the token kernel when tuned so, and by the rule for large dispatches
+    // on all SMs (from 64K receive rows; not FP8 at top-1/2)
+    const bool limited = p.row_sms < ctx->num_sms;
+    const bool token = kern == 3 || (kern == 0 && !short_fp8 && ep::token_kernel_rule(p.N, p.K, c.hidden, fp8, limited));
+    if (token && ep::token_kernel_fits(c.hidden, fp8)) {
+        // one CTA per token; on an SM budget a grid of that many SMs' worth
+        // of CTAs loops over the tokens
+        const int nt = (c.hidden / 16 + 31) / 32 * 32;
+        const int bps = nt >= 2048 ? 1 : 2048 / nt;
+        p.token_grid = p.row_sms < ctx->num_sms ? (int64_t)p.row_sms * bps : p.N;
+    }
     p.status = ctx->d_status;
     p.early_x = behind_layout ? 1 : 0;
     const int cap = grid_cap(ctx, fp8 ? ctx->dispatch_bps_fp8 : ctx->dispatch_bps_bf16);
@@ -1274,7 +1287,7 @@ ep_status ep_set_tuning(ep_ctx *ctx, const ep_tuning *t) {
     if (t->combine_chunks != 0 && t->combine_chunks != 1 && t->combine_chunks != 2 && t->combine_chunks != 4)
         return EP_ERR_INVALID_ARG;
     if (t->round_trip_chunk < 0) return EP_ERR_INVALID_ARG;
-    if (t->dispatch_kernel < 0 || t->dispatch_kernel > 2) return EP_ERR_INVALID_ARG;
+    if (t->dispatch_kernel < 0 || t->dispatch_kernel > 3) return EP_ERR_INVALID_ARG;
     if (t->layout_form < 0 || t->layout_form > 2) return EP_ERR_INVALID_ARG;
     if (!on_ctx_device(ctx)) return EP_ERR_INVALID_ARG;
     ctx->tune = *t;
@@ -1358,6 +1371,7 @@ ep_status ep_autotune(ep_ctx *ctx, const void *d_x, const int64_t *d_topk_idx, i
         if (c.hidden % 512 == 0 && c.hidden <= 16384)
             for (int b = 1; b <= 4; ++b) cands.push_back({1, b});
         cands.push_back({2, 0});
+        if (ep::token_kernel_fits(c.hidden, fp8)) cands.push_back({3, 0});
         float best_us = 0.0f;
         for (size_t j = 0; s == EP_OK && j < cands.size(); ++j) {
             ep_tuning t = best;

@@ -92,10 +92,19 @@ struct DispatchParams {
                                // which started after x was written, so x may be read before
                                // griddepcontrol.wait; 0: wait first (x may come from the kernel
                                // just before)
+    int64_t token_grid;        // > 0: the token kernel (token_tpb tokens per CTA) on at most this
+                               // many CTAs; 0: the row or the warp-item kernel (row_sms)
+    int32_t token_tpb;         // tokens per CTA of the token kernel: 1 or 2
 };
 
 cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks,
                             bool pdl, cudaStream_t stream);
+// Whether the token kernel runs this hidden size (H % 16 == 0, H / 16 <= 1024;
+// FP8: H % 128 == 0).
+bool token_kernel_fits(int H, bool fp8);
+// The built-in rule's choice of the token kernel for N tokens of K entries
+// (large dispatches on all SMs).
+bool token_kernel_rule(int64_t N, int K, int H, bool fp8, bool sm_limited);
 // The row dispatch kernel's CTAs per SM by the built-in rule (from H and the payload).
 int dispatch_row_ctas_rule(int H, bool fp8);
 // Resident blocks per SM of the warp-item dispatch kernel (for grid sizing).

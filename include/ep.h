@@ -439,11 +439,17 @@ ep_status ep_round_trip_auto_chunk(const ep_ctx *ctx, int32_t use_fp8, int32_t r
  *                         ep_round_trip; 0 = the L2 rule; >= R*T (INT32_MAX
  *                         from ep_autotune) = one chunk
  *   dispatch_kernel       0 = the built-in rule (the warp-item kernel for FP8
- *                         rows of H <= 1024, or H <= 2048 with topk <= 4, else
- *                         the row kernel where it applies), 1 = the row kernel (bulk copies of whole
+ *                         rows of H <= 1024, or H <= 2048 with topk <= 4; else
+ *                         the token kernel from 64K receive rows (tokens x
+ *                         topk) on all SMs, except FP8 at topk <= 2; else the
+ *                         row kernel where it applies), 1 = the row kernel (bulk copies of whole
  *                         rows; only where H % 512 == 0 and H <= 15872, the
  *                         warp-item kernel elsewhere), 2 = the warp-item kernel
- *                         (16-byte stores by every lane)
+ *                         (16-byte stores by every lane), 3 = the token kernel
+ *                         (one CTA per token holding its row in registers,
+ *                         16-byte stores of the whole row per entry; where
+ *                         H % 16 == 0 (FP8: H % 128 == 0) and H <= 16384, the
+ *                         rule's kernel elsewhere)
  *   layout_form           0 = the built-in rule (one thread-block cluster below
  *                         a size, the grid form over all SMs from it), 1 = the
  *                         cluster, 2 = the grid form (one cooperative kernel;

@@ -172,17 +172,41 @@ DISPATCH_CASES = {
     # the largest hidden size (the warp-item kernel)
     "h65536_bf16": wl.TINY.with_(hidden=65536, tokens_per_rank=2, max_tokens_per_rank=2),
     "h65536_fp8": wl.TINY.with_(hidden=65536, tokens_per_rank=2, max_tokens_per_rank=2, use_fp8=True),
+    # from 64K receive rows the built-in rule takes the token kernel (one CTA per token)
+    "token_rule_bf16": wl.TINY.with_(num_ranks=8, tokens_per_rank=2048, max_tokens_per_rank=2048, topk=4,
+                                     layout=wl.PACKED),
+    "token_rule_fp8": wl.TINY.with_(num_ranks=8, tokens_per_rank=2000, max_tokens_per_rank=2048, hidden=2048,
+                                    num_experts=64, topk=6, use_fp8=True, x_scale="loguniform"),
 }
 
 
 @pytest.mark.parametrize("name", list(DISPATCH_CASES))
 @pytest.mark.parametrize("reuse", [False, True])
 def test_dispatch_parity(name, reuse):
-    w = DISPATCH_CASES[name]
+    _check_dispatch(DISPATCH_CASES[name], reuse)
+
+
+# the token kernel forced by the tuning on every shape it runs (and on two it
+# does not: H = 200 and 65536 fall back to the rule's kernel); H = 400 and 384
+# leave 7 / 8 threads of the CTA's last warp without channels
+TOKEN_CASES = ["tiny_bf16", "tiny_fp8", "ll_fp8", "ll_bf16", "skew_fp8", "ll_ragged_fp8", "h384_fp8", "h200_bf16",
+               "k32_fp8", "h16384_bf16", "h15872_fp8", "packed_fp8", "h65536_fp8", "h400_bf16"]
+
+
+@pytest.mark.parametrize("name", TOKEN_CASES)
+def test_token_kernel_parity(name):
+    w = DISPATCH_CASES.get(name) or {"h400_bf16": wl.TINY.with_(hidden=400)}[name]
+    _check_dispatch(w, False, kernel=3)
+    _check_dispatch(w, True, kernel=3, tokens_per_cta=2)
+
+
+def _check_dispatch(w, reuse, kernel=None, tokens_per_cta=0):
     d = wl.generate(w)
     idx, xb = d["topk_idx"], d["x_bits"]
     o = _orc_layout(w, idx)
     buf = make_buffer(w)
+    if kernel is not None:
+        ep.ep_set_tuning(buf.ctx, ep.ep_tuning(tokens_per_cta, 0, 0, kernel))
     x = bits_to_bf16(xb)
     idx_d = torch.from_numpy(idx).cuda()
     recv, scales = _sentinel_recv(buf, w.use_fp8)

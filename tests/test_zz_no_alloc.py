@@ -151,10 +151,13 @@ def test_noalloc_repeated_calls_leave_free_memory_unchanged():
     sc = torch.empty(rows, w.hidden // 128, dtype=torch.float32, device="cuda")
     cnt = torch.empty(w.num_experts, dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     free0, _ = torch.cuda.mem_get_info()
     alloc0 = torch.cuda.memory_allocated()
     for _ in range(3):
         ep.ep_dispatch_noalloc(cfg, x, idx, w.tokens_per_rank, True, recv, sc, cnt)
     torch.cuda.synchronize()
-    assert torch.cuda.mem_get_info()[0] == free0
+    # free device memory never drops (it can rise when the driver returns
+    # memory that an earlier test released: once by 2 MiB after other tests)
+    assert torch.cuda.mem_get_info()[0] >= free0
     assert torch.cuda.memory_allocated() == alloc0
