@@ -11,6 +11,8 @@ than it holds), with nothing written past the oracle's rows; and repeated
 calls must not change the device's free memory.
 
 Kept in a file of its own that pytest collects last."""
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -150,6 +152,7 @@ def test_noalloc_repeated_calls_leave_free_memory_unchanged():
     recv = torch.empty(rows, w.hidden, dtype=torch.float8_e4m3fn, device="cuda")
     sc = torch.empty(rows, w.hidden // 128, dtype=torch.float32, device="cuda")
     cnt = torch.empty(w.num_experts, dtype=torch.int32, device="cuda")
+    gc.collect()  # tensors of earlier tests that only a collection frees
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     free0, _ = torch.cuda.mem_get_info()
@@ -157,7 +160,8 @@ def test_noalloc_repeated_calls_leave_free_memory_unchanged():
     for _ in range(3):
         ep.ep_dispatch_noalloc(cfg, x, idx, w.tokens_per_rank, True, recv, sc, cnt)
     torch.cuda.synchronize()
-    # free device memory never drops (it can rise when the driver returns
-    # memory that an earlier test released: once by 2 MiB after other tests)
+    # neither the device's free memory nor torch's allocated memory grows
+    # (either can shrink when something an earlier test left is released
+    # meanwhile: seen once each, by 2 MiB and by 1.5 KB, after other tests)
     assert torch.cuda.mem_get_info()[0] >= free0
-    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.memory_allocated() <= alloc0
