@@ -983,9 +983,10 @@ def run_sweep(args):
 
 def run_kernels(args):
     """The dispatch of the workload with each kernel (ep_tuning.dispatch_kernel
-    0 = the rule's choice, 1 = row, 2 = warp-item, 3 = token): median µs of
-    20 runs on the cached layout and behind the layout kernel, L2 flushed
-    before each, and the cached time's fraction of the HBM peak."""
+    0 = the rule's choice, 1 = row, 2 = warp-item, 3 = token with 1 and 2
+    tokens per CTA): median µs of 20 runs on the cached layout and behind the
+    layout kernel (with --rank: the rank layout), L2 flushed before each, and
+    the cached time's fraction of the HBM peak."""
     import torch
     from combine_get_dispatch_02_gb300 import Buffer, ep
     from combine_get_dispatch_02_gb300 import build as epbuild
@@ -1005,10 +1006,20 @@ def run_kernels(args):
     N, K, H = w.num_tokens, w.topk, w.hidden
     x = torch.from_numpy(np.ascontiguousarray(d["x_bits"]).view(np.int16)).cuda().view(torch.bfloat16)
     idx = torch.from_numpy(d["topk_idx"]).cuda()
+    wts = torch.from_numpy(d["topk_weights"].reshape(N, K)).cuda()
     buf = Buffer(w.num_ranks, w.max_tokens_per_rank, H, w.num_experts, K, low_latency_mode=(w.layout == wl.PADDED))
-    recv, scales = buf.alloc_recv(w.use_fp8)
+    recv, scales = buf.alloc_rank_recv(w.use_fp8) if args.rank else buf.alloc_recv(w.use_fp8)
     h = buf.new_handle()
     ctx = buf.ctx
+    T = w.tokens_per_rank
+
+    def with_layout():
+        if args.rank:  # the rank layout, then the dispatch on it
+            ep.ep_get_rank_layout(ctx, idx, wts, T, None, None, None, h.raw, stream)
+            ep.ep_dispatch(ctx, x, None, T, w.use_fp8, h.raw, recv, scales, None, stream)
+        else:
+            ep.ep_dispatch(ctx, x, idx, T, w.use_fp8, h.raw, recv, scales, None, stream)
+
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     flush_w = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
     flush_r = torch.ones(2 * l2 // 4, dtype=torch.float32, device="cuda")
@@ -1029,24 +1040,24 @@ def run_kernels(args):
         torch.cuda.synchronize()
         return statistics.median([a.elapsed_time(b) * 1e3 for a, b in ts])
 
-    ep.ep_dispatch(ctx, x, idx, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales, None, stream)
+    with_layout()
     M = int((h.tensors()["slot"] >= 0).sum().item())
     _, disp_bytes, _ = _algorithmic_bytes(w, M)
     res = {}
-    for kern, name in ((0, "rule"), (1, "row"), (2, "warp_item"), (3, "token")):
+    for kern, per, name in ((0, 0, "rule"), (1, 0, "row"), (2, 0, "warp_item"), (3, 0, "token"),
+                            (3, 2, "token_2_per_cta")):
         t = ep.ep_get_tuning(ctx)
         t.dispatch_kernel = kern
-        t.dispatch_ctas_per_sm = 0
+        t.dispatch_ctas_per_sm = per
         ep.ep_set_tuning(ctx, t)
-        cached = timed(lambda: ep.ep_dispatch(ctx, x, None, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales,
-                                              None, stream))
-        fresh = timed(lambda: ep.ep_dispatch(ctx, x, idx, w.tokens_per_rank, w.use_fp8, h.raw, recv, scales,
-                                             None, stream))
+        cached = timed(lambda: ep.ep_dispatch(ctx, x, None, T, w.use_fp8, h.raw, recv, scales, None, stream))
+        fresh = timed(with_layout)
         res[name] = {"cached_us": round(cached, 1), "with_layout_us": round(fresh, 1),
                      "cached_frac": round(disp_bytes / (cached / 1e6) / 1e9 / peak, 3)}
     if buf.device_status() != ep.EP_OK:
         raise RuntimeError("device status error")
-    print(json.dumps({"workload": _workload_desc(w), "rows": M, "dispatch_bytes": disp_bytes,
+    print(json.dumps({"workload": _workload_desc(w) + (", rank-deduplicated" if args.rank else ""),
+                      "rows": M, "dispatch_bytes": disp_bytes,
                       "peak_gbs": peak, "peak_source": peak_kind, "kernels": res}), flush=True)
 
 

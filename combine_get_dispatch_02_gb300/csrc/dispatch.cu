@@ -295,8 +295,13 @@ __global__ void __launch_bounds__(1024, 1) dispatch_token_kernel(const DispatchP
             a[u] = make_uint4(0, 0, 0, 0);
             b[u] = a[u];
             if (act && g0 + u < p.N) {
-                a[u] = ld_nc_na_v4(x + (g0 + u) * nv + i0);
-                b[u] = ld_nc_na_v4(x + (g0 + u) * nv + i1);
+                if constexpr (FP8) {  // 32 contiguous bytes per thread: the second load hits L1
+                    a[u] = __ldg(x + (g0 + u) * nv + i0);
+                    b[u] = __ldg(x + (g0 + u) * nv + i1);
+                } else {  // each load instruction of a warp reads 512 contiguous bytes
+                    a[u] = ld_nc_na_v4(x + (g0 + u) * nv + i0);
+                    b[u] = ld_nc_na_v4(x + (g0 + u) * nv + i1);
+                }
             }
         }
 #pragma unroll
