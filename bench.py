@@ -983,10 +983,10 @@ def run_sweep(args):
 
 def run_kernels(args):
     """The dispatch of the workload with each kernel (ep_tuning.dispatch_kernel
-    0 = the rule's choice, 1 = row, 2 = warp-item, 3 = token with 1 and 2
-    tokens per CTA): median µs of 20 runs on the cached layout and behind the
-    layout kernel (with --rank: the rank layout), L2 flushed before each, and
-    the cached time's fraction of the HBM peak."""
+    0 = the rule's choice, 1 = row, 2 = warp-item, 3 = token): median µs of
+    20 runs on the cached layout and behind the layout kernel (with --rank:
+    the rank layout), L2 flushed before each, and the cached time's fraction
+    of the HBM peak."""
     import torch
     from combine_get_dispatch_02_gb300 import Buffer, ep
     from combine_get_dispatch_02_gb300 import build as epbuild
@@ -1044,8 +1044,7 @@ def run_kernels(args):
     M = int((h.tensors()["slot"] >= 0).sum().item())
     _, disp_bytes, _ = _algorithmic_bytes(w, M)
     res = {}
-    for kern, per, name in ((0, 0, "rule"), (1, 0, "row"), (2, 0, "warp_item"), (3, 0, "token"),
-                            (3, 2, "token_2_per_cta")):
+    for kern, per, name in ((0, 0, "rule"), (1, 0, "row"), (2, 0, "warp_item"), (3, 0, "token")):
         t = ep.ep_get_tuning(ctx)
         t.dispatch_kernel = kern
         t.dispatch_ctas_per_sm = per

@@ -256,20 +256,19 @@ __device__ __forceinline__ void put_row(uint8_t *row, int t, int H, uint4 ca, ui
 }
 
 // ---------------------------------------------------------------- token kernel
-// TPB tokens per CTA, a short-lived grid of N / TPB CTAs (or a persistent
-// grid looping over the tokens when the SMs are limited).  H/16 threads: for
-// FP8 thread t holds channels [16t, 16t + 16) (two 16-byte loads) and casts
-// them once (8 threads per 128-channel block, the amax by three xor
-// shuffles); for BF16 thread t holds the row's 16-byte vectors t and
-// t + H/16, so every store instruction of a warp writes 512 contiguous
-// bytes.  All TPB rows are loaded before the first is stored (more reads in
-// flight per CTA); each row then goes to the receive row of every top-k
-// entry with plain 16-byte stores, one contiguous row written by the whole
-// CTA within a few store instructions per warp.  Every CTA lets the next
-// kernel launch as it starts (the dependents start once the last CTA has
-// started); x may be read before the slots are waited for behind this
-// library's own layout kernel (early_x).
-template <bool FP8, int TPB>
+// One CTA per token, a short-lived grid of N CTAs (or a persistent grid
+// looping over the tokens when the SMs are limited).  H/16 threads: for FP8
+// thread t holds channels [16t, 16t + 16) (two 16-byte loads) and casts them
+// once (8 threads per 128-channel block, the amax by three xor shuffles);
+// for BF16 thread t holds the row's 16-byte vectors t and t + H/16, so
+// every store instruction of a warp writes 512 contiguous bytes.  The row
+// then goes to the receive row of every top-k entry with plain 16-byte
+// stores, one contiguous row written by the whole CTA within a few store
+// instructions per warp.  Every CTA lets the next kernel launch as it
+// starts (the dependents start once the last CTA has started); x may be
+// read before the slots are waited for behind this library's own layout
+// kernel (early_x).
+template <bool FP8>
 __global__ void __launch_bounds__(1024, 1) dispatch_token_kernel(const DispatchParams p) {
     pdl_launch_dependents();
     const int H = p.H, K = p.K, nt = H / 16;
@@ -288,46 +287,36 @@ __global__ void __launch_bounds__(1024, 1) dispatch_token_kernel(const DispatchP
     const uint4 *x = static_cast<const uint4 *>(p.x);  // H / 8 vectors per row
     const int64_t nv = H / 8;
     const int i0 = FP8 ? 2 * t : t, i1 = FP8 ? 2 * t + 1 : t + nt;
-    for (int64_t g0 = (int64_t)blockIdx.x * TPB; g0 < p.N; g0 += (int64_t)gridDim.x * TPB) {
-        uint4 a[TPB], b[TPB];
-#pragma unroll
-        for (int u = 0; u < TPB; ++u) {
-            a[u] = make_uint4(0, 0, 0, 0);
-            b[u] = a[u];
-            if (act && g0 + u < p.N) {
-                if constexpr (FP8) {  // 32 contiguous bytes per thread: the second load hits L1
-                    a[u] = __ldg(x + (g0 + u) * nv + i0);
-                    b[u] = __ldg(x + (g0 + u) * nv + i1);
-                } else {  // each load instruction of a warp reads 512 contiguous bytes
-                    a[u] = ld_nc_na_v4(x + (g0 + u) * nv + i0);
-                    b[u] = ld_nc_na_v4(x + (g0 + u) * nv + i1);
-                }
+    for (int64_t g = blockIdx.x; g < p.N; g += gridDim.x) {
+        uint4 a = make_uint4(0, 0, 0, 0), b = a;
+        if (act) {
+            if constexpr (FP8) {  // 32 contiguous bytes per thread: the second load hits L1
+                a = __ldg(x + g * nv + i0);
+                b = __ldg(x + g * nv + i1);
+            } else {  // each load instruction of a warp reads 512 contiguous bytes
+                a = ld_nc_na_v4(x + g * nv + i0);
+                b = ld_nc_na_v4(x + g * nv + i1);
             }
         }
-#pragma unroll
-        for (int u = 0; u < TPB; ++u) {
-            const int64_t g = g0 + u;
-            if (g >= p.N) break;  // block-uniform
-            uint4 q = make_uint4(0, 0, 0, 0);
-            float scale = 0.0f;
-            if constexpr (FP8) cast16(a[u], b[u], q, scale);
-            if (!waited) {
-                pdl_wait();  // the slots of the layout kernel
-                waited = true;
-            }
-            const int32_t my_slot = slot_of(p, g, lane);
-            for (int k = 0; k < K; ++k) {
-                const int32_t s = __shfl_sync(0xFFFFFFFFu, my_slot, k);
-                if (s < 0 || !act) continue;
-                if constexpr (FP8) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.recv) + (int64_t)s * H);
-                    dst[t] = q;
-                    if ((t & 7) == 0) p.recv_scales[(int64_t)s * (H / 128) + (t >> 3)] = scale;
-                } else {
-                    uint4 *dst = static_cast<uint4 *>(p.recv) + (int64_t)s * nv;
-                    dst[i0] = a[u];
-                    dst[i1] = b[u];
-                }
+        uint4 q = make_uint4(0, 0, 0, 0);
+        float scale = 0.0f;
+        if constexpr (FP8) cast16(a, b, q, scale);
+        if (!waited) {
+            pdl_wait();  // the slots of the layout kernel
+            waited = true;
+        }
+        const int32_t my_slot = slot_of(p, g, lane);
+        for (int k = 0; k < K; ++k) {
+            const int32_t s = __shfl_sync(0xFFFFFFFFu, my_slot, k);
+            if (s < 0 || !act) continue;
+            if constexpr (FP8) {
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.recv) + (int64_t)s * H);
+                dst[t] = q;
+                if ((t & 7) == 0) p.recv_scales[(int64_t)s * (H / 128) + (t >> 3)] = scale;
+            } else {
+                uint4 *dst = static_cast<uint4 *>(p.recv) + (int64_t)s * nv;
+                dst[i0] = a;
+                dst[i1] = b;
             }
         }
     }
@@ -549,9 +538,7 @@ cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks, b
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     if (p.token_grid > 0 && token_kernel_fits(p.H, fp8)) {
-        const int tpb = p.token_tpb >= 2 ? 2 : 1;
-        const int64_t need = (p.N + tpb - 1) / tpb;
-        int64_t blocks = need < p.token_grid ? need : p.token_grid;
+        int64_t blocks = p.N < p.token_grid ? p.N : p.token_grid;
         if (blocks < 1) blocks = 1;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)blocks, 1, 1);
@@ -560,11 +547,8 @@ cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks, b
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = pdl ? 1 : 0;
-        if (p.token_tpb >= 2)
-            return fp8 ? cudaLaunchKernelEx(&cfg, dispatch_token_kernel<true, 2>, p)
-                       : cudaLaunchKernelEx(&cfg, dispatch_token_kernel<false, 2>, p);
-        return fp8 ? cudaLaunchKernelEx(&cfg, dispatch_token_kernel<true, 1>, p)
-                   : cudaLaunchKernelEx(&cfg, dispatch_token_kernel<false, 1>, p);
+        return fp8 ? cudaLaunchKernelEx(&cfg, dispatch_token_kernel<true>, p)
+                   : cudaLaunchKernelEx(&cfg, dispatch_token_kernel<false>, p);
     }
     if (row_kernel_fits(p.H) && p.row_sms > 0) {
         const int bps = p.row_bps > 0 ? p.row_bps : row_blocks_per_sm(p.H, fp8);

@@ -240,7 +240,6 @@ ep_status enqueue_dispatch(ep_ctx *ctx, const ep_handle *h, const void *x, int64
     if (kern == 2 || (kern == 0 && short_fp8)) p.row_sms = 0;
     p.row_bps = ctx->tune.dispatch_ctas_per_sm;
     p.token_grid = 0;
-    p.token_tpb = ctx->tune.dispatch_ctas_per_sm >= 2 ? 2 : 1;
     // the token kernel when tuned so, and by the rule for large dispatches
     // on all SMs (from 64K receive rows; not FP8 at top-1/2)
     const bool limited = p.row_sms < ctx->num_sms;

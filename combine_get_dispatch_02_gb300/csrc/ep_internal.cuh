@@ -92,9 +92,8 @@ struct DispatchParams {
                                // which started after x was written, so x may be read before
                                // griddepcontrol.wait; 0: wait first (x may come from the kernel
                                // just before)
-    int64_t token_grid;        // > 0: the token kernel (token_tpb tokens per CTA) on at most this
-                               // many CTAs; 0: the row or the warp-item kernel (row_sms)
-    int32_t token_tpb;         // tokens per CTA of the token kernel: 1 or 2
+    int64_t token_grid;        // > 0: the token kernel (one CTA per token) on at most this many
+                               // CTAs; 0: the row or the warp-item kernel (row_sms)
 };
 
 cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks,

@@ -179,7 +179,6 @@ extern "C" ep_status ep_dispatch_noalloc(const ep_config *cfg, const void *d_x, 
     dp.status = status;
     dp.early_x = 1;  // behind the layout kernel
     dp.token_grid = 0;  // the token kernel by the rule of ep_dispatch (large dispatches on all SMs)
-    dp.token_tpb = 1;
     if (!short_fp8 && ep::token_kernel_rule(N, c.topk, c.hidden, use_fp8 != 0, sms < s.num_sms)) dp.token_grid = N;
     const int cap = sms * (use_fp8 ? s.bps_fp8 : s.bps_bf16);
     const cudaError_t de = ep::launch_dispatch(dp, use_fp8 != 0, cap, /*pdl=*/true, st);

@@ -197,16 +197,16 @@ TOKEN_CASES = ["tiny_bf16", "tiny_fp8", "ll_fp8", "ll_bf16", "skew_fp8", "ll_rag
 def test_token_kernel_parity(name):
     w = DISPATCH_CASES.get(name) or {"h400_bf16": wl.TINY.with_(hidden=400)}[name]
     _check_dispatch(w, False, kernel=3)
-    _check_dispatch(w, True, kernel=3, tokens_per_cta=2)
+    _check_dispatch(w, True, kernel=3)
 
 
-def _check_dispatch(w, reuse, kernel=None, tokens_per_cta=0):
+def _check_dispatch(w, reuse, kernel=None):
     d = wl.generate(w)
     idx, xb = d["topk_idx"], d["x_bits"]
     o = _orc_layout(w, idx)
     buf = make_buffer(w)
     if kernel is not None:
-        ep.ep_set_tuning(buf.ctx, ep.ep_tuning(tokens_per_cta, 0, 0, kernel))
+        ep.ep_set_tuning(buf.ctx, ep.ep_tuning(0, 0, 0, kernel))
     x = bits_to_bf16(xb)
     idx_d = torch.from_numpy(idx).cuda()
     recv, scales = _sentinel_recv(buf, w.use_fp8)

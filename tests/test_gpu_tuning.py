@@ -69,8 +69,8 @@ def test_every_launch_shape_gives_the_same_bits(name):
         assert np.array_equal(bf16_to_bits(ref[2]),
                               oracle.combine(y_rows, slot_c.reshape(sl.shape),
                                              d["topk_weights"].reshape(w.num_tokens, w.topk)))
-    # + the warp-item kernel and the token kernel (1 and 2 tokens per CTA)
-    shapes = [(bps, cpi, 0) for bps in (1, 2, 3, 4) for cpi in (1, 2, 4)] + [(0, 0, 2), (0, 0, 3), (2, 0, 3)]
+    # + the warp-item kernel and the token kernel
+    shapes = [(bps, cpi, 0) for bps in (1, 2, 3, 4) for cpi in (1, 2, 4)] + [(0, 0, 2), (0, 0, 3)]
     for bps, cpi, kern in shapes:
         ep.ep_set_tuning(buf.ctx, ep.ep_tuning(bps, cpi, 0, kern))
         got = _run(buf, w, x, idx_d, wts_d, y, rank)
