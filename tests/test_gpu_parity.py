@@ -200,11 +200,17 @@ def test_token_kernel_parity(name):
     _check_dispatch(w, True, kernel=3)
 
 
-def _check_dispatch(w, reuse, kernel=None):
+@pytest.mark.parametrize("name", ["ll_fp8", "ll_bf16", "ll_ragged_fp8"])
+def test_token_kernel_sm_budget(name):
+    # on an SM budget the token kernel runs a persistent grid that loops over the tokens
+    _check_dispatch(DISPATCH_CASES[name], False, kernel=3, max_sms=5)
+
+
+def _check_dispatch(w, reuse, kernel=None, max_sms=0):
     d = wl.generate(w)
     idx, xb = d["topk_idx"], d["x_bits"]
     o = _orc_layout(w, idx)
-    buf = make_buffer(w)
+    buf = make_buffer(w, max_sms=max_sms)
     if kernel is not None:
         ep.ep_set_tuning(buf.ctx, ep.ep_tuning(0, 0, 0, kernel))
     x = bits_to_bf16(xb)
