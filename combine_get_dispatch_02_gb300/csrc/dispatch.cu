@@ -268,8 +268,8 @@ __device__ __forceinline__ void put_row(uint8_t *row, int t, int H, uint4 ca, ui
 // starts (the dependents start once the last CTA has started); x may be
 // read before the slots are waited for behind this library's own layout
 // kernel (early_x).
-template <bool FP8>
-__global__ void __launch_bounds__(1024, 1) dispatch_token_kernel(const DispatchParams p) {
+template <bool FP8, int MINB>
+__global__ void __launch_bounds__(MINB == 4 ? 512 : 1024, MINB) dispatch_token_kernel(const DispatchParams p) {
     pdl_launch_dependents();
     const int H = p.H, K = p.K, nt = H / 16;
     const int t = threadIdx.x, lane = t & 31;
@@ -547,8 +547,10 @@ cudaError_t launch_dispatch(const DispatchParams &p, bool fp8, int max_blocks, b
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = pdl ? 1 : 0;
-        return fp8 ? cudaLaunchKernelEx(&cfg, dispatch_token_kernel<true>, p)
-                   : cudaLaunchKernelEx(&cfg, dispatch_token_kernel<false>, p);
+        // FP8 rows of up to 512 threads: registers for 4 CTAs per SM (3 otherwise)
+        if (fp8 && cfg.blockDim.x <= 512) return cudaLaunchKernelEx(&cfg, dispatch_token_kernel<true, 4>, p);
+        return fp8 ? cudaLaunchKernelEx(&cfg, dispatch_token_kernel<true, 1>, p)
+                   : cudaLaunchKernelEx(&cfg, dispatch_token_kernel<false, 1>, p);
     }
     if (row_kernel_fits(p.H) && p.row_sms > 0) {
         const int bps = p.row_bps > 0 ? p.row_bps : row_blocks_per_sm(p.H, fp8);
