@@ -426,13 +426,12 @@ bool token_kernel_fits(int H, bool fp8) { return H % (fp8 ? 128 : 16) == 0 && H 
 
 // Measured over the sweep grid (T >= 32 tokens per rank, R in {8, 32}, H in
 // {2048, 4096, 7168}, top-2/6/8, BF16 and FP8, cached layout): from 64K
-// receive rows the token kernel takes 0.88-0.94 of the row kernel's time,
-// except FP8 at top-2 (1.06-1.17: a 7 KB row written twice per 14 KB read,
-// where the row kernel's reads two tokens ahead matter more); at 32K rows and
-// below it ties or loses (the low-latency size, where the row kernel's ring
-// also overlaps more of the layout kernel before it).
+// receive rows the token kernel takes 0.79-0.98 of the row kernel's time
+// (FP8 at top-2 and H = 7168: 1.00-1.02); at 32K rows and below it ties or
+// loses (the low-latency size, where the row kernel's ring also overlaps
+// more of the layout kernel before it).
 bool token_kernel_rule(int64_t N, int K, int H, bool fp8, bool sm_limited) {
-    return !sm_limited && token_kernel_fits(H, fp8) && N * K >= 65536 && !(fp8 && K <= 2);
+    return !sm_limited && token_kernel_fits(H, fp8) && N * K >= 65536;
 }
 
 namespace {

@@ -241,7 +241,7 @@ ep_status enqueue_dispatch(ep_ctx *ctx, const ep_handle *h, const void *x, int64
     p.row_bps = ctx->tune.dispatch_ctas_per_sm;
     p.token_grid = 0;
     // the token kernel when tuned so, and by the rule for large dispatches
-    // on all SMs (from 64K receive rows; not FP8 at top-1/2)
+    // on all SMs (from 64K receive rows)
     const bool limited = p.row_sms < ctx->num_sms;
     const bool token = kern == 3 || (kern == 0 && !short_fp8 && ep::token_kernel_rule(p.N, p.K, c.hidden, fp8, limited));
     if (token && ep::token_kernel_fits(c.hidden, fp8)) {

@@ -441,8 +441,8 @@ ep_status ep_round_trip_auto_chunk(const ep_ctx *ctx, int32_t use_fp8, int32_t r
  *   dispatch_kernel       0 = the built-in rule (the warp-item kernel for FP8
  *                         rows of H <= 1024, or H <= 2048 with topk <= 4; else
  *                         the token kernel from 64K receive rows (tokens x
- *                         topk) on all SMs, except FP8 at topk <= 2; else the
- *                         row kernel where it applies), 1 = the row kernel (bulk copies of whole
+ *                         topk) on all SMs; else the row kernel where it
+ *                         applies), 1 = the row kernel (bulk copies of whole
  *                         rows; only where H % 512 == 0 and H <= 15872, the
  *                         warp-item kernel elsewhere), 2 = the warp-item kernel
  *                         (16-byte stores by every lane), 3 = the token kernel

@@ -177,6 +177,8 @@ DISPATCH_CASES = {
                                      layout=wl.PACKED),
     "token_rule_fp8": wl.TINY.with_(num_ranks=8, tokens_per_rank=2000, max_tokens_per_rank=2048, hidden=2048,
                                     num_experts=64, topk=6, use_fp8=True, x_scale="loguniform"),
+    "token_rule_fp8_k2": wl.TINY.with_(num_ranks=8, tokens_per_rank=4096, max_tokens_per_rank=4096, hidden=2560,
+                                       num_experts=64, topk=2, use_fp8=True, layout=wl.PACKED),
 }
 
 
