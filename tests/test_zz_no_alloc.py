@@ -61,7 +61,10 @@ def _noalloc(w, x, idx):
 
 
 def test_noalloc_dispatch_matches_dispatch_on_two_calls():
-    cases = [wl.LL, wl.SKEW.with_(layout=wl.PACKED, use_fp8=False)]
+    # at the size limit (65536 entries) the built-in rule takes the token kernel
+    cases = [wl.LL, wl.SKEW.with_(layout=wl.PACKED, use_fp8=False),
+             wl.LL.with_(tokens_per_rank=256, max_tokens_per_rank=256, layout=wl.PACKED),
+             wl.TINY.with_(num_ranks=8, tokens_per_rank=2048, max_tokens_per_rank=2048, layout=wl.PACKED)]
     for w in cases:
         d = wl.generate(w)
         x = bits_to_bf16(d["x_bits"])
