@@ -76,9 +76,11 @@ def test_fp8_hidden_not_multiple_of_128_is_unsupported():
     assert e.value.status == ep.EP_ERR_UNSUPPORTED
 
 
-def test_cuda_graph_replay_matches_eager():
+@pytest.mark.parametrize("kernel", [0, 3])  # the rule's (row) kernel, the token kernel
+def test_cuda_graph_replay_matches_eager(kernel):
     w = wl.LL
     buf = make_buffer(w)
+    ep.ep_set_tuning(buf.ctx, ep.ep_tuning(0, 0, 0, kernel))
     x, idx, wts, _ = _inputs(w)
     h = buf.new_handle()
     recv, sc = buf.alloc_recv(True)
