@@ -1,7 +1,8 @@
 """GPU parity over seeded random shapes: rank counts and experts per rank that
 are not powers of two (3, 5, 6 ranks; 3 or 5 experts per rank), hidden sizes
-that are any multiple of 8 (BF16) or of 128 (FP8) up to 2048 (so both
-dispatch kernels run at odd sizes), T anywhere in
+that are any multiple of 8 (BF16) or of 128 (FP8) up to 2048 (so the row and
+warp-item dispatch kernels run at odd sizes, and the token kernel, forced on
+the cached layout, too), T anywhere in
 [0, Tmax], top-k up to 12 (also above E, with repeated experts), masked
 entries, both layouts and padded overflow.  Each case runs the fresh dispatch
 (layout inside), the explicit layout and the combine through the C ABI and
@@ -99,6 +100,22 @@ def test_random_shape_parity(i):
     rest = torch.ones(recv.shape[0], dtype=torch.bool, device="cuda")
     rest[rows_d] = False
     assert bool((recv.view(torch.uint8)[rest] == 0xA5).all().item())
+
+    # the same rows from the token kernel on the cached layout (where H suits it:
+    # a multiple of 16, FP8 of 128; the rule's kernel elsewhere)
+    ep.ep_set_tuning(buf.ctx, ep.ep_tuning(0, 0, 0, 3))
+    recv.view(torch.uint8).fill_(0xA5)
+    if fp8:
+        scales.fill_(-3.0)
+    buf.low_latency_dispatch(x, None, Tmax, E, use_fp8=fp8, handle=h, out=(recv, scales))
+    assert buf.device_status() == ep.EP_OK  # (a capacity overflow is the layout's to report)
+    if fp8:
+        assert np.array_equal(e4m3_to_bits(recv.view(torch.uint8)[rows_d]), q[g_of])
+        assert np.array_equal(scales[rows_d].cpu().numpy().view(np.uint32), s[g_of].view(np.uint32))
+    else:
+        assert np.array_equal(bf16_to_bits(recv[rows_d]), xb[g_of])
+    assert bool((recv.view(torch.uint8)[rest] == 0xA5).all().item())
+    ep.ep_set_tuning(buf.ctx, ep.ep_tuning())
 
     # explicit layout: every array of it
     ntr, nte, itr, h2 = buf.get_dispatch_layout(idx_d)
